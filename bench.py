@@ -1,0 +1,372 @@
+#!/usr/bin/env python3
+"""MLA decode benchmark on GB300: one decode step of the DeepSeek-V3-shaped
+workload (batch 32, q_len 1, 128 heads, d_c 512 + d_R 64, 4096 cached tokens per
+sequence, bf16 paged cache, page size 64, shuffled pages) through the C ABI.
+
+A step = append of the step's new tokens + absorb_q + paged decode (+ split
+combine) + out_proj. The latent cache (151 MB) is larger than L2, and L2 is
+additionally flushed (a 256 MiB write) before every timed step, outside the
+per-step CUDA-event window.
+
+Prints ONE JSON line (rank 0). --impl reference times the fp64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode latent-cache GB/s & tokens/s at 1 GB300; % of HBM roofline"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "dsv3_bf16"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def decode_bytes(w) -> int:
+    """Algorithmic bytes of one mla_decode_paged call: every visible cached row
+    once per sequence (shared by its q_len queries), the queries, u and lse."""
+    rows = sum(int(L) for L in w.seq_lens)
+    act = 4 if w.act_dtype == "f32" else 2
+    q = w.batch * w.q_len * w.heads * (512 + 64) * act
+    out = w.batch * w.q_len * w.heads * (512 * act + 4)
+    return rows * w.row_bytes() + q + out
+
+
+def recorded_traffic(kernel_src: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel; else None."""
+    prof = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    try:
+        txt = open(prof).read()
+        src = open(kernel_src, "rb").read()
+    except OSError:
+        return None
+    h = hashlib.sha256(src).hexdigest()[:16]
+    m_h = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", txt)
+    m_t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if m_h and m_t and m_h.group(1) == h:
+        return float(m_t.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev: int):
+        self.dev = dev
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.dev)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_run(w, d, seconds: float):
+    """Time the fp64 oracle (non-absorbed form, one head at a time) on a bounded
+    sample of the workload: whole sequences with all heads, in order, until
+    `seconds` of oracle work are done (the last sequence may stop part-way
+    through its heads). Building the oracle's cache is set-up, not timed.
+    Returns (GB/s of cache rows processed, sample description, threads, seconds)."""
+    import numpy as np
+    from oracle import mla_oracle as O
+    from oracle.harness import f64, oracle_pool, seq_token_mask
+
+    threads = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            threads = max(i.get("num_threads", 1) for i in info)
+    except Exception:
+        pass
+    q_nope, q_rope, w_uk, w_uv = f64(d["q_nope"]), f64(d["q_rope"]), f64(d["w_uk"]), f64(d["w_uv"])
+    bt = d["block_table"].numpy()
+    H = w.heads
+    elapsed, done_bytes, seqs, partial = 0.0, 0.0, 0, None
+    for b in range(w.batch):
+        pool, sc = oracle_pool(w, d, token_mask=seq_token_mask(w, [b]))
+        L = int(w.seq_lens[b])
+        t0 = time.perf_counter()
+        rows = O.gather_rows(pool, sc, bt[b], L, w.page_size, w.cache_dtype)
+        hd = 0
+        for h in range(H):
+            for j in range(w.q_len):
+                T = O.visible_tokens(L, w.q_len, j)
+                O.attend_nonabsorbed(q_nope[b, j, h:h + 1], q_rope[b, j, h:h + 1], w_uk[h:h + 1],
+                                     w_uv[h:h + 1], rows[:T], O.default_scale())
+            hd += 1
+            if elapsed + time.perf_counter() - t0 > seconds:
+                break
+        elapsed += time.perf_counter() - t0
+        done_bytes += L * w.row_bytes() * hd / H
+        seqs += 1
+        if hd < H:
+            partial = hd
+            break
+        if elapsed > seconds:
+            break
+    last = f"the last with {partial}/{H} heads" if partial else "all heads"
+    sample = f"{seqs} sequence(s) of {w.name} ({last}); non-absorbed fp64 oracle, one head at a time"
+    return done_bytes / elapsed / 1e9, sample, threads, elapsed
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from mla_latent_kv_16_gb300 import build as B
+    if rank == 0 or world == 1:
+        B.build()
+    if world > 1:
+        dist.barrier()
+    from mla_latent_kv_16_gb300 import capi, workloads as W
+    from mla_latent_kv_16_gb300.engine import build_layer, step_inputs
+    capi.load()
+
+    w = W.preset(args.workload)
+    d = W.make_inputs(w)
+    layer = build_layer(w, d)
+    s = step_inputs(d)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0, "device error while filling the cache"
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        layer.append(s["new_c_kv"], s["new_k_r"], s["new_positions"], s["new_slots"])
+        q_lat = layer.absorb(s["q_nope"])
+        ev_d0.record(stream)
+        u, _ = layer.decode(q_lat, s["q_rope"])
+        ev_d1.record(stream)
+        layer.out_proj(u)
+
+    ev_d0 = torch.cuda.Event(enable_timing=True)
+    ev_d1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        one_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        e_s, d0, d1, e_e = ev[i]
+        e_s.record(stream)
+        ev_d0, ev_d1 = d0, d1
+        one_step()
+        e_e.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, _, _, b in ev]
+    dec_ms = [a.elapsed_time(b) for _, a, b, _ in ev]
+    tot = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([tot], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot = float(t.item())
+    assert layer.device_error() == 0
+
+    # end to end through the public API with pinned host buffers
+    host_in = {k: v.cpu().pin_memory() for k, v in s.items()}
+    host_out = torch.empty(layer.o.shape, dtype=layer.o.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    dev_in = {k: torch.empty_like(v) for k, v in s.items()}
+
+    def e2e_step():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        o = layer.step(**dev_in)
+        host_out.copy_(o, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_tot = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_tot], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_tot = float(t.item())
+
+    cache_bytes = sum(int(L) for L in w.seq_lens) * w.row_bytes()
+    ms = tot / args.steps
+    gbs = world * cache_bytes / (ms * 1e-3) / 1e9
+    tok_s = world * w.batch * w.q_len / (ms * 1e-3)
+    e2e_msps = e2e_tot / args.steps
+    dec = statistics.mean(dec_ms)
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = decode_bytes(w) / (dec * 1e-3) / 1e9
+    kernel_src = os.path.join(ROOT, "mla_latent_kv_16_gb300", "csrc",
+                              "decode_tc.cu" if (w.heads == 128 and w.act_dtype == "bf16") else "decode_simt.cu")
+    traffic = recorded_traffic(kernel_src, w.name)
+    splits = layer.splits
+    launches_per_step = 4 + (1 if splits > 1 else 0)
+    out = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.cache_dtype, "data": "synthetic (seeded N(0,1) values, N(0,1/sqrt(512)) weights)",
+        "config": {"workload": w.name, "batch": w.batch, "q_len": w.q_len, "heads": w.heads,
+                   "seq_len": int(max(w.seq_lens)), "page_size": w.page_size, "cache_dtype": w.cache_dtype,
+                   "num_splits": splits, "l2": "flushed (256 MiB write) before every timed step; cache > L2",
+                   "parallelism": f"dp{world} (independent replicas, no collective)"},
+        "tokens_per_s": round(tok_s, 1),
+        "decode_call_ms": round(dec, 5),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "mla_decode_paged (decode + combine), algorithmic bytes = cache rows + q + u + lse",
+                     "peak_source": f"hbm_gbs of {src}"},
+        "e2e": {"value": round(world * cache_bytes / (e2e_msps * 1e-3) / 1e9, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_msps, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample, thr, el = cpu_oracle_run(w, d, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": thr, "kind": "oracle",
+                               "sample": sample, "seconds": round(el, 2)}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from mla_latent_kv_16_gb300 import workloads as W
+    w = W.preset(args.workload)
+    d = W.make_inputs(w)
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_oracle_run(w, d, min(budget, 2.0))
+    vals, secs = [], 0.0
+    sample, thr = "", 1
+    for _ in range(args.steps):
+        v, sample, thr, el = cpu_oracle_run(w, d, budget)
+        vals.append(v)
+        secs += el
+    value = statistics.mean(vals)
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded)", "config": {"workload": w.name, "batch": w.batch, "q_len": w.q_len,
+                                                     "heads": w.heads, "seq_len": int(max(w.seq_lens)),
+                                                     "page_size": w.page_size, "cache_dtype": w.cache_dtype},
+           "cpu_baseline": {"kind": "oracle", "cores": thr, "sample": sample, "value": round(value, 4), "unit": UNIT},
+           "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,221 @@
+/*
+ * mla.h -- C ABI of the GB300 (sm_103a) MLA decode library.
+ *
+ * DeepSeek Multi-Head Latent Attention decode with matrix absorption over a
+ * paged latent KV cache. One decode step is
+ *
+ *   mla_cache_append  : write the step's new tokens (c_KV, RoPE(k_R)) into the pages
+ *   mla_absorb_q      : q_lat[t,h,:]  = W_UK[h]^T q_nope[t,h,:]         (128 -> 512)
+ *   mla_decode_paged  : s = (q_lat.c_KV + q_rope.k_R)/sqrt(192), online softmax,
+ *                       u[t,h,:] = sum_j p_j c_KV[j]  (split-KV + log-sum-exp combine)
+ *   mla_out_proj      : o[t,h,:]     = W_UV[h] u[t,h,:]                 (512 -> 128)
+ *
+ * Sources (page titles):
+ *   [P1] "Model Architecture Driving Inference Systems: From MHA/GQA to DeepSeek
+ *        MLA Matrix Absorption and Memory Minimalism" (dev.to)
+ *   [P2] "Multi-Head Latent Attention (MLA): Mathematical Foundations, Low-Rank KV
+ *        Compression, Decoupled Rotary Positional Embeddings, and Inference Matrix
+ *        Absorption" (llms.blog)
+ *   [P5] "Tech Radar: DeepSeek-V3 Multi-Head Latent Attention (MLA) Architecture &
+ *        KV Cache Compression" (tanhdev.com)
+ *
+ * Conventions for every entry point:
+ *   - Ownership: the caller owns every buffer. The library never allocates or
+ *     frees memory on these paths; scratch space is passed in (workspace).
+ *   - Pointers: device pointers unless stated otherwise, to contiguous row-major
+ *     arrays with the layouts given below, 16-byte aligned.
+ *   - Asynchrony: every call only enqueues work on `stream` (a cudaStream_t, NULL
+ *     for the legacy default stream) and returns without synchronising, except
+ *     mla_read_device_error, which synchronises the stream.
+ *   - Errors: argument checks (shapes, dtypes, alignment, sizes) fail
+ *     synchronously with MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED /
+ *     MLA_ERR_WORKSPACE_TOO_SMALL and enqueue nothing. A failed launch returns
+ *     MLA_ERR_CUDA. Faults that depend on device data (a block-table entry
+ *     outside the pool, a bad seq_len, slot or position) never trap: the
+ *     kernel skips the affected work, writes zeros (and lse = -inf) there, and
+ *     ORs an MLA_DEVERR_* bit into *dev_error (if dev_error is not NULL).
+ *   - No C++ exception crosses this boundary.
+ *   - Dimensions: d_nope = d_v = 128, d_c = 512, d_rope = 64; num_heads in
+ *     [1, 128]. A cached row is 576 values: [0,512) c_KV, [512,576) RoPE(k_R).
+ */
+#ifndef MLA_GB300_MLA_H
+#define MLA_GB300_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,
+  MLA_ERR_UNSUPPORTED = 2,
+  MLA_ERR_CUDA = 3,
+  MLA_ERR_WORKSPACE_TOO_SMALL = 4,
+  MLA_ERR_DEVICE_FLAG = 5
+} mla_status_t;
+
+/* Element types. MLA_E4M3 (OCP FP8 E4M3FN) is a cache type only. */
+typedef enum { MLA_F32 = 0, MLA_BF16 = 1, MLA_E4M3 = 2 } mla_dtype_t;
+
+typedef struct {
+  int32_t num_heads; /* H, 1..128                                  */
+  int32_t d_nope;    /* 128: per-head content query / key width     */
+  int32_t d_c;       /* 512: latent width                           */
+  int32_t d_rope;    /* 64: decoupled RoPE width                    */
+  int32_t d_v;       /* 128: per-head value width                   */
+} mla_dims_t;
+
+typedef void *mla_stream_t; /* cudaStream_t */
+
+/* Bits ORed into *dev_error by kernels. */
+#define MLA_DEVERR_BAD_PAGE 1     /* block_table entry outside [0, num_pages)  */
+#define MLA_DEVERR_BAD_SEQLEN 2   /* seq_len < q_len or > max_pages*page_size   */
+#define MLA_DEVERR_BAD_SLOT 4     /* slot_mapping entry outside the pool        */
+#define MLA_DEVERR_BAD_POSITION 8 /* position outside [0, max_pos)              */
+
+/* E4M3 cache: one fp32 scale per token per group; groups of the 576-value row
+ * are [0,128) [128,256) [256,384) [384,512) [512,576). */
+#define MLA_E4M3_GROUPS 5
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *mla_status_string(mla_status_t status);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int32_t mla_version(void);
+
+/*
+ * mla_rope_table -- HOST function. Fills cos_out/sin_out [max_pos][d_rope/2]
+ * (host fp32 arrays owned by the caller) with cos/sin of pos*theta_i,
+ * theta_i = base^(-(2i)/d_rope), each evaluated in double precision by the C
+ * library and rounded once to fp32. [P1] §2.3 / [P2] "The Decoupled RoPE
+ * Solution": k_R = RoPE(W_KR h) with standard rotary frequencies.
+ * Returns MLA_ERR_INVALID_ARG for max_pos < 1, odd or non-positive d_rope, a
+ * non-positive base or NULL outputs.
+ */
+mla_status_t mla_rope_table(int32_t max_pos, int32_t d_rope, double base, float *cos_out,
+                            float *sin_out);
+
+/*
+ * mla_cache_append -- write n_tokens new tokens into the paged latent cache.
+ * [P2] forward_decode_absorbed, step 2 (the token is cached before attending);
+ * [P1] §2.4 (row = 512 c_KV + 64 k_R); [P2] "High-Throughput Serving Kernels"
+ * (FP8 E4M3 cache with per-block scaling factors).
+ *
+ *   c_kv        [n_tokens][512]  in_dtype (MLA_F32 or MLA_BF16)
+ *   k_r         [n_tokens][64]   in_dtype, BEFORE rotation
+ *   positions   [n_tokens] int32, 0-based absolute position of each token
+ *   slot_mapping[n_tokens] int64, row of the pool: page * page_size + offset
+ *   rope_cos, rope_sin [max_pos][32] fp32 (from mla_rope_table, copied to device)
+ *   cache       [num_pages][page_size][576] cache_dtype
+ *   scales      [num_pages][page_size][5] fp32 when cache_dtype == MLA_E4M3, else NULL
+ *
+ * Row values: c_KV rounded (nearest-even) to the cache type; k_R rotated in
+ * fp32 as adjacent pairs, r0 = x0*c - x1*s, r1 = x0*s + x1*c with each product
+ * and sum rounded separately, then rounded to the cache type. For MLA_E4M3 the
+ * fp32 row (c_KV exact, rotated k_R unrounded) is quantised per group:
+ * scale = fl32(amax/448) (1 if amax == 0), byte = E4M3(fl32(x/scale)) with
+ * round-to-nearest-even and saturation to +-448. The result is bit-identical
+ * to that definition. Tokens with a bad slot or position are skipped and
+ * flagged (MLA_DEVERR_BAD_SLOT / MLA_DEVERR_BAD_POSITION).
+ */
+mla_status_t mla_cache_append(const void *c_kv, const void *k_r, const int32_t *positions,
+                              const int64_t *slot_mapping, const float *rope_cos,
+                              const float *rope_sin, int32_t n_tokens, int32_t max_pos,
+                              void *cache, float *scales, int64_t num_pages, int32_t page_size,
+                              mla_dtype_t in_dtype, mla_dtype_t cache_dtype, int32_t *dev_error,
+                              mla_stream_t stream);
+
+/*
+ * mla_absorb_q -- absorbed query, q_lat[t][h][:] = W_UK[h]^T q_nope[t][h][:].
+ * [P1] §3.1 (absorbed query, computed once per query token); [P2] "Attention
+ * Logit Matrix Absorption" and einsum('bthd,hdc->bhtc') with W_UK viewed as
+ * [n_heads][d_head][d_c].
+ *
+ *   q_nope [n_tokens][H][128] act, w_uk [H][128][512] act, q_lat [n_tokens][H][512] act
+ * act is MLA_F32 or MLA_BF16; fp32 accumulation; q_lat rounded to act.
+ * n_tokens = batch * q_len, token-major; n_tokens == 0 is a no-op.
+ */
+mla_status_t mla_absorb_q(const void *q_nope, const void *w_uk, void *q_lat, int32_t n_tokens,
+                          mla_dims_t dims, mla_dtype_t act, mla_stream_t stream);
+
+/*
+ * Number of KV splits mla_decode_paged will use for these arguments
+ * (num_splits > 0 is returned clamped to [1, max_pages_per_seq]; 0 selects
+ * the library's policy for the current device). Returns < 1 on bad arguments.
+ */
+int32_t mla_decode_num_splits(int32_t batch, int32_t q_len, int32_t max_pages_per_seq,
+                              int32_t page_size, int32_t num_splits, mla_dims_t dims,
+                              mla_dtype_t cache_dtype);
+
+/*
+ * Bytes of workspace mla_decode_paged needs for these arguments: the split-KV
+ * partials, [batch][q_len][splits][H][512] fp32 latent outputs plus
+ * [batch][q_len][splits][H] fp32 log-sum-exps, each 256-byte aligned.
+ * 0 when a single split is used.
+ */
+size_t mla_decode_workspace_size(int32_t batch, int32_t q_len, int32_t max_pages_per_seq,
+                                 int32_t page_size, int32_t num_splits, mla_dims_t dims,
+                                 mla_dtype_t cache_dtype);
+
+/*
+ * mla_decode_paged -- latent-space attention over the paged cache.
+ * [P1] §3.1 score S = ((q^C)^T k^C + (q^R)^T k^R)/sqrt(d_h + d_R) with
+ * (q^C)^T k^C = q_lat . c_KV; [P1] §3.2 latent sum u = sum_j P_j c_KV[j];
+ * [P5] §2 score formula; [P1] §4.1 paged cache with block size 64,
+ * variable-length batch.
+ *
+ *   q_lat       [batch][q_len][H][512] act (from mla_absorb_q)
+ *   q_rope      [batch][q_len][H][64]  act, already rotated
+ *   cache, scales: as written by mla_cache_append
+ *   block_table [batch][max_pages_per_seq] int32: physical page of logical page i
+ *   seq_lens    [batch] int32: cached tokens of each sequence INCLUDING the
+ *               step's q_len new ones; query j (0-based) attends to logical
+ *               tokens 0 .. seq_len - q_len + j (causal within the step)
+ *   softmax_scale: multiplies q.k (1/sqrt(192) for DeepSeek dimensions)
+ *   num_splits  : KV splits per (sequence, query); 0 = library policy
+ *   workspace   : workspace_bytes >= mla_decode_workspace_size(...)
+ *   u_out       [batch][q_len][H][512] act, normalised latent output
+ *   lse_out     [batch][q_len][H] fp32 natural-log log-sum-exp of the scaled
+ *               scores, or NULL
+ *   dev_error   : device int32 that bad data is reported into, or NULL
+ *
+ * Rows past seq_len in a sequence's last page are never read into the result
+ * (they may hold anything, NaN included). act is MLA_F32 or MLA_BF16;
+ * cache_dtype is act, or MLA_E4M3 with act == MLA_BF16.
+ */
+mla_status_t mla_decode_paged(const void *q_lat, const void *q_rope, const void *cache,
+                              const float *scales, const int32_t *block_table,
+                              const int32_t *seq_lens, int32_t batch, int32_t q_len,
+                              int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size,
+                              float softmax_scale, int32_t num_splits, void *workspace,
+                              size_t workspace_bytes, void *u_out, float *lse_out,
+                              int32_t *dev_error, mla_dims_t dims, mla_dtype_t act,
+                              mla_dtype_t cache_dtype, mla_stream_t stream);
+
+/*
+ * mla_out_proj -- per-head value up-projection, o[t][h][:] = W_UV[h] u[t][h][:].
+ * [P1] §3.2 (W_UV moved after the attention-weighted sum); [P2] "Value Output
+ * Matrix Absorption" with W_UV viewed as [n_heads][d_head][d_c].
+ *
+ *   u [n_tokens][H][512] act, w_uv [H][128][512] act, o [n_tokens][H][128] act
+ * fp32 accumulation, o rounded to act.
+ */
+mla_status_t mla_out_proj(const void *u, const void *w_uv, void *o, int32_t n_tokens,
+                          mla_dims_t dims, mla_dtype_t act, mla_stream_t stream);
+
+/*
+ * mla_read_device_error -- synchronise `stream`, copy *dev_error (device) to
+ * *code_out (host) and return MLA_ERR_DEVICE_FLAG if it is non-zero, MLA_OK
+ * otherwise. Does not clear the flag.
+ */
+mla_status_t mla_read_device_error(const int32_t *dev_error, mla_stream_t stream,
+                                   int32_t *code_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_MLA_H */

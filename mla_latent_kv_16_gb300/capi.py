@@ -1,0 +1,214 @@
+"""Thin Python binding of the C ABI in include/mla.h.
+
+Argument marshalling only: every step of the decode path runs in the library's
+CUDA kernels. Functions carry the ABI's names and take torch CUDA tensors
+(PyTorch provides device memory and streams). Output tensors are allocated with
+torch when the caller does not pass them. If the shared library is missing, the
+import of the library fails loudly; there is no other implementation to fall
+back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_WORKSPACE_TOO_SMALL, \
+    MLA_ERR_DEVICE_FLAG = range(6)
+MLA_F32, MLA_BF16, MLA_E4M3 = 0, 1, 2
+DTYPE_CODE = {"f32": MLA_F32, "bf16": MLA_BF16, "e4m3": MLA_E4M3}
+MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_SEQLEN, MLA_DEVERR_BAD_SLOT, MLA_DEVERR_BAD_POSITION = 1, 2, 4, 8
+
+EXPORTED = ("mla_status_string", "mla_version", "mla_rope_table", "mla_cache_append", "mla_absorb_q",
+            "mla_decode_num_splits", "mla_decode_workspace_size", "mla_decode_paged", "mla_out_proj",
+            "mla_read_device_error")
+
+
+class MlaDims(ctypes.Structure):
+    _fields_ = [("num_heads", ctypes.c_int32), ("d_nope", ctypes.c_int32), ("d_c", ctypes.c_int32),
+                ("d_rope", ctypes.c_int32), ("d_v", ctypes.c_int32)]
+
+
+def dims(num_heads: int) -> MlaDims:
+    return MlaDims(num_heads, 128, 512, 64, 128)
+
+
+class MlaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {status_string(status)}")
+        self.status = status
+
+
+_LIB = None
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: Optional[str] = None):
+    """Load (once) and return the ctypes handle of libmla_gb300.so."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    p = path or lib_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"libmla_gb300.so is not built ({p}); run mla_latent_kv_16_gb300.build.build()")
+    L = ctypes.CDLL(p)
+    vp, i32, i64, sz, f32, f64 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t,
+                                  ctypes.c_float, ctypes.c_double)
+    L.mla_status_string.restype = ctypes.c_char_p
+    L.mla_status_string.argtypes = [ctypes.c_int]
+    L.mla_version.restype = i32
+    L.mla_rope_table.restype = ctypes.c_int
+    L.mla_rope_table.argtypes = [i32, i32, f64, vp, vp]
+    L.mla_cache_append.restype = ctypes.c_int
+    L.mla_cache_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i64, i32, ctypes.c_int,
+                                   ctypes.c_int, vp, vp]
+    L.mla_absorb_q.restype = ctypes.c_int
+    L.mla_absorb_q.argtypes = [vp, vp, vp, i32, MlaDims, ctypes.c_int, vp]
+    L.mla_out_proj.restype = ctypes.c_int
+    L.mla_out_proj.argtypes = [vp, vp, vp, i32, MlaDims, ctypes.c_int, vp]
+    L.mla_decode_num_splits.restype = i32
+    L.mla_decode_num_splits.argtypes = [i32, i32, i32, i32, i32, MlaDims, ctypes.c_int]
+    L.mla_decode_workspace_size.restype = sz
+    L.mla_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, MlaDims, ctypes.c_int]
+    L.mla_decode_paged.restype = ctypes.c_int
+    L.mla_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, f32, i32, vp, sz, vp, vp,
+                                   vp, MlaDims, ctypes.c_int, ctypes.c_int, vp]
+    L.mla_read_device_error.restype = ctypes.c_int
+    L.mla_read_device_error.argtypes = [vp, vp, vp]
+    _LIB = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return load().mla_status_string(status).decode()
+
+
+def _check(fn: str, status: int):
+    if status != MLA_OK:
+        raise MlaError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _act_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MLA_F32
+    if t.dtype == torch.bfloat16:
+        return MLA_BF16
+    raise TypeError(f"unsupported activation dtype {t.dtype}")
+
+
+def _contig_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+# --------------------------------------------------------------------------- host helpers
+
+def mla_rope_table(max_pos: int, d_rope: int = 64, base: float = 10000.0):
+    """(cos, sin) host fp32 tensors [max_pos, d_rope/2] computed by the library."""
+    cos = torch.empty(max_pos, d_rope // 2, dtype=torch.float32)
+    sin = torch.empty_like(cos)
+    _check("mla_rope_table", load().mla_rope_table(max_pos, d_rope, base, _ptr(cos), _ptr(sin)))
+    return cos, sin
+
+
+def mla_decode_num_splits(batch, q_len, max_pages_per_seq, page_size, num_splits, num_heads, cache_dtype):
+    return load().mla_decode_num_splits(batch, q_len, max_pages_per_seq, page_size, num_splits, dims(num_heads),
+                                        DTYPE_CODE[cache_dtype])
+
+
+def mla_decode_workspace_size(batch, q_len, max_pages_per_seq, page_size, num_splits, num_heads, cache_dtype):
+    return load().mla_decode_workspace_size(batch, q_len, max_pages_per_seq, page_size, num_splits,
+                                            dims(num_heads), DTYPE_CODE[cache_dtype])
+
+
+# --------------------------------------------------------------------------- device calls
+
+def mla_cache_append(c_kv, k_r, positions, slot_mapping, rope_cos, rope_sin, cache, scales, page_size,
+                     cache_dtype: str, dev_error=None, stream=None):
+    _contig_cuda(c_kv, k_r, positions, slot_mapping, rope_cos, rope_sin, cache, scales, dev_error)
+    n = c_kv.shape[0]
+    rows = cache.shape[0] * cache.shape[1] if cache.dim() == 3 else cache.shape[0]
+    num_pages = rows // page_size
+    st = load().mla_cache_append(_ptr(c_kv), _ptr(k_r), _ptr(positions), _ptr(slot_mapping), _ptr(rope_cos),
+                                 _ptr(rope_sin), n, rope_cos.shape[0], _ptr(cache), _ptr(scales), num_pages,
+                                 page_size, _act_code(c_kv), DTYPE_CODE[cache_dtype], _ptr(dev_error),
+                                 _stream(stream))
+    _check("mla_cache_append", st)
+
+
+def mla_absorb_q(q_nope, w_uk, q_lat=None, stream=None):
+    """q_nope [..., H, 128], w_uk [H, 128, 512] -> q_lat [..., H, 512]."""
+    _contig_cuda(q_nope, w_uk, q_lat)
+    H = w_uk.shape[0]
+    n = q_nope.numel() // (H * 128)
+    if q_lat is None:
+        q_lat = torch.empty(*q_nope.shape[:-1], 512, dtype=q_nope.dtype, device=q_nope.device)
+    _check("mla_absorb_q", load().mla_absorb_q(_ptr(q_nope), _ptr(w_uk), _ptr(q_lat), n, dims(H),
+                                                _act_code(q_nope), _stream(stream)))
+    return q_lat
+
+
+def mla_out_proj(u, w_uv, o=None, stream=None):
+    """u [..., H, 512], w_uv [H, 128, 512] -> o [..., H, 128]."""
+    _contig_cuda(u, w_uv, o)
+    H = w_uv.shape[0]
+    n = u.numel() // (H * 512)
+    if o is None:
+        o = torch.empty(*u.shape[:-1], 128, dtype=u.dtype, device=u.device)
+    _check("mla_out_proj", load().mla_out_proj(_ptr(u), _ptr(w_uv), _ptr(o), n, dims(H), _act_code(u),
+                                                _stream(stream)))
+    return o
+
+
+def mla_decode_paged(q_lat, q_rope, cache, scales, block_table, seq_lens, page_size: int, cache_dtype: str,
+                     softmax_scale: Optional[float] = None, num_splits: int = 0, workspace=None, u_out=None,
+                     lse_out=None, dev_error=None, stream=None, want_lse: bool = True):
+    """q_lat [B, Lq, H, 512], q_rope [B, Lq, H, 64] -> (u [B, Lq, H, 512], lse [B, Lq, H] or None)."""
+    _contig_cuda(q_lat, q_rope, cache, scales, block_table, seq_lens, workspace, u_out, lse_out, dev_error)
+    B, Lq, H = q_lat.shape[0], q_lat.shape[1], q_lat.shape[2]
+    maxp = block_table.shape[1]
+    rows = cache.shape[0] * cache.shape[1] if cache.dim() == 3 else cache.shape[0]
+    num_pages = rows // page_size
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(128 + 64)
+    if u_out is None:
+        u_out = torch.empty(B, Lq, H, 512, dtype=q_lat.dtype, device=q_lat.device)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty(B, Lq, H, dtype=torch.float32, device=q_lat.device)
+    need = mla_decode_workspace_size(B, Lq, maxp, page_size, num_splits, H, cache_dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_lat.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().mla_decode_paged(_ptr(q_lat), _ptr(q_rope), _ptr(cache), _ptr(scales), _ptr(block_table),
+                                 _ptr(seq_lens), B, Lq, maxp, num_pages, page_size, softmax_scale, num_splits,
+                                 _ptr(workspace), ws_bytes, _ptr(u_out), _ptr(lse_out), _ptr(dev_error), dims(H),
+                                 _act_code(q_lat), DTYPE_CODE[cache_dtype], _stream(stream))
+    _check("mla_decode_paged", st)
+    return u_out, lse_out
+
+
+def mla_read_device_error(dev_error, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    st = load().mla_read_device_error(_ptr(dev_error), _stream(stream), ctypes.byref(code))
+    if st not in (MLA_OK, MLA_ERR_DEVICE_FLAG):
+        _check("mla_read_device_error", st)
+    return code.value

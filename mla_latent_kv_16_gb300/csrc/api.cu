@@ -1,0 +1,251 @@
+// C ABI entry points (include/mla.h): argument validation, split policy and
+// dispatch to the sm_103a kernels. No allocation happens here; every buffer is
+// the caller's.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "launchers.h"
+#include "mla.h"
+
+namespace mla {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+namespace {
+
+constexpr int32_t kMaxTokens = 1 << 20;
+constexpr int32_t kMaxBatchQ = 65535;
+
+bool dims_ok(const mla_dims_t& d) {
+  return d.d_nope == 128 && d.d_c == 512 && d.d_rope == 64 && d.d_v == 128 && d.num_heads >= 1 &&
+         d.num_heads <= 128;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mla_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+bool use_tc_decode(int32_t heads, int32_t page_size, mla_dtype_t act, mla_dtype_t cache_dtype) {
+  return heads == 128 && act == MLA_BF16 && (cache_dtype == MLA_BF16 || cache_dtype == MLA_E4M3) &&
+         page_size % 64 == 0;
+}
+
+// Work items of one split: the SIMT kernel runs ceil(H/8) CTAs per (b, j, split);
+// the tcgen05 kernel one CTA pair.
+int32_t resolve_splits(int32_t batch, int32_t q_len, int32_t max_pages, int32_t page_size,
+                       int32_t requested, const mla_dims_t& d, mla_dtype_t cache_dtype) {
+  if (batch < 0 || q_len < 1 || max_pages < 1 || page_size < 1 || requested < 0 || !dims_ok(d)) return 0;
+  if (requested > 0) return requested > max_pages ? max_pages : requested;
+  const bool tc = use_tc_decode(d.num_heads, page_size, MLA_BF16, cache_dtype);
+  const int sms = device_sm_count();
+  const int64_t slots = tc ? sms / 2 : sms * 2;            // concurrent work items
+  const int64_t per_item = tc ? 1 : (d.num_heads + 7) / 8;
+  const int64_t items0 = static_cast<int64_t>(batch > 0 ? batch : 1) * q_len * per_item;
+  // cost = waves * (pages per split + partial-output overhead in page units)
+  const double part_cost = tc ? 2.0 : 0.5;
+  int32_t best = 1;
+  double best_cost = 1e300;
+  const int32_t smax = max_pages < 256 ? max_pages : 256;
+  for (int32_t s = 1; s <= smax; ++s) {
+    const int64_t pps = (max_pages + s - 1) / s;
+    const int32_t s_eff = static_cast<int32_t>((max_pages + pps - 1) / pps);
+    if (s_eff != s) continue;
+    const int64_t waves = (items0 * s + slots - 1) / slots;
+    const double cost = static_cast<double>(waves) * (static_cast<double>(pps) + (s > 1 ? part_cost : 0.0));
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t workspace_bytes_for(int32_t batch, int32_t q_len, int32_t splits, int32_t heads) {
+  if (splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(batch) * q_len * splits * heads;
+  return align256(rows * 512 * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_status_string(mla_status_t s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
+    case MLA_ERR_DEVICE_FLAG: return "MLA_ERR_DEVICE_FLAG";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+int32_t mla_version(void) { return 100; }
+
+mla_status_t mla_rope_table(int32_t max_pos, int32_t d_rope, double base, float* cos_out, float* sin_out) {
+  if (max_pos < 1 || d_rope < 2 || (d_rope & 1) || !(base > 0.0) || cos_out == nullptr || sin_out == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  const int half = d_rope / 2;
+  for (int i = 0; i < half; ++i) {
+    const double theta = std::pow(base, -(2.0 * i) / static_cast<double>(d_rope));
+    for (int32_t p = 0; p < max_pos; ++p) {
+      const double ang = static_cast<double>(p) * theta;
+      cos_out[static_cast<int64_t>(p) * half + i] = static_cast<float>(std::cos(ang));
+      sin_out[static_cast<int64_t>(p) * half + i] = static_cast<float>(std::sin(ang));
+    }
+  }
+  return MLA_OK;
+}
+
+mla_status_t mla_cache_append(const void* c_kv, const void* k_r, const int32_t* positions,
+                              const int64_t* slot_mapping, const float* rope_cos, const float* rope_sin,
+                              int32_t n_tokens, int32_t max_pos, void* cache, float* scales, int64_t num_pages,
+                              int32_t page_size, mla_dtype_t in_dtype, mla_dtype_t cache_dtype,
+                              int32_t* dev_error, mla_stream_t stream) {
+  if (n_tokens < 0 || n_tokens > kMaxTokens || max_pos < 1 || num_pages < 1 || page_size < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (in_dtype != MLA_F32 && in_dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (cache_dtype != MLA_F32 && cache_dtype != MLA_BF16 && cache_dtype != MLA_E4M3) return MLA_ERR_UNSUPPORTED;
+  if ((cache_dtype == MLA_E4M3) != (scales != nullptr)) return MLA_ERR_INVALID_ARG;
+  if (cache == nullptr || rope_cos == nullptr || rope_sin == nullptr) return MLA_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (c_kv == nullptr || k_r == nullptr || positions == nullptr || slot_mapping == nullptr))
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(c_kv) || !aligned16(k_r) || !aligned16(cache) || (reinterpret_cast<uintptr_t>(k_r) & 7))
+    return MLA_ERR_INVALID_ARG;
+  AppendArgs a{c_kv, k_r, positions, slot_mapping, rope_cos, rope_sin, n_tokens, max_pos, cache, scales,
+               num_pages * static_cast<int64_t>(page_size), in_dtype, cache_dtype, dev_error};
+  return from_cuda(launch_append(a, static_cast<cudaStream_t>(stream)));
+}
+
+mla_status_t mla_absorb_q(const void* q_nope, const void* w_uk, void* q_lat, int32_t n_tokens, mla_dims_t dims,
+                          mla_dtype_t act, mla_stream_t stream) {
+  if (!dims_ok(dims) || n_tokens < 0 || n_tokens > kMaxTokens) return MLA_ERR_INVALID_ARG;
+  if (act != MLA_F32 && act != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return MLA_OK;
+  if (q_nope == nullptr || w_uk == nullptr || q_lat == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_lat)) return MLA_ERR_INVALID_ARG;
+  ProjArgs a{q_nope, w_uk, q_lat, n_tokens, dims.num_heads, act};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (act == MLA_BF16) {
+    cudaError_t e = launch_absorb_tc(a, s);
+    if (e != cudaErrorNotSupported) return from_cuda(e);
+  }
+  return from_cuda(launch_absorb_simt(a, s));
+}
+
+mla_status_t mla_out_proj(const void* u, const void* w_uv, void* o, int32_t n_tokens, mla_dims_t dims,
+                          mla_dtype_t act, mla_stream_t stream) {
+  if (!dims_ok(dims) || n_tokens < 0 || n_tokens > kMaxTokens) return MLA_ERR_INVALID_ARG;
+  if (act != MLA_F32 && act != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return MLA_OK;
+  if (u == nullptr || w_uv == nullptr || o == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(w_uv) || !aligned16(o)) return MLA_ERR_INVALID_ARG;
+  ProjArgs a{u, w_uv, o, n_tokens, dims.num_heads, act};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (act == MLA_BF16) {
+    cudaError_t e = launch_out_proj_tc(a, s);
+    if (e != cudaErrorNotSupported) return from_cuda(e);
+  }
+  return from_cuda(launch_out_proj_simt(a, s));
+}
+
+int32_t mla_decode_num_splits(int32_t batch, int32_t q_len, int32_t max_pages_per_seq, int32_t page_size,
+                              int32_t num_splits, mla_dims_t dims, mla_dtype_t cache_dtype) {
+  return resolve_splits(batch, q_len, max_pages_per_seq, page_size, num_splits, dims, cache_dtype);
+}
+
+size_t mla_decode_workspace_size(int32_t batch, int32_t q_len, int32_t max_pages_per_seq, int32_t page_size,
+                                 int32_t num_splits, mla_dims_t dims, mla_dtype_t cache_dtype) {
+  const int32_t s = resolve_splits(batch, q_len, max_pages_per_seq, page_size, num_splits, dims, cache_dtype);
+  if (s < 1 || batch < 0) return 0;
+  return workspace_bytes_for(batch, q_len, s, dims.num_heads);
+}
+
+mla_status_t mla_decode_paged(const void* q_lat, const void* q_rope, const void* cache, const float* scales,
+                              const int32_t* block_table, const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                              int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size, float softmax_scale,
+                              int32_t num_splits, void* workspace, size_t workspace_bytes, void* u_out,
+                              float* lse_out, int32_t* dev_error, mla_dims_t dims, mla_dtype_t act,
+                              mla_dtype_t cache_dtype, mla_stream_t stream) {
+  if (!dims_ok(dims) || batch < 0 || q_len < 1 || static_cast<int64_t>(batch) * q_len > kMaxBatchQ ||
+      max_pages_per_seq < 1 || num_pages < 1 || page_size < 1 || num_splits < 0 || !std::isfinite(softmax_scale))
+    return MLA_ERR_INVALID_ARG;
+  if (act != MLA_F32 && act != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (!(cache_dtype == act || (cache_dtype == MLA_E4M3 && act == MLA_BF16))) return MLA_ERR_UNSUPPORTED;
+  if ((cache_dtype == MLA_E4M3) != (scales != nullptr)) return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_pages_per_seq) * page_size > (int64_t(1) << 30)) return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  if (q_lat == nullptr || q_rope == nullptr || cache == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      u_out == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_lat) || !aligned16(q_rope) || !aligned16(cache) || !aligned16(u_out))
+    return MLA_ERR_INVALID_ARG;
+  const int32_t S = resolve_splits(batch, q_len, max_pages_per_seq, page_size, num_splits, dims, cache_dtype);
+  if (S < 1) return MLA_ERR_INVALID_ARG;
+  const size_t need = workspace_bytes_for(batch, q_len, S, dims.num_heads);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+  DecodeArgs a{};
+  a.q_lat = q_lat;
+  a.q_rope = q_rope;
+  a.cache = cache;
+  a.scales = scales;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.q_len = q_len;
+  a.max_pages = max_pages_per_seq;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.softmax_scale = softmax_scale;
+  a.num_splits = S;
+  a.pages_per_split = (max_pages_per_seq + S - 1) / S;
+  const size_t rows = static_cast<size_t>(batch) * q_len * S * dims.num_heads;
+  a.part_u = need > 0 ? static_cast<float*>(workspace) : nullptr;
+  a.part_lse = need > 0 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * 512 * sizeof(float)))
+                        : nullptr;
+  a.u_out = u_out;
+  a.lse_out = lse_out;
+  a.dev_error = dev_error;
+  a.heads = dims.num_heads;
+  a.act = act;
+  a.cache_dtype = cache_dtype;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (use_tc_decode(dims.num_heads, page_size, act, cache_dtype) && decode_tc_supported(a))
+    e = launch_decode_tc(a, s);
+  else
+    e = launch_decode_simt(a, s);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  return from_cuda(launch_combine(a, s));
+}
+
+mla_status_t mla_read_device_error(const int32_t* dev_error, mla_stream_t stream, int32_t* code_out) {
+  if (dev_error == nullptr || code_out == nullptr) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, dev_error, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  *code_out = v;
+  return v != 0 ? MLA_ERR_DEVICE_FLAG : MLA_OK;
+}
+
+}  // extern "C"

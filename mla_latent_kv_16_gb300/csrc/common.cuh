@@ -1,0 +1,75 @@
+// Device helpers shared by the MLA decode kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla.h"
+
+namespace mla {
+
+constexpr int kDNope = 128;  // per-head content query/key width
+constexpr int kDC = 512;     // latent width
+constexpr int kDRope = 64;   // decoupled RoPE width
+constexpr int kDV = 128;     // per-head value width
+constexpr int kRow = kDC + kDRope;  // 576 values per cached token
+constexpr int kGroups = MLA_E4M3_GROUPS;
+constexpr float kE4M3Max = 448.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ void flag_error(int32_t* flag, int32_t bits) {
+  if (flag != nullptr) atomicOr(flag, bits);
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// Round-to-nearest-even fp32 -> bf16 bits.
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return uint32_t(f32_to_bf16_bits(lo)) | (uint32_t(f32_to_bf16_bits(hi)) << 16);
+}
+
+// Exact E4M3FN -> fp32 decode of one byte (bias 7, subnormals, no inf).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+  __nv_fp8_e4m3 v;
+  v.__x = static_cast<__nv_fp8_storage_t>(byte);
+  return static_cast<float>(v);
+}
+
+template <typename T>
+struct ActIO;
+template <>
+struct ActIO<float> {
+  __device__ __forceinline__ static float load(const float* p) { return *p; }
+  __device__ __forceinline__ static void store(float* p, float v) { *p = v; }
+};
+template <>
+struct ActIO<__nv_bfloat16> {
+  __device__ __forceinline__ static float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+  __device__ __forceinline__ static void store(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace mla

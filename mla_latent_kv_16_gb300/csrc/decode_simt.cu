@@ -1,0 +1,257 @@
+// Paged latent-space decode attention on CUDA cores, plus the split-KV
+// log-sum-exp combine.
+//
+// Score per head h and cached token j ("Model Architecture Driving Inference
+// Systems" §3.1; "Tech Radar: DeepSeek-V3 MLA" §2):
+//   s_j = (q_lat[h] . c_KV[j] + q_rope[h] . k_R[j]) * softmax_scale
+// latent output (§3.2): u[h] = sum_j softmax(s)_j c_KV[j], computed with a
+// running max / running sum over token tiles so that no score leaves the chip.
+//
+// This kernel handles every dtype and head count (fp32 tiny decode, any H); the
+// bf16/E4M3 128-head path is the tcgen05 kernel in decode_tc.cu.
+//
+// CTA = 8 warps = 8 heads of one (sequence, query, split); warp lane = token
+// inside a 32-token tile. Rows are decoded to fp32 in shared memory (rows past
+// the visible range are zero-filled, so poisoned page tails never enter).
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "launchers.h"
+
+namespace mla {
+namespace {
+
+constexpr int kTile = 32;
+constexpr int kHG = 8;                // heads per CTA
+constexpr int kRowPad = kRow + 1;     // bank-conflict-free row stride (floats)
+constexpr size_t kSimtSmem = (size_t(kTile) * kRowPad + size_t(kHG) * kRow) * sizeof(float);
+
+template <typename T>
+__device__ __forceinline__ float ld_act(const void* base, int64_t idx) {
+  return ActIO<T>::load(static_cast<const T*>(base) + idx);
+}
+
+template <int kCache>
+__device__ __forceinline__ void load_row(const void* cache, const float* scales, int64_t slot, int k0,
+                                         float* dst, int lane) {
+  // lane-strided copy of one 576-value row into fp32 shared memory
+  if constexpr (kCache == MLA_F32) {
+    const float* r = static_cast<const float*>(cache) + slot * kRow;
+    for (int k = k0 + lane; k < kRow; k += 32) dst[k] = r[k];
+  } else if constexpr (kCache == MLA_BF16) {
+    const uint16_t* r = static_cast<const uint16_t*>(cache) + slot * kRow;
+    for (int k = k0 + lane; k < kRow; k += 32) dst[k] = bf16_bits_to_f32(r[k]);
+  } else {
+    const uint8_t* r = static_cast<const uint8_t*>(cache) + slot * kRow;
+    const float* sc = scales + slot * kGroups;
+    for (int k = k0 + lane; k < kRow; k += 32) dst[k] = e4m3_to_f32(r[k]) * sc[k >> 7];
+  }
+}
+
+template <typename T, int kCache>
+__global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
+  extern __shared__ float smem[];
+  float* rs = smem;                          // [kTile][kRowPad]
+  float* qs = smem + kTile * kRowPad;        // [kHG][kRow]
+  const int split = blockIdx.x;
+  const int h0 = blockIdx.y * kHG;
+  const int bj = blockIdx.z;
+  const int b = bj / a.q_len, j = bj % a.q_len;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = h0 + warp;
+  const bool head_ok = h < a.heads;
+
+  const int L = a.seq_lens[b];
+  const int P = a.page_size;
+  int n_vis = L - a.q_len + j + 1;
+  bool bad = false;
+  if (L < a.q_len || static_cast<int64_t>(L) > static_cast<int64_t>(a.max_pages) * P) {
+    if (threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_SEQLEN);
+    bad = true;
+    n_vis = 0;
+  }
+  const int tok_begin = split * a.pages_per_split * P;
+  const int tok_end = min(n_vis, (split + 1) * a.pages_per_split * P);
+  const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
+  // validate every page this split touches
+  if (tok_begin < tok_end) {
+    const int pg0 = tok_begin / P, pg1 = (tok_end - 1) / P;
+    int local_bad = 0;
+    for (int pg = pg0 + threadIdx.x; pg <= pg1; pg += blockDim.x) {
+      const int32_t pp = bt[pg];
+      if (pp < 0 || pp >= a.num_pages) local_bad = 1;
+    }
+    if (__syncthreads_or(local_bad)) {
+      if (threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_PAGE);
+      bad = true;
+    }
+  }
+
+  // this warp's query, pre-scaled into the log2 domain
+  const float qscale = a.softmax_scale * kLog2e;
+  if (head_ok) {
+    const int64_t qi = (static_cast<int64_t>(bj) * a.heads + h);
+    for (int k = lane; k < kRow; k += 32) {
+      const float v = k < kDC ? ld_act<T>(a.q_lat, qi * kDC + k) : ld_act<T>(a.q_rope, qi * kDRope + (k - kDC));
+      qs[warp * kRow + k] = v * qscale;
+    }
+  }
+
+  float m = -CUDART_INF_F, l = 0.0f;
+  float acc[kDC / 32];
+#pragma unroll
+  for (int i = 0; i < kDC / 32; ++i) acc[i] = 0.0f;
+
+  const int end = bad ? tok_begin : tok_end;
+  for (int t0 = tok_begin; t0 < end; t0 += kTile) {
+    __syncthreads();
+    // warp w loads rows t0 + w, t0 + w + 8, ...
+    for (int r = warp; r < kTile; r += 8) {
+      const int tok = t0 + r;
+      float* dst = rs + r * kRowPad;
+      if (tok < end) {
+        const int64_t slot = static_cast<int64_t>(bt[tok / P]) * P + tok % P;
+        load_row<kCache>(a.cache, a.scales, slot, 0, dst, lane);
+      } else {
+        for (int k = lane; k < kRow; k += 32) dst[k] = 0.0f;
+      }
+    }
+    __syncthreads();
+    if (head_ok) {
+      const float* qh = qs + warp * kRow;
+      const float* rr = rs + lane * kRowPad;
+      float s = 0.0f;
+#pragma unroll 8
+      for (int k = 0; k < kRow; ++k) s = fmaf(qh[k], rr[k], s);
+      if (t0 + lane >= end) s = -CUDART_INF_F;
+      const float m_new = fmaxf(m, warp_max(s));
+      const float alpha = fast_exp2(m - m_new);   // m = -inf on the first tile -> 0
+      const float p = fast_exp2(s - m_new);
+      l = l * alpha + warp_sum(p);
+      m = m_new;
+#pragma unroll
+      for (int i = 0; i < kDC / 32; ++i) acc[i] *= alpha;
+      for (int t = 0; t < kTile; ++t) {
+        const float pt = __shfl_sync(0xffffffffu, p, t);
+        const float* rt = rs + t * kRowPad + lane;
+#pragma unroll
+        for (int i = 0; i < kDC / 32; ++i) acc[i] = fmaf(pt, rt[32 * i], acc[i]);
+      }
+    }
+  }
+  if (!head_ok) return;
+
+  const bool empty = !(l > 0.0f);
+  const float inv_l = empty ? 0.0f : 1.0f / l;
+  const float lse = empty ? -CUDART_INF_F : (m + log2f(l)) * kLn2;
+  const int64_t row = static_cast<int64_t>(bj) * a.heads + h;
+  if (a.num_splits == 1) {
+    T* u = static_cast<T*>(a.u_out) + row * kDC;
+#pragma unroll
+    for (int i = 0; i < kDC / 32; ++i) ActIO<T>::store(u + lane + 32 * i, acc[i] * inv_l);
+    if (a.lse_out != nullptr && lane == 0) a.lse_out[row] = lse;
+  } else {
+    const int64_t prow = (static_cast<int64_t>(bj) * a.num_splits + split) * a.heads + h;
+    float* pu = a.part_u + prow * kDC;
+#pragma unroll
+    for (int i = 0; i < kDC / 32; ++i) pu[lane + 32 * i] = acc[i] * inv_l;
+    if (lane == 0) a.part_lse[prow] = lse;
+  }
+}
+
+// One CTA per (head, sequence*query); 128 threads x 4 latent columns.
+template <typename T>
+__global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
+  extern __shared__ float wsh[];  // [S]
+  __shared__ float red[2];
+  const int h = blockIdx.x, bj = blockIdx.y;
+  const int S = a.num_splits;
+  const float* lse_s = a.part_lse;
+  auto lse_at = [&](int s) { return lse_s[(static_cast<int64_t>(bj) * S + s) * a.heads + h]; };
+  float mx = -CUDART_INF_F;
+  for (int s = threadIdx.x; s < S; s += blockDim.x) mx = fmaxf(mx, lse_at(s));
+  mx = warp_max(mx);
+  if ((threadIdx.x & 31) == 0) wsh[S + (threadIdx.x >> 5)] = mx;  // scratch after weights
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float v = -CUDART_INF_F;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) v = fmaxf(v, wsh[S + w]);
+    red[0] = v;
+  }
+  __syncthreads();
+  mx = red[0];
+  const bool none = (mx == -CUDART_INF_F);
+  float sum = 0.0f;
+  for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    const float ls = lse_at(s);
+    const float wv = (none || ls == -CUDART_INF_F) ? 0.0f : fast_exp2((ls - mx) * kLog2e);
+    wsh[s] = wv;
+    sum += wv;
+  }
+  sum = warp_sum(sum);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) wsh[S + (threadIdx.x >> 5)] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float v = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) v += wsh[S + w];
+    red[1] = v;
+  }
+  __syncthreads();
+  const float tot = red[1];
+  const float inv = none ? 0.0f : 1.0f / tot;
+  const int64_t row = static_cast<int64_t>(bj) * a.heads + h;
+  T* u = static_cast<T*>(a.u_out) + row * kDC;
+  for (int c = threadIdx.x; c < kDC; c += blockDim.x) {
+    float v = 0.0f;
+    for (int s = 0; s < S; ++s) {
+      const float wv = wsh[s];
+      if (wv != 0.0f) v = fmaf(wv, a.part_u[((static_cast<int64_t>(bj) * S + s) * a.heads + h) * kDC + c], v);
+    }
+    ActIO<T>::store(u + c, v * inv);
+  }
+  if (threadIdx.x == 0 && a.lse_out != nullptr) a.lse_out[row] = none ? -CUDART_INF_F : mx + logf(tot);
+}
+
+template <typename T>
+cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
+  dim3 grid(a.num_splits, (a.heads + kHG - 1) / kHG, a.batch * a.q_len);
+  cudaError_t e = cudaSuccess;
+  switch (a.cache_dtype) {
+    case MLA_F32:
+      e = cudaFuncSetAttribute(decode_simt_kernel<T, MLA_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSimtSmem);
+      if (e == cudaSuccess) decode_simt_kernel<T, MLA_F32><<<grid, 256, kSimtSmem, s>>>(a);
+      break;
+    case MLA_BF16:
+      e = cudaFuncSetAttribute(decode_simt_kernel<T, MLA_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSimtSmem);
+      if (e == cudaSuccess) decode_simt_kernel<T, MLA_BF16><<<grid, 256, kSimtSmem, s>>>(a);
+      break;
+    default:
+      e = cudaFuncSetAttribute(decode_simt_kernel<T, MLA_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSimtSmem);
+      if (e == cudaSuccess) decode_simt_kernel<T, MLA_E4M3><<<grid, 256, kSimtSmem, s>>>(a);
+      break;
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s) {
+  if (a.batch == 0) return cudaSuccess;
+  if (a.act == MLA_F32) return launch_decode_t<float>(a, s);
+  return launch_decode_t<__nv_bfloat16>(a, s);
+}
+
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
+  if (a.batch == 0 || a.num_splits == 1) return cudaSuccess;
+  dim3 grid(a.heads, a.batch * a.q_len);
+  const size_t smem = (a.num_splits + 8) * sizeof(float);
+  if (a.act == MLA_F32)
+    combine_kernel<float><<<grid, 128, smem, s>>>(a);
+  else
+    combine_kernel<__nv_bfloat16><<<grid, 128, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,75 @@
+// Internal launchers behind the C ABI (mla.h). Arguments are already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "mla.h"
+
+namespace mla {
+
+struct AppendArgs {
+  const void* c_kv;
+  const void* k_r;
+  const int32_t* positions;
+  const int64_t* slots;
+  const float* cos_t;
+  const float* sin_t;
+  int32_t n_tokens;
+  int32_t max_pos;
+  void* cache;
+  float* scales;
+  int64_t n_rows;  // num_pages * page_size
+  mla_dtype_t in_dtype;
+  mla_dtype_t cache_dtype;
+  int32_t* dev_error;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+
+struct ProjArgs {
+  const void* x;  // q_nope [n][H][128] (absorb) or u [n][H][512] (out_proj)
+  const void* w;  // [H][128][512]
+  void* y;        // q_lat [n][H][512] or o [n][H][128]
+  int32_t n_tokens;
+  int32_t heads;
+  mla_dtype_t act;
+};
+cudaError_t launch_absorb_simt(const ProjArgs& a, cudaStream_t s);
+cudaError_t launch_out_proj_simt(const ProjArgs& a, cudaStream_t s);
+// tcgen05 versions (bf16 only). Return cudaErrorNotSupported when not applicable.
+cudaError_t launch_absorb_tc(const ProjArgs& a, cudaStream_t s);
+cudaError_t launch_out_proj_tc(const ProjArgs& a, cudaStream_t s);
+
+struct DecodeArgs {
+  const void* q_lat;
+  const void* q_rope;
+  const void* cache;
+  const float* scales;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t batch;
+  int32_t q_len;
+  int32_t max_pages;
+  int64_t num_pages;
+  int32_t page_size;
+  float softmax_scale;
+  int32_t num_splits;     // resolved, >= 1
+  int32_t pages_per_split;
+  float* part_u;          // [B][Lq][S][H][512] fp32 (S > 1)
+  float* part_lse;        // [B][Lq][S][H] fp32 (S > 1)
+  void* u_out;            // [B][Lq][H][512] act
+  float* lse_out;         // [B][Lq][H] or nullptr
+  int32_t* dev_error;
+  int32_t heads;
+  mla_dtype_t act;
+  mla_dtype_t cache_dtype;
+};
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
+bool decode_tc_supported(const DecodeArgs& a);
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace mla

@@ -1,0 +1,127 @@
+"""One MLA decode layer over a paged latent cache, driven through the C ABI.
+
+MLADecodeLayer owns the device state of one attention layer: the weights
+W_UK, W_UV, the paged latent cache (and E4M3 scales), the RoPE tables, the
+block table / sequence lengths, and reusable workspace and output buffers. A
+decode step is
+
+    append(new tokens) -> absorb_q -> decode_paged (+ combine) -> out_proj
+
+exactly the four calls of the library, on one stream, with no allocation in
+the step once the buffers exist.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import torch
+
+from . import capi
+from .workloads import BF16, E4M3, F32, ROW, TORCH_DTYPE, Workload
+
+CACHE_TORCH = {F32: torch.float32, BF16: torch.bfloat16, E4M3: torch.uint8}
+
+
+class MLADecodeLayer:
+    def __init__(self, w: Workload, w_uk: torch.Tensor, w_uv: torch.Tensor, block_table: torch.Tensor,
+                 seq_lens: torch.Tensor, device="cuda", poison: bool = True, num_splits: Optional[int] = None):
+        self.w = w
+        self.device = torch.device(device)
+        self.H = w.heads
+        self.P = w.page_size
+        self.cache_dtype = w.cache_dtype
+        self.act = TORCH_DTYPE[w.act_dtype]
+        self.w_uk = w_uk.to(self.device).contiguous()
+        self.w_uv = w_uv.to(self.device).contiguous()
+        self.block_table = block_table.to(self.device, torch.int32).contiguous()
+        self.seq_lens = seq_lens.to(self.device, torch.int32).contiguous()
+        self.num_pages = w.num_pages
+        ct = CACHE_TORCH[w.cache_dtype]
+        self.cache = torch.empty(self.num_pages, self.P, ROW, dtype=ct, device=self.device)
+        self.scales = (torch.empty(self.num_pages, self.P, 5, dtype=torch.float32, device=self.device)
+                       if w.cache_dtype == E4M3 else None)
+        if poison:
+            self.poison()
+        cos, sin = capi.mla_rope_table(max(w.max_pos, 1), 64, w.rope_base)
+        self.rope_cos = cos.to(self.device)
+        self.rope_sin = sin.to(self.device)
+        self.dev_error = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.num_splits = w.num_splits if num_splits is None else num_splits
+        B, Lq = w.batch, w.q_len
+        self.splits = capi.mla_decode_num_splits(B, Lq, w.max_pages_per_seq, self.P, self.num_splits, self.H,
+                                                 self.cache_dtype)
+        need = capi.mla_decode_workspace_size(B, Lq, w.max_pages_per_seq, self.P, self.num_splits, self.H,
+                                              self.cache_dtype)
+        self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=self.device)
+        self.q_lat = torch.empty(B, Lq, self.H, 512, dtype=self.act, device=self.device)
+        self.u = torch.empty(B, Lq, self.H, 512, dtype=self.act, device=self.device)
+        self.lse = torch.empty(B, Lq, self.H, dtype=torch.float32, device=self.device)
+        self.o = torch.empty(B, Lq, self.H, 128, dtype=self.act, device=self.device)
+        self.softmax_scale = 1.0 / math.sqrt(128 + 64)
+
+    def poison(self):
+        """Fill the pool with NaN (values and scales) so unwritten rows are visible."""
+        if self.cache_dtype == E4M3:
+            self.cache.fill_(0x7F)
+            self.scales.fill_(float("nan"))
+        else:
+            self.cache.fill_(float("nan"))
+
+    def append(self, c_kv, k_r, positions, slots, stream=None):
+        capi.mla_cache_append(c_kv, k_r, positions, slots, self.rope_cos, self.rope_sin, self.cache, self.scales,
+                              self.P, self.cache_dtype, self.dev_error, stream)
+
+    def append_chunked(self, c_kv, k_r, positions, slots, chunk: int = 1 << 18):
+        """Fill a long context from host or device tensors, chunk by chunk."""
+        n = c_kv.shape[0]
+        for i in range(0, n, chunk):
+            sl = slice(i, min(n, i + chunk))
+            self.append(c_kv[sl].to(self.device, non_blocking=True).contiguous(),
+                        k_r[sl].to(self.device, non_blocking=True).contiguous(),
+                        positions[sl].to(self.device, non_blocking=True).contiguous(),
+                        slots[sl].to(self.device, non_blocking=True).contiguous())
+
+    def absorb(self, q_nope, stream=None):
+        return capi.mla_absorb_q(q_nope, self.w_uk, self.q_lat, stream)
+
+    def decode(self, q_lat, q_rope, stream=None):
+        return capi.mla_decode_paged(q_lat, q_rope, self.cache, self.scales, self.block_table, self.seq_lens, self.P,
+                                     self.cache_dtype, self.softmax_scale, self.num_splits, self.workspace, self.u,
+                                     self.lse, self.dev_error, stream)
+
+    def out_proj(self, u, stream=None):
+        return capi.mla_out_proj(u, self.w_uv, self.o, stream)
+
+    def step(self, q_nope, q_rope, new_c_kv, new_k_r, new_positions, new_slots, stream=None):
+        """One decode step: append the q_len new tokens, then attend. Returns o."""
+        if new_c_kv is not None and new_c_kv.shape[0] > 0:
+            self.append(new_c_kv, new_k_r, new_positions, new_slots, stream)
+        q_lat = self.absorb(q_nope, stream)
+        u, _ = self.decode(q_lat, q_rope, stream)
+        return self.out_proj(u, stream)
+
+    def device_error(self) -> int:
+        return capi.mla_read_device_error(self.dev_error)
+
+
+def build_layer(w: Workload, d: dict, device="cuda", fill_context: bool = True, **kw) -> MLADecodeLayer:
+    """A layer for workload w with the inputs d of workloads.make_inputs, its cache
+    filled with every context token except the step's new ones (when fill_context)."""
+    layer = MLADecodeLayer(w, d["w_uk"], d["w_uv"], d["block_table"], d["seq_lens"], device=device, **kw)
+    if fill_context:
+        n = d["ctx_c_kv"].shape[0]
+        keep = torch.ones(n, dtype=torch.bool)
+        keep[d["new_index"]] = False
+        idx = torch.nonzero(keep)[:, 0]
+        layer.append_chunked(d["ctx_c_kv"][idx], d["ctx_k_r"][idx], d["ctx_positions"][idx], d["ctx_slots"][idx])
+    return layer
+
+
+def step_inputs(d: dict, device="cuda"):
+    """Device tensors of one step's inputs (queries and the new tokens)."""
+    ni = d["new_index"]
+    return dict(q_nope=d["q_nope"].to(device).contiguous(), q_rope=d["q_rope"].to(device).contiguous(),
+                new_c_kv=d["ctx_c_kv"][ni].to(device).contiguous(), new_k_r=d["ctx_k_r"][ni].to(device).contiguous(),
+                new_positions=d["ctx_positions"][ni].to(device).contiguous(),
+                new_slots=d["ctx_slots"][ni].to(device).contiguous())

@@ -1,0 +1,91 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports
+every symbol include/mla.h declares, its host-only functions agree with the
+oracle, and argument validation fails synchronously before any device work."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import mla_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from mla_latent_kv_16_gb300 import build
+    build.build()
+    from mla_latent_kv_16_gb300 import capi as C
+    C.load()
+    return C
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "mla.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", txt)))
+
+
+def test_exports_every_declared_symbol(capi):
+    L = capi.load()
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(capi.EXPORTED)
+
+
+def test_version_and_status_strings(capi):
+    assert capi.load().mla_version() >= 100
+    assert capi.status_string(capi.MLA_OK) == "MLA_OK"
+    assert capi.status_string(capi.MLA_ERR_WORKSPACE_TOO_SMALL) == "MLA_ERR_WORKSPACE_TOO_SMALL"
+
+
+def test_rope_table_bitwise_equal_to_oracle(capi):
+    cos, sin = capi.mla_rope_table(3000)
+    oc, os_ = O.rope_tables(3000)
+    assert np.array_equal(cos.numpy().view(np.uint32), oc.view(np.uint32))
+    assert np.array_equal(sin.numpy().view(np.uint32), os_.view(np.uint32))
+
+
+def test_rope_table_rejects_bad_args(capi):
+    L = capi.load()
+    assert L.mla_rope_table(0, 64, 10000.0, None, None) == capi.MLA_ERR_INVALID_ARG
+    assert L.mla_rope_table(4, 63, 10000.0, None, None) == capi.MLA_ERR_INVALID_ARG
+
+
+def test_split_policy_and_workspace(capi):
+    # explicit split counts are honoured and clamped to the page count
+    assert capi.mla_decode_num_splits(4, 1, 2048, 64, 128, 128, "bf16") == 128
+    assert capi.mla_decode_num_splits(4, 1, 10, 64, 128, 128, "bf16") == 10
+    s = capi.mla_decode_num_splits(32, 1, 64, 64, 0, 128, "bf16")
+    assert 1 <= s <= 64
+    # workspace: fp32 partials [B][Lq][S][H][512] + lse, 256-byte aligned pieces
+    ws = capi.mla_decode_workspace_size(4, 1, 2048, 64, 128, 128, "bf16")
+    rows = 4 * 1 * 128 * 128
+    assert ws == rows * 512 * 4 + ((rows * 4 + 255) // 256) * 256
+    assert capi.mla_decode_workspace_size(4, 1, 2048, 64, 1, 128, "bf16") == 0
+    assert capi.mla_decode_num_splits(4, 0, 2048, 64, 0, 128, "bf16") < 1
+
+
+def test_validation_fails_before_device_work(capi):
+    """Calls with bad arguments return an error code without touching a GPU."""
+    L = capi.load()
+    bad_dims = capi.MlaDims(128, 128, 256, 64, 128)
+    assert L.mla_absorb_q(None, None, None, 4, bad_dims, capi.MLA_BF16, None) == capi.MLA_ERR_INVALID_ARG
+    assert L.mla_absorb_q(None, None, None, 4, capi.dims(128), capi.MLA_E4M3, None) == capi.MLA_ERR_UNSUPPORTED
+    assert L.mla_out_proj(None, None, None, -1, capi.dims(128), capi.MLA_BF16, None) == capi.MLA_ERR_INVALID_ARG
+    assert L.mla_absorb_q(None, None, None, 0, capi.dims(128), capi.MLA_BF16, None) == capi.MLA_OK  # no-op
+    # E4M3 cache without scales, and an fp32 activation with an E4M3 cache
+    assert L.mla_decode_paged(16, 16, 16, None, 16, 16, 1, 1, 1, 1, 64, 0.1, 0, None, 0, 16, None, None,
+                              capi.dims(128), capi.MLA_BF16, capi.MLA_E4M3, None) == capi.MLA_ERR_INVALID_ARG
+    assert L.mla_decode_paged(16, 16, 16, 16, 16, 16, 1, 1, 1, 1, 64, 0.1, 0, None, 0, 16, None, None,
+                              capi.dims(128), capi.MLA_F32, capi.MLA_E4M3, None) == capi.MLA_ERR_UNSUPPORTED
+    # workspace too small for an explicit split count
+    assert L.mla_decode_paged(16, 16, 16, None, 16, 16, 2, 1, 8, 16, 64, 0.1, 4, None, 0, 16, None, None,
+                              capi.dims(128), capi.MLA_BF16, capi.MLA_BF16, None) == capi.MLA_ERR_WORKSPACE_TOO_SMALL
+    assert L.mla_cache_append(16, 16, 16, 16, 16, 16, 1, 8, 16, None, 1, 64, capi.MLA_BF16, capi.MLA_E4M3, None,
+                              None) == capi.MLA_ERR_INVALID_ARG
+    assert L.mla_decode_paged(16, 16, 16, None, 16, 16, 1, 1, 1, 1, 64, float("nan"), 0, None, 0, 16, None, None,
+                              capi.dims(128), capi.MLA_BF16, capi.MLA_BF16, None) == capi.MLA_ERR_INVALID_ARG

@@ -1,0 +1,279 @@
+"""Parity of the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Small cases span several tiles and ragged page tails; the full-size workloads
+are checked on all or a seeded sample of sequences in the launch configuration
+the benchmark times. Tolerances: bit-exact for cache bytes and page indexing;
+rel-L2 <= 5e-3 and max-abs <= 2e-2 for floating outputs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from _util import REL_L2, MAX_ABS, assert_close, bits, f64, oracle_pool, rel_l2, seq_token_mask
+from oracle import mla_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from mla_latent_kv_16_gb300 import build
+    build.build()
+    from mla_latent_kv_16_gb300 import capi
+    capi.load()
+    yield
+
+
+def _W():
+    from mla_latent_kv_16_gb300 import workloads as W
+    return W
+
+
+def _layer(w, d, **kw):
+    from mla_latent_kv_16_gb300.engine import build_layer
+    return build_layer(w, d, **kw)
+
+
+def _step(layer, d):
+    from mla_latent_kv_16_gb300.engine import step_inputs
+    s = step_inputs(d)
+    o = layer.step(**s)
+    torch.cuda.synchronize()
+    return o
+
+
+SMALL = {
+    "tiny_fp32": dict(),
+    "dsv3_bf16": dict(batch=3, seq_lens=[4096, 700, 129]),
+    "ragged_bf16": dict(batch=5, seq_lens=[1, 63, 64, 65, 1000]),
+    "long_splitkv_bf16": dict(batch=2, seq_lens=[20000, 9000], num_splits=16),
+    "fp8_lq2": dict(batch=3, seq_lens=[2, 130, 515]),
+}
+
+
+def _small(name):
+    return _W().preset(name, **SMALL[name])
+
+
+# ----------------------------------------------------------------------------- append
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_append_bit_exact(name):
+    w = _small(name)
+    d = _W().make_inputs(w)
+    layer = _layer(w, d, fill_context=False)
+    from mla_latent_kv_16_gb300.engine import step_inputs
+    layer.append_chunked(d["ctx_c_kv"], d["ctx_k_r"], d["ctx_positions"], d["ctx_slots"])
+    torch.cuda.synchronize()
+    pool, sc = oracle_pool(w, d)
+    got = bits(layer.cache).reshape(pool.shape)
+    assert np.array_equal(got.view(np.uint8), pool.view(np.uint8)), "cache bytes differ"
+    if sc is not None:
+        assert np.array_equal(bits(layer.scales).reshape(sc.shape).view(np.uint32), sc.view(np.uint32))
+    assert layer.device_error() == 0
+
+
+def test_rope_table_matches_oracle():
+    from mla_latent_kv_16_gb300 import capi
+    cos, sin = capi.mla_rope_table(5000)
+    oc, os_ = O.rope_tables(5000)
+    assert np.array_equal(cos.numpy().view(np.uint32), oc.view(np.uint32))
+    assert np.array_equal(sin.numpy().view(np.uint32), os_.view(np.uint32))
+
+
+# ----------------------------------------------------------------------------- projections
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "dsv3_bf16", "fp8_lq2"])
+@pytest.mark.parametrize("n_tok", [1, 7, 32, 33, 256])
+def test_absorb_and_out_proj(name, n_tok):
+    from mla_latent_kv_16_gb300 import capi
+    w = _small(name)
+    d = _W().make_inputs(w, with_context=False)
+    H = w.heads
+    g = torch.Generator().manual_seed(n_tok)
+    dt = d["q_nope"].dtype
+    q = torch.randn(n_tok, H, 128, generator=g).to(dt)
+    u = torch.randn(n_tok, H, 512, generator=g).to(dt)
+    q_lat = capi.mla_absorb_q(q.cuda(), d["w_uk"].cuda())
+    o = capi.mla_out_proj(u.cuda(), d["w_uv"].cuda())
+    torch.cuda.synchronize()
+    ref_q = O.absorb_q(f64(q), f64(d["w_uk"]))
+    ref_o = O.out_proj(f64(u), f64(d["w_uv"]))
+    tol = 1e-5 if dt == torch.float32 else REL_L2
+    assert_close(f64(q_lat), ref_q, rel=tol, what="absorb")
+    assert_close(f64(o), ref_o, rel=tol, what="out_proj")
+
+
+# ----------------------------------------------------------------------------- decode
+
+def _oracle_latent(w, d, q_lat_gpu, pool, sc, seqs=None):
+    return O.decode_latent(f64(q_lat_gpu), f64(d["q_rope"]), pool, sc, d["block_table"].numpy(),
+                           list(w.seq_lens), w.q_len, w.page_size, w.cache_dtype, O.default_scale(),
+                           batch_index=seqs)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_decode_and_step_small(name):
+    w = _small(name)
+    d = _W().make_inputs(w)
+    layer = _layer(w, d)
+    o = _step(layer, d)
+    assert layer.device_error() == 0
+    pool, sc = oracle_pool(w, d)
+    tol = 1e-5 if w.act_dtype == "f32" else REL_L2
+    # decode step alone, on the GPU's own q_lat
+    ref = _oracle_latent(w, d, layer.q_lat, pool, sc)
+    u = f64(layer.u)
+    lse = layer.lse.cpu().numpy()
+    for b, (ru, rl) in ref.items():
+        assert_close(u[b], ru, rel=tol, what=f"u seq {b}")
+        assert np.max(np.abs(lse[b] - rl)) <= 1e-3 * max(1.0, np.max(np.abs(rl))), f"lse seq {b}"
+    # whole step (absorb + decode + out_proj) against the non-absorbed fp64 form
+    full = O.decode_full(f64(d["q_nope"]), f64(d["q_rope"]), f64(d["w_uk"]), f64(d["w_uv"]), pool, sc,
+                         d["block_table"].numpy(), list(w.seq_lens), w.q_len, w.page_size, w.cache_dtype,
+                         O.default_scale(), heads=range(0, w.heads, max(1, w.heads // 16)))
+    hs = list(range(0, w.heads, max(1, w.heads // 16)))
+    og = f64(o)
+    for b, (ro, _, _) in full.items():
+        assert_close(og[b][:, hs], ro, rel=tol, what=f"o seq {b}")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
+def test_split_count_invariance(splits):
+    w = _W().preset("ragged_bf16", batch=4, seq_lens=[3000, 17, 640, 2049], num_splits=splits)
+    d = _W().make_inputs(w)
+    layer = _layer(w, d)
+    _step(layer, d)
+    pool, sc = oracle_pool(w, d)
+    ref = _oracle_latent(w, d, layer.q_lat, pool, sc)
+    u = f64(layer.u)
+    for b, (ru, _) in ref.items():
+        assert_close(u[b], ru, what=f"splits={splits} seq {b}")
+
+
+def test_page_permutation_bit_identical():
+    W = _W()
+    outs = []
+    for shuffle in (False, True):
+        w = W.preset("dsv3_bf16", batch=2, seq_lens=[1000, 333], shuffle_pages=shuffle, num_splits=3)
+        d = W.make_inputs(w)
+        layer = _layer(w, d)
+        o = _step(layer, d)
+        outs.append((bits(layer.u).copy(), bits(o).copy(), d["block_table"]))
+    assert not torch.equal(outs[0][2], outs[1][2])
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1])
+
+
+def test_single_token_sequence_returns_its_row():
+    W = _W()
+    w = W.preset("dsv3_bf16", batch=2, seq_lens=[1, 1])
+    d = W.make_inputs(w)
+    layer = _layer(w, d)
+    _step(layer, d)
+    u = bits(layer.u)
+    c = bits(d["ctx_c_kv"])
+    pool, sc = oracle_pool(w, d)
+    ref = _oracle_latent(w, d, layer.q_lat, pool, sc)
+    lse = layer.lse.cpu().numpy()
+    for b in range(2):
+        assert np.all(u[b, 0] == c[b][None, :]), "softmax over one token must return c_KV exactly"
+        # lse of a single score is the score itself
+        assert np.max(np.abs(lse[b] - ref[b][1])) <= 1e-3 * max(1.0, np.max(np.abs(ref[b][1])))
+
+
+# ----------------------------------------------------------------------------- data faults
+
+def test_bad_block_table_and_seq_len_are_flagged_not_fatal():
+    W = _W()
+    w = W.preset("dsv3_bf16", batch=3, seq_lens=[200, 300, 100], num_splits=2)
+    d = W.make_inputs(w)
+    layer = _layer(w, d)
+    from mla_latent_kv_16_gb300 import capi
+    bt = layer.block_table.clone()
+    bt[0, 1] = w.num_pages + 5          # outside the pool
+    sl = layer.seq_lens.clone()
+    sl[2] = 10 ** 6                     # beyond max_pages * page_size
+    layer.dev_error.zero_()
+    q_lat = layer.absorb(d["q_nope"].cuda())
+    u, lse = capi.mla_decode_paged(q_lat, d["q_rope"].cuda(), layer.cache, layer.scales, bt, sl, w.page_size,
+                                   w.cache_dtype, num_splits=2, dev_error=layer.dev_error)
+    code = layer.device_error()
+    assert code & capi.MLA_DEVERR_BAD_PAGE and code & capi.MLA_DEVERR_BAD_SEQLEN
+    assert torch.isfinite(u[1]).all()   # the healthy sequence is unaffected
+    assert torch.all(u[2] == 0) and torch.all(torch.isinf(lse[2]))
+    # context still usable afterwards
+    layer.dev_error.zero_()
+    _step(layer, d)
+    assert layer.device_error() == 0
+
+
+def test_bad_slot_and_position_in_append_are_flagged():
+    W = _W()
+    w = W.preset("dsv3_bf16", batch=1, seq_lens=[64])
+    d = W.make_inputs(w)
+    layer = _layer(w, d, fill_context=False)
+    sl = d["ctx_slots"].clone()
+    sl[3] = -1
+    sl[5] = w.num_pages * w.page_size
+    pos = d["ctx_positions"].clone()
+    pos[7] = 10 ** 6
+    layer.append(d["ctx_c_kv"].cuda(), d["ctx_k_r"].cuda(), pos.cuda(), sl.cuda())
+    from mla_latent_kv_16_gb300 import capi
+    code = layer.device_error()
+    assert code & capi.MLA_DEVERR_BAD_SLOT and code & capi.MLA_DEVERR_BAD_POSITION
+
+
+def test_invalid_arguments_rejected_synchronously():
+    from mla_latent_kv_16_gb300 import capi
+    q = torch.zeros(2, 4, 128, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(4, 128, 512, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(2, 4, 512, dtype=torch.bfloat16, device="cuda")
+    L = capi.load()
+    bad = capi.MlaDims(4, 64, 512, 64, 128)
+    assert L.mla_absorb_q(q.data_ptr(), w.data_ptr(), out.data_ptr(), 2, bad, capi.MLA_BF16, None) == \
+        capi.MLA_ERR_INVALID_ARG
+    assert L.mla_absorb_q(q.data_ptr() + 2, w.data_ptr(), out.data_ptr(), 2, capi.dims(4), capi.MLA_BF16, None) == \
+        capi.MLA_ERR_INVALID_ARG
+    assert L.mla_decode_paged(q.data_ptr(), q.data_ptr(), w.data_ptr(), None, None, None, 1, 1, 4, 4, 64, 0.1, 0,
+                              None, 0, out.data_ptr(), None, None, capi.dims(4), capi.MLA_BF16, capi.MLA_E4M3,
+                              None) == capi.MLA_ERR_INVALID_ARG
+
+
+# ----------------------------------------------------------------------------- full size
+
+@pytest.mark.parametrize("name,nseq", [("dsv3_bf16", 32), ("ragged_bf16", 6), ("long_splitkv_bf16", 2),
+                                       ("fp8_lq2", 6), ("tiny_fp32", 2)])
+def test_full_size_workloads(name, nseq):
+    """The benchmark's launch configuration at full size; decode checked on
+    seeded sequence samples (all sequences for the DeepSeek-V3-shaped case)."""
+    W = _W()
+    w = W.preset(name)
+    d = W.make_inputs(w)
+    layer = _layer(w, d)
+    o = _step(layer, d)
+    assert layer.device_error() == 0
+    seqs = W.sample_sequences(w, nseq)
+    mask = seq_token_mask(w, seqs)
+    pool, sc = oracle_pool(w, d, token_mask=mask)
+    # cache bytes of the sampled sequences are bit-exact
+    gcache = bits(layer.cache).reshape(pool.shape[0], -1)
+    slots = d["ctx_slots"].numpy()[mask]
+    assert np.array_equal(gcache[slots].view(np.uint8), pool[slots].view(np.uint8))
+    ref = _oracle_latent(w, d, layer.q_lat, pool, sc, seqs)
+    u = f64(layer.u)
+    tol = 1e-5 if w.act_dtype == "f32" else REL_L2
+    for b, (ru, _) in ref.items():
+        assert_close(u[b], ru, rel=tol, what=f"{name} u seq {b}")
+    # end to end on a few heads of two sequences, non-absorbed form
+    hs = [0, 37, 127] if w.heads == 128 else [0, 15]
+    full = O.decode_full(f64(d["q_nope"]), f64(d["q_rope"]), f64(d["w_uk"]), f64(d["w_uv"]), pool, sc,
+                         d["block_table"].numpy(), list(w.seq_lens), w.q_len, w.page_size, w.cache_dtype,
+                         O.default_scale(), batch_index=seqs[:2], heads=hs)
+    og = f64(o)
+    for b, (ro, _, _) in full.items():
+        assert_close(og[b][:, hs], ro, rel=tol, what=f"{name} o seq {b}")
