@@ -75,6 +75,8 @@ typedef void *mla_stream_t; /* cudaStream_t */
 #define MLA_DEVERR_BAD_SEQLEN 2   /* seq_len < q_len or > max_pages*page_size   */
 #define MLA_DEVERR_BAD_SLOT 4     /* slot_mapping entry outside the pool        */
 #define MLA_DEVERR_BAD_POSITION 8 /* position outside [0, max_pos)              */
+#define MLA_DEVERR_TIMEOUT 16     /* a kernel-internal wait ran out of time; the
+                                     affected outputs are unspecified           */
 
 /* E4M3 cache: one fp32 scale per token per group; groups of the 576-value row
  * are [0,128) [128,256) [256,384) [384,512) [512,576). */

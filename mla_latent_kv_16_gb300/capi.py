@@ -23,6 +23,7 @@ MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_WORKSPAC
 MLA_F32, MLA_BF16, MLA_E4M3 = 0, 1, 2
 DTYPE_CODE = {"f32": MLA_F32, "bf16": MLA_BF16, "e4m3": MLA_E4M3}
 MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_SEQLEN, MLA_DEVERR_BAD_SLOT, MLA_DEVERR_BAD_POSITION = 1, 2, 4, 8
+MLA_DEVERR_TIMEOUT = 16
 
 EXPORTED = ("mla_status_string", "mla_version", "mla_rope_table", "mla_cache_append", "mla_absorb_q",
             "mla_decode_num_splits", "mla_decode_workspace_size", "mla_decode_paged", "mla_out_proj",

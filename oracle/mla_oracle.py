@@ -330,6 +330,25 @@ def attend_nonabsorbed(q_nope, q_rope, w_uk, w_uv, rows: np.ndarray, scale: floa
     return o, u, lse
 
 
+def round_bf16(x) -> np.ndarray:
+    """fp64 values rounded as a GPU stores an fp32 result in bf16: to fp32
+    (nearest) and then to bf16 (nearest-even); returned as fp64."""
+    return bf16_bits_to_f64(f32_to_bf16_bits(np.asarray(x, np.float64).astype(np.float32)))
+
+
+def decode_full_bf16_interface(q_nope, q_rope, w_uk, w_uv, pool, scales, block_table, seq_lens, q_len: int,
+                               page_size: int, cache_dtype: str, scale: float, batch_index=None):
+    """The decode step computed exactly except that the two intermediates the
+    library exchanges in bf16 -- the absorbed query q_lat and the latent
+    output u -- are rounded to bf16 between the steps. Returns dict b -> o
+    [Lq,H,128]. Used to separate a kernel's own error from the rounding its
+    bf16 interface implies."""
+    q_lat = round_bf16(absorb_q(q_nope, w_uk))
+    lat = decode_latent(q_lat, q_rope, pool, scales, block_table, seq_lens, q_len, page_size, cache_dtype, scale,
+                        batch_index=batch_index)
+    return {b: out_proj(round_bf16(u), w_uv) for b, (u, _) in lat.items()}
+
+
 def default_scale(d_nope: int = D_NOPE, d_rope: int = D_ROPE) -> float:
     """1/sqrt(d_h + d_R). [P1] §3.1; [P2] self.scale; [P5] §2."""
     return 1.0 / math.sqrt(d_nope + d_rope)

@@ -117,6 +117,25 @@ def test_absorb_and_out_proj(name, n_tok):
 
 # ----------------------------------------------------------------------------- decode
 
+def _check_o(w, d, og, full, pool, sc, hs, tol, seqs=None):
+    """End-to-end output o: rel-L2 against the exact fp64 (non-absorbed) oracle,
+    and max-abs against the oracle with the ABI's bf16 interface roundings
+    (q_lat and u rounded to bf16 between the steps). Rounding q_lat alone moves
+    o by max-abs 0.05 on the x4-outlier workload, so the exact oracle cannot
+    carry the max-abs bound for a bf16 interface; fp32 paths use the exact one."""
+    iface = None
+    if w.act_dtype != "f32":
+        iface = O.decode_full_bf16_interface(f64(d["q_nope"]), f64(d["q_rope"]), f64(d["w_uk"]), f64(d["w_uv"]), pool,
+                                             sc, d["block_table"].numpy(), list(w.seq_lens), w.q_len, w.page_size,
+                                             w.cache_dtype, O.default_scale(), batch_index=list(full))
+    for b, (ro, _, _) in full.items():
+        if iface is None:
+            assert_close(og[b][:, hs], ro, **tol, what=f"o seq {b}")
+        else:
+            assert_close(og[b][:, hs], ro, rel=tol["rel"], mabs=float("inf"), what=f"o seq {b} vs exact")
+            assert_close(og[b][:, hs], iface[b][:, hs], **tol, what=f"o seq {b} vs bf16-interface oracle")
+
+
 def _oracle_latent(w, d, q_lat_gpu, pool, sc, seqs=None):
     return O.decode_latent(f64(q_lat_gpu), f64(d["q_rope"]), pool, sc, d["block_table"].numpy(),
                            list(w.seq_lens), w.q_len, w.page_size, w.cache_dtype, O.default_scale(),
@@ -144,9 +163,7 @@ def test_decode_and_step_small(name):
                          d["block_table"].numpy(), list(w.seq_lens), w.q_len, w.page_size, w.cache_dtype,
                          O.default_scale(), heads=range(0, w.heads, max(1, w.heads // 16)))
     hs = list(range(0, w.heads, max(1, w.heads // 16)))
-    og = f64(o)
-    for b, (ro, _, _) in full.items():
-        assert_close(og[b][:, hs], ro, **tol, what=f"o seq {b}")
+    _check_o(w, d, f64(o), full, pool, sc, hs, tol)
 
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
@@ -200,6 +217,7 @@ def test_bad_block_table_and_seq_len_are_flagged_not_fatal():
     w = W.preset("dsv3_bf16", batch=3, seq_lens=[200, 300, 100], num_splits=2)
     d = W.make_inputs(w)
     layer = _layer(w, d)
+    _step(layer, d)                     # appends the step's new tokens: every visible row is written
     from mla_latent_kv_16_gb300 import capi
     bt = layer.block_table.clone()
     bt[0, 1] = w.num_pages + 5          # outside the pool
@@ -281,6 +299,4 @@ def test_full_size_workloads(name, nseq):
     full = O.decode_full(f64(d["q_nope"]), f64(d["q_rope"]), f64(d["w_uk"]), f64(d["w_uv"]), pool, sc,
                          d["block_table"].numpy(), list(w.seq_lens), w.q_len, w.page_size, w.cache_dtype,
                          O.default_scale(), batch_index=seqs[:2], heads=hs)
-    og = f64(o)
-    for b, (ro, _, _) in full.items():
-        assert_close(og[b][:, hs], ro, **tol, what=f"{name} o seq {b}")
+    _check_o(w, d, f64(o), full, pool, sc, hs, tol, seqs=seqs[:2])
