@@ -5,8 +5,8 @@ sequence, bf16 paged cache, page size 64, shuffled pages) through the C ABI.
 
 A step = append of the step's new tokens + absorb_q + paged decode (+ split
 combine) + out_proj. The latent cache (151 MB) is larger than L2, and L2 is
-additionally flushed (a 256 MiB write) before every timed step, outside the
-per-step CUDA-event window.
+additionally flushed before every timed step, outside the per-step CUDA-event
+window, by reading a 256 MiB buffer.
 
 Prints ONE JSON line (rank 0). --impl reference times the fp64 CPU oracle on a
 bounded sample of the same workload instead.
@@ -32,7 +32,7 @@ METRIC = "MLA decode latent-cache GB/s & tokens/s at 1 GB300; % of HBM roofline"
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "dsv3_bf16"
 FALLBACK_HBM_GBS = 6800.0
-L2_FLUSH_BYTES = 256 << 20
+L2_FLUSH_BYTES = 256 << 20  # read (not written) before every timed step
 
 
 def parse():
@@ -210,79 +210,78 @@ def run_ours(args):
     s = step_inputs(d)
     torch.cuda.synchronize()
     assert layer.device_error() == 0, "device error while filling the cache"
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    # L2 flush by READING a buffer larger than L2: it evicts the previous step's
+    # data and leaves only clean lines (a write would leave dirty lines whose
+    # write-back would then compete with the timed step for HBM)
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
+    # one decode step = append + absorb + decode (+ combine) + out_proj, replayed
+    # as a CUDA graph so that host launch overhead stays out of the step
     def one_step():
-        layer.append(s["new_c_kv"], s["new_k_r"], s["new_positions"], s["new_slots"])
-        q_lat = layer.absorb(s["q_nope"])
-        ev_d0.record(stream)
-        u, _ = layer.decode(q_lat, s["q_rope"])
-        ev_d1.record(stream)
-        layer.out_proj(u)
+        layer.step(**s)
 
-    ev_d0 = torch.cuda.Event(enable_timing=True)
-    ev_d1 = torch.cuda.Event(enable_timing=True)
+    def decode_only():
+        layer.decode(layer.q_lat, s["q_rope"])
+
+    g_step = layer.capture(one_step)
+    g_dec = layer.capture(decode_only)
+
+    def timed(graph, n, clk=None):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        if clk is not None:
+            clk.start()
+            time.sleep(0.3)
+        for i in range(n):
+            flush.sum()
+            evs[i][0].record(stream)
+            graph.replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
     for _ in range(args.warmup):
-        flush.fill_(1)
-        one_step()
+        flush.sum()
+        g_step.replay()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clk = ClockSampler(local)
-    clk.start()
-    time.sleep(0.3)
-    for i in range(args.steps):
-        flush.fill_(i & 0xff)
-        e_s, d0, d1, e_e = ev[i]
-        e_s.record(stream)
-        ev_d0, ev_d1 = d0, d1
-        one_step()
-        e_e.record(stream)
-    torch.cuda.synchronize()
+    step_ms = timed(g_step, args.steps, clk)
     clocks = clk.stop()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, _, _, b in ev]
-    dec_ms = [a.elapsed_time(b) for _, a, b, _ in ev]
     tot = sum(step_ms)
     if world > 1:
         t = torch.tensor([tot], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         tot = float(t.item())
+    for _ in range(args.warmup):
+        flush.sum()
+        g_dec.replay()
+    dec_ms = timed(g_dec, args.steps)
     assert layer.device_error() == 0
 
-    # end to end through the public API with pinned host buffers
+    # end to end through the public API: the step's inputs copied in from pinned
+    # host memory and o copied back, inside the timed region (also a graph)
     host_in = {k: v.cpu().pin_memory() for k, v in s.items()}
     host_out = torch.empty(layer.o.shape, dtype=layer.o.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = host_out.numel() * host_out.element_size()
-    dev_in = {k: torch.empty_like(v) for k, v in s.items()}
 
     def e2e_step():
         for k in host_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        o = layer.step(**dev_in)
-        host_out.copy_(o, non_blocking=True)
+            s[k].copy_(host_in[k], non_blocking=True)
+        layer.step(**s)
+        host_out.copy_(layer.o, non_blocking=True)
 
-    for _ in range(max(3, args.warmup)):
-        flush.fill_(1)
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = []
-    for i in range(args.steps):
-        flush.fill_(i & 0xff)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        b.synchronize()
-        e2e_ms.append(a.elapsed_time(b))
+    g_e2e = layer.capture(e2e_step)
+    for _ in range(args.warmup):
+        flush.sum()
+        g_e2e.replay()
+    e2e_ms = timed(g_e2e, args.steps)
     e2e_tot = sum(e2e_ms)
     if world > 1:
         t = torch.tensor([e2e_tot], device="cuda")
@@ -309,7 +308,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": w.cache_dtype, "data": "synthetic (seeded N(0,1) values, N(0,1/sqrt(512)) weights)",
         "config": {"workload": w.name, "batch": w.batch, "q_len": w.q_len, "heads": w.heads,
                    "seq_len": int(max(w.seq_lens)), "page_size": w.page_size, "cache_dtype": w.cache_dtype,
-                   "num_splits": splits, "l2": "flushed (256 MiB write) before every timed step; cache > L2",
+                   "num_splits": splits, "l2": "flushed before every timed step by reading a 256 MiB buffer (clean lines); cache > L2",
                    "parallelism": f"dp{world} (independent replicas, no collective)"},
         "tokens_per_s": round(tok_s, 1),
         "decode_call_ms": round(dec, 5),

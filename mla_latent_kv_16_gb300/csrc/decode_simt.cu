@@ -213,26 +213,35 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
   if (threadIdx.x == 0 && a.lse_out != nullptr) a.lse_out[row] = none ? -CUDART_INF_F : mx + logf(tot);
 }
 
+// Opt the kernel into its dynamic shared memory once per device (a host call
+// that costs microseconds, kept out of every launch).
+template <typename K>
+cudaError_t ensure_smem(K kernel, size_t bytes, int& done_for) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || done_for == dev) return e;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) done_for = dev;
+  return e;
+}
+
+template <typename T, int kCache>
+cudaError_t launch_decode_c(const DecodeArgs& a, cudaStream_t s) {
+  static int done_for = -1;
+  const cudaError_t e = ensure_smem(decode_simt_kernel<T, kCache>, kSimtSmem, done_for);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.num_splits, (a.heads + kHG - 1) / kHG, a.batch * a.q_len);
+  decode_simt_kernel<T, kCache><<<grid, 256, kSimtSmem, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
-  dim3 grid(a.num_splits, (a.heads + kHG - 1) / kHG, a.batch * a.q_len);
-  cudaError_t e = cudaSuccess;
   switch (a.cache_dtype) {
-    case MLA_F32:
-      e = cudaFuncSetAttribute(decode_simt_kernel<T, MLA_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSimtSmem);
-      if (e == cudaSuccess) decode_simt_kernel<T, MLA_F32><<<grid, 256, kSimtSmem, s>>>(a);
-      break;
-    case MLA_BF16:
-      e = cudaFuncSetAttribute(decode_simt_kernel<T, MLA_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSimtSmem);
-      if (e == cudaSuccess) decode_simt_kernel<T, MLA_BF16><<<grid, 256, kSimtSmem, s>>>(a);
-      break;
-    default:
-      e = cudaFuncSetAttribute(decode_simt_kernel<T, MLA_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSimtSmem);
-      if (e == cudaSuccess) decode_simt_kernel<T, MLA_E4M3><<<grid, 256, kSimtSmem, s>>>(a);
-      break;
+    case MLA_F32: return launch_decode_c<T, MLA_F32>(a, s);
+    case MLA_BF16: return launch_decode_c<T, MLA_BF16>(a, s);
+    default: return launch_decode_c<T, MLA_E4M3>(a, s);
   }
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
 }
 
 }  // namespace

@@ -9,27 +9,25 @@
 // dimension: S[128 x 64] = Q[128 x 576] * C^T per 64-token tile, and
 // O[128 x 512] += P[128 x 64] * C[64 x 512].
 //
-// GB300 mapping. O alone (128 x 512 fp32) fills a whole SM's TMEM, and Q
-// (128 x 576 bf16) would fill most of its shared memory, so each work item is
-// a cluster of two CTAs that split the row by columns:
-//   CTA rank 0: latent columns [0, 256)             -> K slice of S, O[:, 0:256]
-//   CTA rank 1: latent [256, 512) + RoPE [512, 576) -> K slice of S, O[:, 256:512]
-// Each CTA TMA-loads only its own columns of every page (HBM is read once),
-// keeps its Q slice in TMEM (A operand), computes a partial S, and the pair
-// exchange partial S through distributed shared memory with asynchronous
-// stores that complete on the receiver's mbarrier. Both then hold the same
-// full S (fp32 addition is commutative), run the same online softmax and feed
-// P (bf16, in TMEM) into their own half of the PV product.
+// GB300 mapping. O alone (128 x 512 fp32) fills a whole SM's TMEM, so every
+// work item (sequence, query, KV split) runs on two CTAs, one per half of the
+// latent output: CTA "half" r accumulates O[:, 256r : 256r+256] in TMEM. Both
+// CTAs compute the full score tile (the QK product is duplicated: exchanging
+// 32 KB of fp32 partial scores per page between SMs would cost more than the
+// MMAs it saves), so the pair never communicates. Q (128 x 576 bf16) is split
+// between TMEM (latent 0-255 and RoPE 512-575: 160 columns, the A operand of
+// those MMAs) and shared memory (latent 256-511, 64 KB). The two CTAs of a
+// pair form a cluster so they run together and read each page from L2 once.
 //
-// Warp roles (320 threads): warp 0 issues TMA loads (3-stage ring); warp 1
-// allocates TMEM and issues MMAs from an event loop (QK of a page as soon as
-// its data and the S buffer are free, PV as soon as P is written); warps 2-9
-// own TMEM lanes 0-127 (= heads), two warps per lane quarter, each covering 32
-// of the 64 tokens of a page. Page i+1's partial scores are sent to the peer
-// before page i is softmaxed, so the exchange overlaps the softmax.
+// Per CTA: warp 0 issues TMA loads of whole 576-wide pages (2-stage ring);
+// warp 1 allocates TMEM and issues MMAs from an event loop (QK of a page as
+// soon as its data and the score buffer are free, PV as soon as P is
+// written); warps 2-9 own TMEM lanes 0-127 (= heads), two warps per lane
+// quarter, each covering 32 of the 64 tokens of a page: online softmax with a
+// lazily rescaled running max, P to TMEM in bf16, tail masking, epilogue.
 //
 // Every wait is bounded: on a timeout the CTA raises an error bit, stops, waits
-// for its own copies and MMAs, leaves the cluster barrier and frees TMEM.
+// for its own copies and MMAs and frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
@@ -47,30 +45,29 @@ constexpr int kSmxWarps = 8;
 constexpr int kSmxThreads = kSmxWarps * 32;
 constexpr int kThreads = 64 + kSmxThreads;
 constexpr int kTileTok = 64;
-constexpr int kStages = 3;
-constexpr int kBoxBytes = kTileTok * 128;  // 64 rows x 64 bf16, 128-byte swizzled
-constexpr int kMaxBoxes = 5;
-constexpr int kStageBytes = kMaxBoxes * kBoxBytes;
+constexpr int kStages = 2;
+constexpr int kBoxBytes = kTileTok * 128;      // 64 rows x 64 bf16, 128-byte swizzled
+constexpr int kBoxes = kRow / 64;              // 9 boxes per 576-wide page
+constexpr int kStageBytes = kBoxes * kBoxBytes;
+constexpr int kQBoxBytes = 128 * 128;          // Q in smem: 128 heads x 64 bf16
 constexpr uint32_t kTmemCols = 512;
 // TMEM column map (fp32 columns)
 constexpr uint32_t kTmO = 0;    // O half: 256 columns
 constexpr uint32_t kTmS = 256;  // S tile: 64 columns
 constexpr uint32_t kTmP = 320;  // P tile: 64 bf16 = 32 columns
-constexpr uint32_t kTmQ = 352;  // Q slice: 256 (+64) bf16 = 128 (+32) columns
+constexpr uint32_t kTmQ = 352;  // Q latent [0,256) + RoPE [512,576): 128 + 32 columns
 // Lazy rescale: keep a stale row max until the new one exceeds it by 2^8.
 constexpr float kRescaleLog2 = 8.0f;
 
 struct __align__(1024) Smem {
-  uint8_t stage[kStages][kStageBytes];
-  // partial-S exchange slots: [slot][region = softmax warp][token group of 4][lane]
-  float4 xbuf[2][kSmxWarps][8][32];
-  float red[2][2][128];               // row-max halves per page parity: [parity][half][head]
-  float lsum[2][128];                 // row-sum halves for the epilogue
+  uint8_t stage[kStages][kStageBytes];  // whole pages, 9 boxes of 64 columns
+  uint8_t q[4][kQBoxBytes];             // Q latent [256,512): 4 boxes of 64 columns
+  float red[2][2][128];                 // row-max halves per page parity: [parity][half][head]
+  float lsum[2][128];                   // row-sum halves for the epilogue
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full, s_empty, p_full, pv_done, q_ready, drain;
-  uint64_t x_full[2][kSmxWarps];  // receiver: peer's page landed in a region (arming + tx bytes)
-  uint64_t x_empty[2];  // sender side: the peer has consumed its slot
+  uint64_t q_smem_full;  // TMA of Q latent [256,512) into shared memory landed
   uint64_t red_bar[2];  // softmax warps: row-max halves written (per page parity)
   uint64_t sum_bar;     // softmax warps: row-sum halves written (epilogue)
   uint32_t tmem_base;
@@ -78,8 +75,7 @@ struct __align__(1024) Smem {
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
-constexpr uint32_t kXBytes = 32 * 32 * 4;                 // one region of one page of partial scores
-constexpr int kPlain = 0, kAcqCluster = 1, kSleep = 2;    // mbar_wait modes
+constexpr int kPlain = 0, kSleep = 2;  // mbar_wait modes
 
 // Wait bounded only by time (teardown: our own copies / MMAs must land).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_t* dev_error) {
@@ -88,26 +84,26 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_
 }
 
 // Outputs of a work item with nothing to attend to (or rejected data).
-__device__ void write_empty(const DecodeArgs& a, int64_t row0, int bj, int split, uint32_t rank) {
+__device__ void write_empty(const DecodeArgs& a, int64_t row0, int bj, int split, uint32_t half) {
   const int S = a.num_splits;
   if (S == 1) {
-    uint4* u = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.u_out) + row0 * kDC + rank * 256);
+    uint4* u = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.u_out) + row0 * kDC + half * 256);
     for (int i = threadIdx.x; i < 128 * 32; i += blockDim.x) u[(i >> 5) * (kDC / 8) + (i & 31)] = make_uint4(0, 0, 0, 0);
-    if (rank == 0 && a.lse_out != nullptr)
+    if (half == 0 && a.lse_out != nullptr)
       for (int h = threadIdx.x; h < 128; h += blockDim.x) a.lse_out[row0 + h] = -CUDART_INF_F;
-  } else if (rank == 0) {
+  } else if (half == 0) {
     for (int h = threadIdx.x; h < 128; h += blockDim.x)
       a.part_lse[(static_cast<int64_t>(bj) * S + split) * 128 + h] = -CUDART_INF_F;
   }
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
+                     const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem* sm = reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t peer = rank ^ 1u;
+  const uint32_t ohalf = blockIdx.x & 1u;  // which latent half of O this CTA owns
 
   // ---- work item: (sequence b, query j, split) -- identical in both CTAs
   const int item = blockIdx.x >> 1;
@@ -119,7 +115,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int64_t row0 = static_cast<int64_t>(bj) * 128;
   const int L = a.seq_lens[b];
   const bool bad_len = (L < Lq) || (static_cast<int64_t>(L) > static_cast<int64_t>(a.max_pages) * P);
-  if (bad_len && rank == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_SEQLEN);
+  if (bad_len && ohalf == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_SEQLEN);
   const int n_vis = bad_len ? 0 : L - Lq + j + 1;
   const int tok_begin = split * a.pages_per_split * P;
   const int tok_end = min(n_vis, (split + 1) * a.pages_per_split * P);
@@ -132,18 +128,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       local_bad |= (pp < 0 || pp >= a.num_pages) ? 1 : 0;
     }
     if (__syncthreads_or(local_bad)) {
-      if (rank == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_PAGE);
+      if (ohalf == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_PAGE);
     } else {
       n_tiles = (tok_end - tok_begin + kTileTok - 1) / kTileTok;
     }
   }
   if (n_tiles == 0) {
-    write_empty(a, row0, bj, split, rank);
+    write_empty(a, row0, bj, split, ohalf);
     return;
   }
-
-  const uint32_t nbox = rank == 0 ? 4u : 5u;  // 64-column boxes this CTA loads
-  const uint32_t col0 = rank * 256u;
+  const uint32_t col0 = ohalf * 256u;  // first latent column of this CTA's O half
 
   // ---- set-up
   if (threadIdx.x == 0) {
@@ -157,49 +151,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm->pv_done), 1);
     mbar_init(smem_u32(&sm->q_ready), kSmxWarps);
     mbar_init(smem_u32(&sm->drain), 1);
-    for (int x = 0; x < 2; ++x) {
-      for (int r = 0; r < kSmxWarps; ++r) mbar_init(smem_u32(&sm->x_full[x][r]), 1);  // arming (+ peer bytes)
-      mbar_init(smem_u32(&sm->x_empty[x]), kSmxWarps);  // one remote arrival per peer warp
-    }
+    mbar_init(smem_u32(&sm->q_smem_full), 1);
     for (int x = 0; x < 2; ++x) mbar_init(smem_u32(&sm->red_bar[x]), kSmxWarps);
     mbar_init(smem_u32(&sm->sum_bar), kSmxWarps);
     sm->abort_flag = 0;
     fence_mbar_init_cluster();
-    for (int x = 0; x < 2; ++x)
-      for (int r = 0; r < kSmxWarps; ++r) mbar_arrive_expect_tx(smem_u32(&sm->x_full[x][r]), kXBytes);
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&tmap);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap);
+    prefetch_tmap(&qmap);
+  }
   if (warp == 1) tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // the peer's barriers exist before anything remote happens
   const uint32_t tmem = sm->tmem_base;
   volatile int32_t* abort_flag = &sm->abort_flag;
 
   if (warp == 0) {
-    // ================= TMA producer
+    // ================= TMA producer: whole pages
     if (lane == 0) {
+      // Q latent [256,512) of the 128 heads: four 128 x 64 boxes
+      mbar_arrive_expect_tx(smem_u32(&sm->q_smem_full), 4 * kQBoxBytes);
+      for (int k = 0; k < 4; ++k)
+        tma_load_2d_nohint(smem_u32(sm->q[k]), &qmap, smem_u32(&sm->q_smem_full), 256 + 64 * k,
+                           static_cast<int32_t>(row0));
       const uint64_t pol = l2_policy_evict_first();
       int issued = 0;
-      // the page of tile i+1 is fetched while tile i waits for its stage
-      int32_t page_next = bt[tok_begin / P];
+      auto y_of = [&](int t) {  // pool row of tile t
+        const int tok = tok_begin + t * kTileTok;
+        return bt[tok / P] * P + (tok % P);
+      };
+      // pages kPrefetch tiles ahead are pulled into L2 so that a stage refill
+      // (issued only when PV frees the stage) is an L2 hit
+      constexpr int kPrefetch = 2;
+      for (int t = 0; t < min(n_tiles, kPrefetch); ++t) {
+        const int32_t yp = y_of(t);
+        for (int k = 0; k < kBoxes; ++k) tma_prefetch_l2_2d(&tmap, 64 * k, yp);
+      }
+      int32_t y_next = y_of(0);
       for (int i = 0; i < n_tiles; ++i) {
         const int st = i % kStages;
-        const int tok = tok_begin + i * kTileTok;
-        const int32_t page = page_next;
-        if (i + 1 < n_tiles) page_next = bt[(tok + kTileTok) / P];
+        const int32_t y = y_next;
+        if (i + 1 < n_tiles) y_next = y_of(i + 1);
+        if (i + kPrefetch < n_tiles) {
+          const int32_t yp = y_of(i + kPrefetch);
+          for (int k = 0; k < kBoxes; ++k) tma_prefetch_l2_2d(&tmap, 64 * k, yp);
+        }
         if (!mbar_wait<kSleep>(smem_u32(&sm->kv_empty[st]), ((i / kStages) & 1) ^ 1, abort_flag, a.dev_error)) break;
-        const int32_t y = page * P + (tok % P);
         const uint32_t bar = smem_u32(&sm->kv_full[st]);
-        mbar_arrive_expect_tx(bar, nbox * kBoxBytes);
+        mbar_arrive_expect_tx(bar, kStageBytes);
         const uint32_t dst = smem_u32(sm->stage[st]);
-        for (uint32_t k = 0; k < nbox; ++k)
-          tma_load_2d(dst + k * kBoxBytes, &tmap, bar, static_cast<int32_t>(col0 + 64u * k), y, pol);
+#pragma unroll
+        for (int k = 0; k < kBoxes; ++k) tma_load_2d(dst + k * kBoxBytes, &tmap, bar, 64 * k, y, pol);
         issued = i + 1;
       }
       for (int i = max(0, issued - kStages); i < issued; ++i)
         drain_wait(smem_u32(&sm->kv_full[i % kStages]), (i / kStages) & 1, a.dev_error);
+      drain_wait(smem_u32(&sm->q_smem_full), 0, a.dev_error);
     }
   } else if (warp == 1) {
     // ================= MMA issuer: event loop over "QK of page qk" and "PV of page pv"
@@ -207,11 +216,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdQK = idesc_bf16_f32(128, kTileTok, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, 256, false, true);
       // descriptor start addresses advance in 16-byte units in the low bits
-      const uint64_t dPV0 = sdesc_sw128(smem_u32(sm->stage[0]), kBoxBytes, 1024);
-      const uint64_t dQK0 = sdesc_sw128(smem_u32(sm->stage[0]), 16, 1024);
+      const uint64_t dPV0 = sdesc_sw128(smem_u32(sm->stage[0]) + ohalf * 4 * kBoxBytes, kBoxBytes, 1024);
+      const uint64_t dKB0 = sdesc_sw128(smem_u32(sm->stage[0]), 16, 1024);  // page as K-major B
+      const uint64_t dQA0 = sdesc_sw128(smem_u32(sm->q[0]), 16, 1024);      // Q latent [256,512) as A
       constexpr uint64_t kStageDesc = kStageBytes >> 4;
-      const bool rope = (nbox == 5);
-      bool ok = mbar_wait<kSleep>(smem_u32(&sm->q_ready), 0, abort_flag, a.dev_error);
+      bool ok = mbar_wait<kSleep>(smem_u32(&sm->q_ready), 0, abort_flag, a.dev_error) &&
+                mbar_wait<kSleep>(smem_u32(&sm->q_smem_full), 0, abort_flag, a.dev_error);
       tc_fence_after();
       int qk = 0, pv = 0;
       long long idle_since = 0;
@@ -221,17 +231,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (qk < n_tiles && mbar_test_wait(smem_u32(&sm->kv_full[qk % kStages]), (qk / kStages) & 1) &&
             (qk == 0 || mbar_test_wait(smem_u32(&sm->s_empty), (qk - 1) & 1))) {
           tc_fence_after();
-          const uint64_t d0 = dQK0 + static_cast<uint64_t>(qk % kStages) * kStageDesc;
+          const uint64_t db = dKB0 + static_cast<uint64_t>(qk % kStages) * kStageDesc;
+          // latent [0,256): A = Q from TMEM, B = page boxes 0-3
 #pragma unroll
           for (uint32_t kk = 0; kk < 16; ++kk)
-            mma_ts(tmem + kTmS, tmem + kTmQ + kk * 8u, d0 + (((kk >> 2) * kBoxBytes + (kk & 3u) * 32u) >> 4), kIdQK,
+            mma_ts(tmem + kTmS, tmem + kTmQ + kk * 8u, db + (((kk >> 2) * kBoxBytes + (kk & 3u) * 32u) >> 4), kIdQK,
                    kk > 0 ? 1u : 0u);
-          if (rope) {
+          // RoPE [512,576): A = Q from TMEM, B = page box 8
 #pragma unroll
-            for (uint32_t kk = 16; kk < 20; ++kk)
-              mma_ts(tmem + kTmS, tmem + kTmQ + kk * 8u, d0 + (((kk >> 2) * kBoxBytes + (kk & 3u) * 32u) >> 4),
-                     kIdQK, 1u);
-          }
+          for (uint32_t kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + kTmS, tmem + kTmQ + 128u + kk * 8u, db + ((8 * kBoxBytes + kk * 32u) >> 4), kIdQK, 1u);
+          // latent [256,512): A = Q from shared memory, B = page boxes 4-7
+#pragma unroll
+          for (uint32_t kk = 0; kk < 16; ++kk)
+            mma_ss(tmem + kTmS, dQA0 + (((kk >> 2) * kQBoxBytes + (kk & 3u) * 32u) >> 4),
+                   db + (((4 + (kk >> 2)) * kBoxBytes + (kk & 3u) * 32u) >> 4), kIdQK, 1u);
           mma_commit(smem_u32(&sm->s_full));
           ++qk;
           did = true;
@@ -265,7 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       drain_wait(smem_u32(&sm->drain), 0, a.dev_error);
     }
   } else {
-    // ================= softmax / exchange / epilogue
+    // ================= softmax / epilogue
     // thread = (head h = TMEM lane, half of the page's 64 tokens)
     const uint32_t q4 = static_cast<uint32_t>(warp & 3);
     const int half = (warp - 2) >> 2;
@@ -276,26 +290,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto wwait = [&](uint64_t* bar, uint32_t par) {
       return __all_sync(0xffffffffu, mbar_wait<kPlain>(smem_u32(bar), par, abort_flag, a.dev_error));
     };
-    auto wwait_cluster = [&](uint64_t* bar, uint32_t par) {
-      return __all_sync(0xffffffffu, mbar_wait<kAcqCluster>(smem_u32(bar), par, abort_flag, a.dev_error));
-    };
-    // Q slice of this head into TMEM (bf16 pairs, lower K index in the low half).
-    // Chunks of 32 columns: half 0 writes chunks 0-1, half 1 chunks 2-3 (+4 = RoPE).
+    // Q of this head into TMEM (bf16 pairs, lower K index in the low half):
+    // half 0 writes latent [0,128) and the RoPE part, half 1 latent [128,256).
+    // Latent [256,512) reaches shared memory by TMA (issued by the producer).
     {
-      const uint4* ql = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_lat) + (row0 + h) * kDC + col0);
+      const uint4* ql = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_lat) + (row0 + h) * kDC);
       const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_rope) + (row0 + h) * kDRope);
-      const bool do_rope = (half == 1 && rank == 1);
       uint4 x[24];  // every load in flight at once: one memory round trip
 #pragma unroll
       for (int v = 0; v < 16; ++v) x[v] = ql[half * 16 + v];
-      if (do_rope) {
+      if (half == 0) {
 #pragma unroll
         for (int v = 0; v < 8; ++v) x[16 + v] = qr[v];
       }
       uint32_t r[32];
 #pragma unroll
       for (int c = 0; c < 3; ++c) {
-        if (c == 2 && !do_rope) break;
+        if (c == 2 && half != 0) break;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           r[4 * v] = x[c * 8 + v].x;
@@ -312,53 +323,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     const float c2 = a.softmax_scale * kLog2e;  // scores in log2 units
     float m = -CUDART_INF_F, l = 0.0f;          // l: this thread's half of the row sum
-    const int region = half * 4 + static_cast<int>(q4);  // this warp's exchange region
-    const uint32_t xbuf_peer = map_to_rank(smem_u32(&sm->xbuf[0][region][0][lane]), peer);
-    const uint32_t xfull_peer[2] = {map_to_rank(smem_u32(&sm->x_full[0][region]), peer),
-                                    map_to_rank(smem_u32(&sm->x_full[1][region]), peer)};
-    const uint32_t xempty_peer[2] = {map_to_rank(smem_u32(&sm->x_empty[0]), peer),
-                                     map_to_rank(smem_u32(&sm->x_empty[1]), peer)};
     bool ok = true;
-    // Own partial scores of page i (s) and page i+1 (sn), this thread's 32 tokens.
-    float s[32], sn[32];
-    auto load_and_send = [&](int pg, float (&dst)[32]) -> bool {
-      if (!wwait(&sm->s_full, pg & 1)) return false;
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      if (!wwait(&sm->s_full, i & 1)) { ok = false; break; }
       tc_fence_after();
-      tmem_ld32_sync(tS, dst);
+      float s[32];
+      tmem_ld32_sync(tS, s);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm->s_empty));  // S may be overwritten by QK(pg+1)
-      // asynchronous stores into the peer's slot pg&1, counted on its barrier,
-      // once the peer has consumed page pg-2 from that slot
-      const int xs = pg & 1;
-      if (!wwait_cluster(&sm->x_empty[xs], ((pg >> 1) & 1) ^ 1)) return false;
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_async_v4(xbuf_peer + static_cast<uint32_t>((xs * kSmxWarps * 8 * 32 + q * 32) * 16), dst[4 * q],
-                    dst[4 * q + 1], dst[4 * q + 2], dst[4 * q + 3], xfull_peer[xs]);
-      return true;
-    };
-    if (!load_and_send(0, s)) ok = false;
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      if (i + 1 < n_tiles && !load_and_send(i + 1, sn)) { ok = false; break; }
-      const int xs = i & 1;
-      if (!wwait_cluster(&sm->x_full[xs][region], (i >> 1) & 1)) { ok = false; break; }
-      // re-arm this region for page i+2 (its phase for page i has completed)
-      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sm->x_full[xs][region]), kXBytes);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 v = sm->xbuf[xs][region][q][lane];
-        s[4 * q] += v.x;
-        s[4 * q + 1] += v.y;
-        s[4 * q + 2] += v.z;
-        s[4 * q + 3] += v.w;
-      }
-      // slot consumed (and re-armed): the peer may send page i+2 into it. The
-      // warp barrier orders every lane's reads before lane 0's release.
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(xempty_peer[xs]);
+      if (lane == 0) mbar_arrive(smem_u32(&sm->s_empty));  // S may be overwritten by QK(i+1)
 
-      // ---- online softmax over this tile (identical in both CTAs)
+      // ---- online softmax over this tile
       const int tok0 = tok_begin + i * kTileTok + half * 32;
       const int valid = min(32, tok_end - tok0);  // may be <= 0 for the upper half
       if (valid < 32) {
@@ -377,8 +352,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int t = 0; t < w; ++t) t16[t] = fmaxf(t16[t], t16[t + w]);
         mx = t16[0];
       }
-      // row max over both halves (the other half lives in another warp)
-      // (an mbarrier, not bar.sync, so that an aborting warp cannot hang the rest)
+      // row max over both token halves (the other half lives in another warp);
+      // an mbarrier rather than bar.sync, so that an aborting warp cannot hang the rest
       sm->red[i & 1][half][h] = mx;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm->red_bar[i & 1]));
@@ -418,9 +393,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const int page_valid = min(kTileTok, tok_end - (tok_begin + i * kTileTok));
       if (page_valid < kTileTok) {
-        // rows past the sequence end may hold anything (NaN): zero them in the
-        // V columns so that 0 * row stays 0 in the PV product
-        uint4* base = reinterpret_cast<uint4*>(sm->stage[i % kStages]);
+        // rows past the sequence end may hold anything (NaN): zero them in this
+        // CTA's V columns so that 0 * row stays 0 in the PV product
+        uint4* base = reinterpret_cast<uint4*>(sm->stage[i % kStages] + ohalf * 4 * kBoxBytes);
         const int rows = kTileTok - page_valid;
         const int t_id = half * 128 + h;
         for (int e = t_id; e < rows * 4 * 8; e += kSmxThreads) {
@@ -435,8 +410,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm->p_full));
-#pragma unroll
-      for (int t = 0; t < 32; ++t) s[t] = sn[t];
     }
     // ---- epilogue: u = O / l (this CTA's 256 columns; this thread's 128), lse
     sm->lsum[half][h] = l;
@@ -460,7 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int v = 0; v < 4; ++v) dst[c * 4 + v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
         }
-        if (rank == 0 && half == 0 && a.lse_out != nullptr) a.lse_out[row0 + h] = lse;
+        if (ohalf == 0 && half == 0 && a.lse_out != nullptr) a.lse_out[row0 + h] = lse;
       } else {
         const int64_t prow = (static_cast<int64_t>(bj) * S + split) * 128 + h;
         float4* dst = reinterpret_cast<float4*>(a.part_u + prow * kDC + c_out);
@@ -472,16 +445,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             dst[c * 8 + v] = make_float4(o[4 * v] * inv_l, o[4 * v + 1] * inv_l, o[4 * v + 2] * inv_l,
                                          o[4 * v + 3] * inv_l);
         }
-        if (rank == 0 && half == 0) a.part_lse[prow] = lse;
+        if (ohalf == 0 && half == 0) a.part_lse[prow] = lse;
       }
     }
   }
 
-  // ---- teardown: both CTAs are done with each other's shared memory
+  // ---- teardown
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -511,22 +483,55 @@ bool decode_tc_supported(const DecodeArgs& a) {
          a.num_pages * static_cast<int64_t>(a.page_size) < (int64_t(1) << 31) && tensor_map_encoder() != nullptr;
 }
 
+// Tensor maps are plain host structures; encoding one costs host time on every
+// call, so the last few are kept (keyed by base pointer and shape).
+struct MapCache {
+  static constexpr int kSlots = 8;
+  struct Entry {
+    const void* ptr = nullptr;
+    uint64_t rows = 0;
+    uint32_t cols = 0, box_rows = 0;
+    CUtensorMap map;
+  } e[kSlots];
+  int next = 0;
+  const CUtensorMap* get(const void* ptr, uint64_t rows, uint32_t cols, uint32_t box_rows) {
+    for (auto& x : e)
+      if (x.ptr == ptr && x.rows == rows && x.cols == cols && x.box_rows == box_rows) return &x.map;
+    Entry& n = e[next];
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    if (tensor_map_encoder()(&n.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return nullptr;
+    n.ptr = ptr;
+    n.rows = rows;
+    n.cols = cols;
+    n.box_rows = box_rows;
+    next = (next + 1) % kSlots;
+    return &n.map;
+  }
+};
+
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRow), static_cast<cuuint64_t>(a.num_pages * a.page_size)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRow) * 2};
-  const cuuint32_t box[2] = {64, kTileTok};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = tensor_map_encoder()(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.cache), dims,
-                                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) return e;
+  static MapCache cache;  // host-side; calls on one process are expected from one thread at a time
+  static int attr_set_for_device = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (attr_set_for_device != dev) {
+    const cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set_for_device = dev;
+  }
+  const CUtensorMap* map = cache.get(a.cache, static_cast<uint64_t>(a.num_pages) * a.page_size, kRow, kTileTok);
+  // q_lat as [batch*q_len*128 rows][512] bf16, 128 x 64 boxes
+  const CUtensorMap* qmap = cache.get(a.q_lat, static_cast<uint64_t>(a.batch) * a.q_len * 128, kDC, 128);
+  if (map == nullptr || qmap == nullptr) return cudaErrorInvalidValue;
   const int64_t items = static_cast<int64_t>(a.batch) * a.q_len * a.num_splits;
-  decode_tc_kernel<<<dim3(static_cast<unsigned>(2 * items)), kThreads, kSmemBytes, s>>>(map, a);
+  decode_tc_kernel<<<dim3(static_cast<unsigned>(2 * items)), kThreads, kSmemBytes, s>>>(*map, *qmap, a);
   return cudaGetLastError();
 }
 

@@ -104,6 +104,21 @@ class MLADecodeLayer:
     def device_error(self) -> int:
         return capi.mla_read_device_error(self.dev_error)
 
+    def capture(self, fn, warmup: int = 2):
+        """Capture fn() (a sequence of this layer's calls on the current stream)
+        into a CUDA graph. Every buffer fn touches must already exist; the
+        library itself never allocates. Returns the torch.cuda.CUDAGraph."""
+        side = torch.cuda.Stream(device=self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
 
 def build_layer(w: Workload, d: dict, device="cuda", fill_context: bool = True, **kw) -> MLADecodeLayer:
     """A layer for workload w with the inputs d of workloads.make_inputs, its cache
