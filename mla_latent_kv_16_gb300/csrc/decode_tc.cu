@@ -64,10 +64,14 @@ struct __align__(1024) Smem {
   uint8_t q[4][kQBoxBytes];             // Q latent [256,512): 4 boxes of 64 columns
   float red[2][2][128];                 // row-max halves per page parity: [parity][half][head]
   float lsum[2][128];                   // row-sum halves for the epilogue
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  // Each stage is two groups of boxes: "A" = the boxes only the QK product
+  // reads (the other latent half and RoPE), released as soon as QK's first
+  // part is done; "B" = this CTA's latent half, also read by PV.
+  uint64_t full_a[kStages], full_b[kStages];
+  uint64_t empty_a[kStages], empty_b[kStages];
   uint64_t s_full, s_empty, p_full, pv_done, q_ready, drain;
   uint64_t q_smem_full;  // TMA of Q latent [256,512) into shared memory landed
+  uint64_t q_tm_full;    // TMA of Q latent [0,256) into stage 1 (staging for TMEM) landed
   uint64_t red_bar[2];  // softmax warps: row-max halves written (per page parity)
   uint64_t sum_bar;     // softmax warps: row-sum halves written (epilogue)
   uint32_t tmem_base;
@@ -142,8 +146,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sm->kv_full[s]), 1);
-      mbar_init(smem_u32(&sm->kv_empty[s]), 1);
+      mbar_init(smem_u32(&sm->full_a[s]), 1);
+      mbar_init(smem_u32(&sm->full_b[s]), 1);
+      mbar_init(smem_u32(&sm->empty_a[s]), 1);
+      mbar_init(smem_u32(&sm->empty_b[s]), 1);
     }
     mbar_init(smem_u32(&sm->s_full), 1);
     mbar_init(smem_u32(&sm->s_empty), kSmxWarps);
@@ -152,6 +158,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm->q_ready), kSmxWarps);
     mbar_init(smem_u32(&sm->drain), 1);
     mbar_init(smem_u32(&sm->q_smem_full), 1);
+    mbar_init(smem_u32(&sm->q_tm_full), 1);
     for (int x = 0; x < 2; ++x) mbar_init(smem_u32(&sm->red_bar[x]), kSmxWarps);
     mbar_init(smem_u32(&sm->sum_bar), kSmxWarps);
     sm->abort_flag = 0;
@@ -168,50 +175,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm->tmem_base;
   volatile int32_t* abort_flag = &sm->abort_flag;
 
+  // box groups of this CTA: B = its latent half (boxes 4*ohalf .. +3), A = the rest
+  const int a_first = ohalf == 0 ? 4 : 0;  // A = boxes a_first..a_first+3 and box 8
+  const int b_first = ohalf == 0 ? 0 : 4;
   if (warp == 0) {
-    // ================= TMA producer: whole pages
+    // ================= TMA producer
     if (lane == 0) {
-      // Q latent [256,512) of the 128 heads: four 128 x 64 boxes
+      // Q latent [256,512) -> shared memory (A operand); latent [0,256) -> stage 1,
+      // from where the softmax warps copy it into TMEM before page 1 is loaded
       mbar_arrive_expect_tx(smem_u32(&sm->q_smem_full), 4 * kQBoxBytes);
       for (int k = 0; k < 4; ++k)
         tma_load_2d_nohint(smem_u32(sm->q[k]), &qmap, smem_u32(&sm->q_smem_full), 256 + 64 * k,
                            static_cast<int32_t>(row0));
+      mbar_arrive_expect_tx(smem_u32(&sm->q_tm_full), 4 * kQBoxBytes);
+      for (int k = 0; k < 4; ++k)
+        tma_load_2d_nohint(smem_u32(sm->stage[1]) + k * kQBoxBytes, &qmap, smem_u32(&sm->q_tm_full), 64 * k,
+                           static_cast<int32_t>(row0));
       const uint64_t pol = l2_policy_evict_first();
-      int issued = 0;
       auto y_of = [&](int t) {  // pool row of tile t
         const int tok = tok_begin + t * kTileTok;
         return bt[tok / P] * P + (tok % P);
       };
       // pages kPrefetch tiles ahead are pulled into L2 so that a stage refill
-      // (issued only when PV frees the stage) is an L2 hit
+      // (issued only when the stage frees) is an L2 hit
       constexpr int kPrefetch = 2;
       for (int t = 0; t < min(n_tiles, kPrefetch); ++t) {
         const int32_t yp = y_of(t);
         for (int k = 0; k < kBoxes; ++k) tma_prefetch_l2_2d(&tmap, 64 * k, yp);
       }
+      int issued_a = 0, issued_b = 0;
       int32_t y_next = y_of(0);
       for (int i = 0; i < n_tiles; ++i) {
         const int st = i % kStages;
+        const uint32_t ph = ((i / kStages) & 1) ^ 1;
         const int32_t y = y_next;
         if (i + 1 < n_tiles) y_next = y_of(i + 1);
         if (i + kPrefetch < n_tiles) {
           const int32_t yp = y_of(i + kPrefetch);
           for (int k = 0; k < kBoxes; ++k) tma_prefetch_l2_2d(&tmap, 64 * k, yp);
         }
-        if (!mbar_wait<kSleep>(smem_u32(&sm->kv_empty[st]), ((i / kStages) & 1) ^ 1, abort_flag, a.dev_error)) break;
-        const uint32_t bar = smem_u32(&sm->kv_full[st]);
-        mbar_arrive_expect_tx(bar, kStageBytes);
+        if (i == 1 && !mbar_wait<kSleep>(smem_u32(&sm->q_ready), 0, abort_flag, a.dev_error)) break;
         const uint32_t dst = smem_u32(sm->stage[st]);
-#pragma unroll
-        for (int k = 0; k < kBoxes; ++k) tma_load_2d(dst + k * kBoxBytes, &tmap, bar, 64 * k, y, pol);
-        issued = i + 1;
+        if (!mbar_wait<kSleep>(smem_u32(&sm->empty_a[st]), ph, abort_flag, a.dev_error)) break;
+        mbar_arrive_expect_tx(smem_u32(&sm->full_a[st]), 5 * kBoxBytes);
+        for (int k = 0; k < 4; ++k)
+          tma_load_2d(dst + (a_first + k) * kBoxBytes, &tmap, smem_u32(&sm->full_a[st]), 64 * (a_first + k), y, pol);
+        tma_load_2d(dst + 8 * kBoxBytes, &tmap, smem_u32(&sm->full_a[st]), 512, y, pol);
+        issued_a = i + 1;
+        if (!mbar_wait<kSleep>(smem_u32(&sm->empty_b[st]), ph, abort_flag, a.dev_error)) break;
+        mbar_arrive_expect_tx(smem_u32(&sm->full_b[st]), 4 * kBoxBytes);
+        for (int k = 0; k < 4; ++k)
+          tma_load_2d(dst + (b_first + k) * kBoxBytes, &tmap, smem_u32(&sm->full_b[st]), 64 * (b_first + k), y, pol);
+        issued_b = i + 1;
       }
-      for (int i = max(0, issued - kStages); i < issued; ++i)
-        drain_wait(smem_u32(&sm->kv_full[i % kStages]), (i / kStages) & 1, a.dev_error);
+      for (int i = max(0, issued_a - kStages); i < issued_a; ++i)
+        drain_wait(smem_u32(&sm->full_a[i % kStages]), (i / kStages) & 1, a.dev_error);
+      for (int i = max(0, issued_b - kStages); i < issued_b; ++i)
+        drain_wait(smem_u32(&sm->full_b[i % kStages]), (i / kStages) & 1, a.dev_error);
       drain_wait(smem_u32(&sm->q_smem_full), 0, a.dev_error);
+      drain_wait(smem_u32(&sm->q_tm_full), 0, a.dev_error);
     }
   } else if (warp == 1) {
-    // ================= MMA issuer: event loop over "QK of page qk" and "PV of page pv"
+    // ================= MMA issuer: event loop over QK part 1 (A boxes), QK part 2
+    // (B boxes) and PV of successive pages
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16_f32(128, kTileTok, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, 256, false, true);
@@ -220,46 +246,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t dKB0 = sdesc_sw128(smem_u32(sm->stage[0]), 16, 1024);  // page as K-major B
       const uint64_t dQA0 = sdesc_sw128(smem_u32(sm->q[0]), 16, 1024);      // Q latent [256,512) as A
       constexpr uint64_t kStageDesc = kStageBytes >> 4;
+      // latent [0,256): A = Q from TMEM, B = page boxes 0-3
+      auto qk_low = [&](uint64_t db, uint32_t first_acc) {
+#pragma unroll
+        for (uint32_t kk = 0; kk < 16; ++kk)
+          mma_ts(tmem + kTmS, tmem + kTmQ + kk * 8u, db + (((kk >> 2) * kBoxBytes + (kk & 3u) * 32u) >> 4), kIdQK,
+                 (kk > 0 || first_acc) ? 1u : 0u);
+      };
+      // latent [256,512): A = Q from shared memory, B = page boxes 4-7
+      auto qk_high = [&](uint64_t db, uint32_t first_acc) {
+#pragma unroll
+        for (uint32_t kk = 0; kk < 16; ++kk)
+          mma_ss(tmem + kTmS, dQA0 + (((kk >> 2) * kQBoxBytes + (kk & 3u) * 32u) >> 4),
+                 db + (((4 + (kk >> 2)) * kBoxBytes + (kk & 3u) * 32u) >> 4), kIdQK, (kk > 0 || first_acc) ? 1u : 0u);
+      };
+      // RoPE [512,576): A = Q from TMEM, B = page box 8
+      auto qk_rope = [&](uint64_t db) {
+#pragma unroll
+        for (uint32_t kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + kTmS, tmem + kTmQ + 128u + kk * 8u, db + ((8 * kBoxBytes + kk * 32u) >> 4), kIdQK, 1u);
+      };
       bool ok = mbar_wait<kSleep>(smem_u32(&sm->q_ready), 0, abort_flag, a.dev_error) &&
                 mbar_wait<kSleep>(smem_u32(&sm->q_smem_full), 0, abort_flag, a.dev_error);
       tc_fence_after();
-      int qk = 0, pv = 0;
+      int q1 = 0, q2 = 0, pv = 0;  // next page for QK part 1, QK part 2, PV
       long long idle_since = 0;
       while (ok && pv < n_tiles) {
         bool did = false;
-        // S(qk) may be written once S(qk-1) has been read out of TMEM
-        if (qk < n_tiles && mbar_test_wait(smem_u32(&sm->kv_full[qk % kStages]), (qk / kStages) & 1) &&
-            (qk == 0 || mbar_test_wait(smem_u32(&sm->s_empty), (qk - 1) & 1))) {
-          tc_fence_after();
-          const uint64_t db = dKB0 + static_cast<uint64_t>(qk % kStages) * kStageDesc;
-          // latent [0,256): A = Q from TMEM, B = page boxes 0-3
-#pragma unroll
-          for (uint32_t kk = 0; kk < 16; ++kk)
-            mma_ts(tmem + kTmS, tmem + kTmQ + kk * 8u, db + (((kk >> 2) * kBoxBytes + (kk & 3u) * 32u) >> 4), kIdQK,
-                   kk > 0 ? 1u : 0u);
-          // RoPE [512,576): A = Q from TMEM, B = page box 8
-#pragma unroll
-          for (uint32_t kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kTmS, tmem + kTmQ + 128u + kk * 8u, db + ((8 * kBoxBytes + kk * 32u) >> 4), kIdQK, 1u);
-          // latent [256,512): A = Q from shared memory, B = page boxes 4-7
-#pragma unroll
-          for (uint32_t kk = 0; kk < 16; ++kk)
-            mma_ss(tmem + kTmS, dQA0 + (((kk >> 2) * kQBoxBytes + (kk & 3u) * 32u) >> 4),
-                   db + (((4 + (kk >> 2)) * kBoxBytes + (kk & 3u) * 32u) >> 4), kIdQK, 1u);
-          mma_commit(smem_u32(&sm->s_full));
-          ++qk;
-          did = true;
-        }
-        if (pv < qk && mbar_test_wait(smem_u32(&sm->p_full), pv & 1)) {
+        if (pv < q2 && mbar_test_wait(smem_u32(&sm->p_full), pv & 1)) {
           tc_fence_after();
           const uint64_t d0 = dPV0 + static_cast<uint64_t>(pv % kStages) * kStageDesc;
 #pragma unroll
           for (uint32_t kk = 0; kk < kTileTok / 16; ++kk)
             mma_ts(tmem + kTmO, tmem + kTmP + kk * 8u, d0 + kk * (16u * 128u >> 4), kIdPV,
                    (pv > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&sm->kv_empty[pv % kStages]));
+          mma_commit(smem_u32(&sm->empty_b[pv % kStages]));
           mma_commit(smem_u32(&sm->pv_done));
           ++pv;
+          did = true;
+        }
+        if (q2 < q1 && mbar_test_wait(smem_u32(&sm->full_b[q2 % kStages]), (q2 / kStages) & 1)) {
+          tc_fence_after();
+          const uint64_t db = dKB0 + static_cast<uint64_t>(q2 % kStages) * kStageDesc;
+          if (ohalf == 0) qk_low(db, 1u); else qk_high(db, 1u);
+          mma_commit(smem_u32(&sm->s_full));
+          ++q2;
+          did = true;
+        }
+        // S(q1) may be written once S(q1-1) has been read out of TMEM
+        if (q1 == q2 && q1 < n_tiles && mbar_test_wait(smem_u32(&sm->full_a[q1 % kStages]), (q1 / kStages) & 1) &&
+            (q1 == 0 || mbar_test_wait(smem_u32(&sm->s_empty), (q1 - 1) & 1))) {
+          tc_fence_after();
+          const uint64_t db = dKB0 + static_cast<uint64_t>(q1 % kStages) * kStageDesc;
+          if (ohalf == 0) qk_high(db, 0u); else qk_low(db, 0u);
+          qk_rope(db);
+          mma_commit(smem_u32(&sm->empty_a[q1 % kStages]));
+          ++q1;
           did = true;
         }
         if (did) {
@@ -290,36 +332,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto wwait = [&](uint64_t* bar, uint32_t par) {
       return __all_sync(0xffffffffu, mbar_wait<kPlain>(smem_u32(bar), par, abort_flag, a.dev_error));
     };
-    // Q of this head into TMEM (bf16 pairs, lower K index in the low half):
-    // half 0 writes latent [0,128) and the RoPE part, half 1 latent [128,256).
-    // Latent [256,512) reaches shared memory by TMA (issued by the producer).
+    // Q of this head into TMEM (bf16 pairs, lower K index in the low half). The
+    // producer staged latent [0,256) in stage 1 (four 128 x 64 boxes, 128-byte
+    // swizzle: 16-byte chunk c of row h sits at chunk c ^ (h mod 8)); half 0
+    // copies latent [0,128) and the RoPE part (from global memory), half 1
+    // latent [128,256). Latent [256,512) stays in shared memory (A operand).
     {
-      const uint4* ql = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_lat) + (row0 + h) * kDC);
-      const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_rope) + (row0 + h) * kDRope);
-      uint4 x[24];  // every load in flight at once: one memory round trip
-#pragma unroll
-      for (int v = 0; v < 16; ++v) x[v] = ql[half * 16 + v];
+      uint4 xr[8];
       if (half == 0) {
+        const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_rope) + (row0 + h) * kDRope);
 #pragma unroll
-        for (int v = 0; v < 8; ++v) x[16 + v] = qr[v];
+        for (int v = 0; v < 8; ++v) xr[v] = qr[v];
       }
-      uint32_t r[32];
+      const bool qok = wwait(&sm->q_tm_full, 0);
+      if (qok) {
+        uint32_t r[32];
 #pragma unroll
-      for (int c = 0; c < 3; ++c) {
-        if (c == 2 && half != 0) break;
+        for (int bb = 0; bb < 2; ++bb) {
+          const uint8_t* box = sm->stage[1] + (half * 2 + bb) * kQBoxBytes + h * 128;
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          r[4 * v] = x[c * 8 + v].x;
-          r[4 * v + 1] = x[c * 8 + v].y;
-          r[4 * v + 2] = x[c * 8 + v].z;
-          r[4 * v + 3] = x[c * 8 + v].w;
+          for (int c = 0; c < 8; ++c) {
+            const uint4 x = *reinterpret_cast<const uint4*>(box + ((c ^ (h & 7)) << 4));
+            r[4 * c] = x.x;
+            r[4 * c + 1] = x.y;
+            r[4 * c + 2] = x.z;
+            r[4 * c + 3] = x.w;
+          }
+          tmem_st32(tQ + static_cast<uint32_t>((half * 2 + bb) * 32), r);
         }
-        tmem_st32(tQ + (c == 2 ? 128u : static_cast<uint32_t>(half * 64 + c * 32)), r);
+        if (half == 0) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            r[4 * v] = xr[v].x;
+            r[4 * v + 1] = xr[v].y;
+            r[4 * v + 2] = xr[v].z;
+            r[4 * v + 3] = xr[v].w;
+          }
+          tmem_st32(tQ + 128u, r);
+        }
+        tmem_wait_st();
       }
-      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm->q_ready));
+      if (lane == 0) mbar_arrive(smem_u32(&sm->q_ready));  // also frees stage 1 for page 1
     }
     const float c2 = a.softmax_scale * kLog2e;  // scores in log2 units
     float m = -CUDART_INF_F, l = 0.0f;          // l: this thread's half of the row sum
