@@ -198,6 +198,39 @@ mla_status_t mla_decode_paged(const void *q_lat, const void *q_rope, const void 
                               mla_dtype_t cache_dtype, mla_stream_t stream);
 
 /*
+ * mla_decode_paged_static_scratch -- mla_decode_paged without a caller
+ * workspace. The pages describe no such call: it exists for callers that
+ * cannot allocate device memory or pass it in at call time. The split-KV
+ * partials go to one device array of MLA_STATIC_SCRATCH_BYTES bytes that the
+ * library holds for each device from module load on; the call allocates and
+ * frees nothing.
+ *
+ * Arguments and results are those of mla_decode_paged (minus workspace and
+ * workspace_bytes); the same kernels run, so outputs are identical to
+ * mla_decode_paged's for the same inputs and split count.
+ * Errors: those of mla_decode_paged, plus MLA_ERR_WORKSPACE_TOO_SMALL when
+ * mla_decode_workspace_size(...) for these arguments exceeds
+ * MLA_STATIC_SCRATCH_BYTES (nothing is enqueued; use fewer splits, a smaller
+ * batch, or mla_decode_paged with a workspace), and MLA_ERR_CUDA if the
+ * array's address cannot be obtained.
+ * Set-up: the first call on a device (that device current) looks up and caches
+ * the array's address; make it before any stream capture on that device.
+ * Sharing: all calls on a device share the array. Calls that may run
+ * concurrently on the device (unordered streams, several host threads) race on
+ * it and corrupt each other's results; order them. Nothing in the array has to
+ * start at zero.
+ */
+#define MLA_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+mla_status_t mla_decode_paged_static_scratch(const void *q_lat, const void *q_rope, const void *cache,
+                                             const float *scales, const int32_t *block_table,
+                                             const int32_t *seq_lens, int32_t batch, int32_t q_len,
+                                             int32_t max_pages_per_seq, int64_t num_pages,
+                                             int32_t page_size, float softmax_scale, int32_t num_splits,
+                                             void *u_out, float *lse_out, int32_t *dev_error,
+                                             mla_dims_t dims, mla_dtype_t act, mla_dtype_t cache_dtype,
+                                             mla_stream_t stream);
+
+/*
  * mla_out_proj -- per-head value up-projection, o[t][h][:] = W_UV[h] u[t][h][:].
  * [P1] §3.2 (W_UV moved after the attention-weighted sum); [P2] "Value Output
  * Matrix Absorption" with W_UV viewed as [n_heads][d_head][d_c].

@@ -24,10 +24,11 @@ MLA_F32, MLA_BF16, MLA_E4M3 = 0, 1, 2
 DTYPE_CODE = {"f32": MLA_F32, "bf16": MLA_BF16, "e4m3": MLA_E4M3}
 MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_SEQLEN, MLA_DEVERR_BAD_SLOT, MLA_DEVERR_BAD_POSITION = 1, 2, 4, 8
 MLA_DEVERR_TIMEOUT = 16
+MLA_STATIC_SCRATCH_BYTES = 32 << 20  # size of the library's fixed split-KV scratch array
 
 EXPORTED = ("mla_status_string", "mla_version", "mla_rope_table", "mla_cache_append", "mla_absorb_q",
             "mla_decode_num_splits", "mla_decode_workspace_size", "mla_decode_paged", "mla_out_proj",
-            "mla_read_device_error")
+            "mla_read_device_error", "mla_decode_paged_static_scratch")
 
 
 class MlaDims(ctypes.Structure):
@@ -82,6 +83,9 @@ def load(path: Optional[str] = None):
     L.mla_decode_paged.restype = ctypes.c_int
     L.mla_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, f32, i32, vp, sz, vp, vp,
                                    vp, MlaDims, ctypes.c_int, ctypes.c_int, vp]
+    L.mla_decode_paged_static_scratch.restype = ctypes.c_int
+    L.mla_decode_paged_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, f32, i32, vp,
+                                                  vp, vp, MlaDims, ctypes.c_int, ctypes.c_int, vp]
     L.mla_read_device_error.restype = ctypes.c_int
     L.mla_read_device_error.argtypes = [vp, vp, vp]
     _LIB = L
@@ -204,6 +208,26 @@ def mla_decode_paged(q_lat, q_rope, cache, scales, block_table, seq_lens, page_s
                                  _ptr(workspace), ws_bytes, _ptr(u_out), _ptr(lse_out), _ptr(dev_error), dims(H),
                                  _act_code(q_lat), DTYPE_CODE[cache_dtype], _stream(stream))
     _check("mla_decode_paged", st)
+    return u_out, lse_out
+
+
+def mla_decode_paged_static_scratch(q_lat, q_rope, cache, scales, block_table, seq_lens, page_size: int,
+                                    cache_dtype: str, softmax_scale: Optional[float] = None, num_splits: int = 0,
+                                    u_out=None, lse_out=None, dev_error=None, stream=None):
+    """mla_decode_paged with the split-KV partials in the library's fixed device
+    array (no workspace argument). u_out and lse_out must be passed in."""
+    _contig_cuda(q_lat, q_rope, cache, scales, block_table, seq_lens, u_out, lse_out, dev_error)
+    if u_out is None:
+        raise ValueError("u_out is required")
+    B, Lq, H = q_lat.shape[0], q_lat.shape[1], q_lat.shape[2]
+    rows = cache.shape[0] * cache.shape[1] if cache.dim() == 3 else cache.shape[0]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(128 + 64)
+    st = load().mla_decode_paged_static_scratch(
+        _ptr(q_lat), _ptr(q_rope), _ptr(cache), _ptr(scales), _ptr(block_table), _ptr(seq_lens), B, Lq,
+        block_table.shape[1], rows // page_size, page_size, softmax_scale, num_splits, _ptr(u_out), _ptr(lse_out),
+        _ptr(dev_error), dims(H), _act_code(q_lat), DTYPE_CODE[cache_dtype], _stream(stream))
+    _check("mla_decode_paged_static_scratch", st)
     return u_out, lse_out
 
 
