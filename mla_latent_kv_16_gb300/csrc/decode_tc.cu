@@ -539,7 +539,9 @@ bool decode_tc_supported(const DecodeArgs& a) {
 }
 
 // Tensor maps are plain host structures; encoding one costs host time on every
-// call, so the last few are kept (keyed by base pointer and shape).
+// call, so the last few are kept (keyed by base pointer and shape). get()
+// copies the map out, so a later miss that recycles a slot cannot change a map
+// already handed to a launch.
 struct MapCache {
   static constexpr int kSlots = 8;
   struct Entry {
@@ -549,9 +551,12 @@ struct MapCache {
     CUtensorMap map;
   } e[kSlots];
   int next = 0;
-  const CUtensorMap* get(const void* ptr, uint64_t rows, uint32_t cols, uint32_t box_rows) {
+  bool get(const void* ptr, uint64_t rows, uint32_t cols, uint32_t box_rows, CUtensorMap* out) {
     for (auto& x : e)
-      if (x.ptr == ptr && x.rows == rows && x.cols == cols && x.box_rows == box_rows) return &x.map;
+      if (x.ptr == ptr && x.rows == rows && x.cols == cols && x.box_rows == box_rows) {
+        *out = x.map;
+        return true;
+      }
     Entry& n = e[next];
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
@@ -559,14 +564,17 @@ struct MapCache {
     const cuuint32_t estr[2] = {1, 1};
     if (tensor_map_encoder()(&n.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return nullptr;
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      n.ptr = nullptr;
+      return false;
+    }
     n.ptr = ptr;
     n.rows = rows;
     n.cols = cols;
     n.box_rows = box_rows;
     next = (next + 1) % kSlots;
-    return &n.map;
+    *out = n.map;
+    return true;
   }
 };
 
@@ -581,12 +589,14 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set_for_device = dev;
   }
-  const CUtensorMap* map = cache.get(a.cache, static_cast<uint64_t>(a.num_pages) * a.page_size, kRow, kTileTok);
-  // q_lat as [batch*q_len*128 rows][512] bf16, 128 x 64 boxes
-  const CUtensorMap* qmap = cache.get(a.q_lat, static_cast<uint64_t>(a.batch) * a.q_len * 128, kDC, 128);
-  if (map == nullptr || qmap == nullptr) return cudaErrorInvalidValue;
+  CUtensorMap map, qmap;
+  // cache as [num_pages*page_size rows][576] bf16, 64 x 64 boxes; q_lat as
+  // [batch*q_len*128 rows][512] bf16, 128 x 64 boxes
+  if (!cache.get(a.cache, static_cast<uint64_t>(a.num_pages) * a.page_size, kRow, kTileTok, &map) ||
+      !cache.get(a.q_lat, static_cast<uint64_t>(a.batch) * a.q_len * 128, kDC, 128, &qmap))
+    return cudaErrorInvalidValue;
   const int64_t items = static_cast<int64_t>(a.batch) * a.q_len * a.num_splits;
-  decode_tc_kernel<<<dim3(static_cast<unsigned>(2 * items)), kThreads, kSmemBytes, s>>>(*map, *qmap, a);
+  decode_tc_kernel<<<dim3(static_cast<unsigned>(2 * items)), kThreads, kSmemBytes, s>>>(map, qmap, a);
   return cudaGetLastError();
 }
 
