@@ -1,4 +1,5 @@
-// Paged MLA decode on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+// Paged MLA decode on the 5th-generation tensor cores (tcgen05 + TMEM + TMA),
+// one CTA pair (cluster of 2) per work item, each CTA doing half of the work.
 //
 // What is computed ("Model Architecture Driving Inference Systems" §3.1-3.2;
 // "Tech Radar: DeepSeek-V3 MLA" §2): for every head h of one query position,
@@ -6,25 +7,39 @@
 //   u[h] = sum_t softmax(s)_t c_KV[t]
 // In the decode ("MQA") form all 128 heads share the same 576-wide cached rows
 // ("DeepSeek's attention evolution - [MLA]" §2.5), so the heads are the MMA M
-// dimension: S[128 x 64] = Q[128 x 576] * C^T per 64-token tile, and
+// dimension: S[128 x 64] = Q[128 x 576] * C^T per 64-token page, and
 // O[128 x 512] += P[128 x 64] * C[64 x 512].
 //
-// GB300 mapping. O alone (128 x 512 fp32) fills a whole SM's TMEM, so every
-// work item (sequence, query, KV split) runs on two CTAs, one per half of the
-// latent output: CTA "half" r accumulates O[:, 256r : 256r+256] in TMEM. Both
-// CTAs compute the full score tile (the QK product is duplicated: exchanging
-// 32 KB of fp32 partial scores per page between SMs would cost more than the
-// MMAs it saves), so the pair never communicates. Q (128 x 576 bf16) is split
-// between TMEM (latent 0-255 and RoPE 512-575: 160 columns, the A operand of
-// those MMAs) and shared memory (latent 256-511, 64 KB). The two CTAs of a
-// pair form a cluster so they run together and read each page from L2 once.
+// GB300 mapping. O (128 x 512 fp32) alone fills one SM's TMEM, so the pair
+// splits it: CTA r owns latent half r (columns [256r, 256r+256)) for all 128
+// heads. Each CTA reads only its own latent half of every page (plus the RoPE
+// columns of every other page) and computes a PARTIAL score over it:
+// S_r = Q[:, half r] * C[:, half r]^T (+ the RoPE term on pages i = r mod 2),
+// S = S_0 + S_1. The softmax is split by heads: CTA r owns heads
+// [64r, 64r+64). Per page each CTA
+//   1. sends the peer the partial scores of the peer's 64 heads (16 KB, DSMEM),
+//   2. adds the peer's partial to its own for its heads, runs the online
+//      softmax (running max with lazy rescale, row sums) and
+//   3. writes P (bf16) of its heads into its own and the peer's P tile (8 KB
+//      each way) together with the rescale factors of its heads,
+// after which both CTAs run the PV MMAs for their O half. Nothing is computed
+// twice, and each page crosses the SM boundary only as scores and weights.
 //
-// Per CTA: warp 0 issues TMA loads of whole 576-wide pages (2-stage ring);
-// warp 1 allocates TMEM and issues MMAs from an event loop (QK of a page as
-// soon as its data and the score buffer are free, PV as soon as P is
-// written); warps 2-9 own TMEM lanes 0-127 (= heads), two warps per lane
-// quarter, each covering 32 of the 64 tokens of a page: online softmax with a
-// lazily rescaled running max, P to TMEM in bf16, tail masking, epilogue.
+// TMEM (512 columns): O half [0,256), two score buffers [256,320) and
+// [320,384), Q's own latent half as bf16 pairs [384,512) (A of the QK MMAs).
+// Shared memory: a 4-deep ring of page halves (4 boxes of 64 tokens x 64
+// columns, 128-byte swizzle), a RoPE box, Q's RoPE part, two P tiles
+// (A of the PV MMAs), two inboxes for the peer's partial scores.
+//
+// Warps: 0 = TMA producer; 1 = TMEM allocation and MMA issue (PV of a page as
+// soon as its P is complete, else the next page's QK as soon as its score
+// buffer has been read and its data landed); 2-9 = two warps per TMEM lane
+// quarter. On the quarters of this CTA's heads the two run the softmax of
+// alternate pages (the running max passes between them through shared
+// memory); on the other quarters one warp forwards the
+// peer's partial scores and the other receives the peer's P rows and applies
+// its rescale factors to those O rows. In the epilogue each warp normalises
+// one half of the O columns of its quarter.
 //
 // Every wait is bounded: on a timeout the CTA raises an error bit, stops, waits
 // for its own copies and MMAs and frees TMEM.
@@ -45,40 +60,47 @@ constexpr int kSmxWarps = 8;
 constexpr int kSmxThreads = kSmxWarps * 32;
 constexpr int kThreads = 64 + kSmxThreads;
 constexpr int kTileTok = 64;
-constexpr int kStages = 2;
-constexpr int kBoxBytes = kTileTok * 128;      // 64 rows x 64 bf16, 128-byte swizzled
-constexpr int kBoxes = kRow / 64;              // 9 boxes per 576-wide page
-constexpr int kStageBytes = kBoxes * kBoxBytes;
-constexpr int kQBoxBytes = 128 * 128;          // Q in smem: 128 heads x 64 bf16
+constexpr int kStages = 4;                  // ring of page halves
+constexpr int kBoxBytes = kTileTok * 128;   // 64 rows x 64 bf16, 128-byte swizzled
+constexpr int kHalfBytes = 4 * kBoxBytes;   // one page, one latent half
+constexpr int kQBoxBytes = 128 * 128;       // 128 heads x 64 bf16
+constexpr int kPTileBytes = 128 * 128;      // P: 128 heads x 64 tokens bf16
+constexpr int kSinStride = 68;              // floats per row of a score inbox (padded: 272 B)
+constexpr uint32_t kSinBytes = 64 * 64 * 4; // payload of one score inbox
+constexpr uint32_t kPinBytes = 64 * 128 + 64 * 4;  // peer's P rows + rescale factors
 constexpr uint32_t kTmemCols = 512;
-// TMEM column map (fp32 columns)
 constexpr uint32_t kTmO = 0;    // O half: 256 columns
-constexpr uint32_t kTmS = 256;  // S tile: 64 columns
-constexpr uint32_t kTmP = 320;  // P tile: 64 bf16 = 32 columns
-constexpr uint32_t kTmQ = 352;  // Q latent [0,256) + RoPE [512,576): 128 + 32 columns
+constexpr uint32_t kTmS = 256;  // two partial-score buffers of 64 columns
+constexpr uint32_t kTmQ = 384;  // Q's own latent half: 128 columns of bf16 pairs
 // Lazy rescale: keep a stale row max until the new one exceeds it by 2^8.
 constexpr float kRescaleLog2 = 8.0f;
 
 struct __align__(1024) Smem {
-  uint8_t stage[kStages][kStageBytes];  // whole pages, 9 boxes of 64 columns
-  uint8_t q[4][kQBoxBytes];             // Q latent [256,512): 4 boxes of 64 columns
-  float red[2][2][128];                 // row-max halves per page parity: [parity][half][head]
-  float lsum[2][128];                   // row-sum halves for the epilogue
-  // Each stage is two groups of boxes: "A" = the boxes only the QK product
-  // reads (the other latent half and RoPE), released as soon as QK's first
-  // part is done; "B" = this CTA's latent half, also read by PV.
-  uint64_t full_a[kStages], full_b[kStages];
-  uint64_t empty_a[kStages], empty_b[kStages];
-  uint64_t s_full, s_empty, p_full, pv_done, q_ready, drain;
-  uint64_t q_smem_full;  // TMA of Q latent [256,512) into shared memory landed
-  uint64_t q_tm_full;    // TMA of Q latent [0,256) into stage 1 (staging for TMEM) landed
-  uint64_t red_bar[2];  // softmax warps: row-max halves written (per page parity)
-  uint64_t sum_bar;     // softmax warps: row-sum halves written (epilogue)
+  uint8_t kv[kStages][kHalfBytes];  // own latent half of page i in slot i % 4; slots 1-2 first stage Q
+  uint8_t rope[kBoxBytes];          // RoPE box of this CTA's next RoPE page (i = r mod 2)
+  uint8_t qr[kQBoxBytes];           // Q RoPE part (A of the RoPE MMAs)
+  uint8_t pt[2][kPTileBytes];       // P tile per page parity (A of the PV MMAs)
+  float sin[2][64][kSinStride];     // peer's partial scores for this CTA's heads
+  float alpha_in[2][64];            // peer's rescale factors for the peer's heads
+  float alpha_out[2][64];           // this CTA's rescale factors, bulk-copied to the peer
+  float mh[2][64];                  // running max after page i (log2 units), in mh[i & 1]
+  float lsum[2][64];                // each softmax warp's row sum, for the epilogue
+  float mlast[2][64];               // the max each softmax warp's row sum refers to
+  float l_in[64];                   // peer's row sums for the peer's heads
+  uint64_t full_kv[kStages], empty_kv[kStages];
+  uint64_t full_rope, empty_rope;
+  uint64_t q_smem_full, q_tm_full, q_ready;
+  uint64_t s_full[2], s_free[2];    // partial scores in TMEM: written / read by all 8 warps
+  uint64_t s_in[2], rs_free[2];     // score inbox: filled by the peer / the peer's inbox is free
+  uint64_t p_in[2], rp_free[2];     // P rows from the peer landed / the peer's P tile is free
+  uint64_t p_ready[2];              // this CTA's P rows and rescale factors written (4 softmax warps)
+  uint64_t pt_free[2];              // PV of the page that last used P tile x is done
+  uint64_t m_bar[2], p_full, pv_done, o_done, sum_bar, l_bar, drain;
   uint32_t tmem_base;
   int32_t abort_flag;
 };
-
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + realignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 constexpr int kPlain = 0, kSleep = 2;  // mbar_wait modes
 
 // Wait bounded only by time (teardown: our own copies / MMAs must land).
@@ -103,11 +125,12 @@ __device__ void write_empty(const DecodeArgs& a, int64_t row0, int bj, int split
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
-                     const DecodeArgs a) {
+                     const __grid_constant__ CUtensorMap rmap, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem* sm = reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t ohalf = blockIdx.x & 1u;  // which latent half of O this CTA owns
+  const uint32_t r = cluster_ctarank();  // latent half of O and head half of the softmax this CTA owns
+  const uint32_t peer = r ^ 1u;
 
   // ---- work item: (sequence b, query j, split) -- identical in both CTAs
   const int item = blockIdx.x >> 1;
@@ -119,7 +142,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int64_t row0 = static_cast<int64_t>(bj) * 128;
   const int L = a.seq_lens[b];
   const bool bad_len = (L < Lq) || (static_cast<int64_t>(L) > static_cast<int64_t>(a.max_pages) * P);
-  if (bad_len && ohalf == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_SEQLEN);
+  if (bad_len && r == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_SEQLEN);
   const int n_vis = bad_len ? 0 : L - Lq + j + 1;
   const int tok_begin = split * a.pages_per_split * P;
   const int tok_end = min(n_vis, (split + 1) * a.pages_per_split * P);
@@ -132,176 +155,179 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       local_bad |= (pp < 0 || pp >= a.num_pages) ? 1 : 0;
     }
     if (__syncthreads_or(local_bad)) {
-      if (ohalf == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_PAGE);
+      if (r == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_PAGE);
     } else {
       n_tiles = (tok_end - tok_begin + kTileTok - 1) / kTileTok;
     }
   }
-  if (n_tiles == 0) {
-    write_empty(a, row0, bj, split, ohalf);
+  if (n_tiles == 0) {  // both CTAs of the pair take this exit together
+    write_empty(a, row0, bj, split, r);
     return;
   }
-  const uint32_t col0 = ohalf * 256u;  // first latent column of this CTA's O half
 
   // ---- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sm->full_a[s]), 1);
-      mbar_init(smem_u32(&sm->full_b[s]), 1);
-      mbar_init(smem_u32(&sm->empty_a[s]), 1);
-      mbar_init(smem_u32(&sm->empty_b[s]), 1);
+      mbar_init(smem_u32(&sm->full_kv[s]), 1);
+      mbar_init(smem_u32(&sm->empty_kv[s]), 1);
     }
-    mbar_init(smem_u32(&sm->s_full), 1);
-    mbar_init(smem_u32(&sm->s_empty), kSmxWarps);
-    mbar_init(smem_u32(&sm->p_full), kSmxWarps);
-    mbar_init(smem_u32(&sm->pv_done), 1);
-    mbar_init(smem_u32(&sm->q_ready), kSmxWarps);
-    mbar_init(smem_u32(&sm->drain), 1);
+    mbar_init(smem_u32(&sm->full_rope), 1);
+    mbar_init(smem_u32(&sm->empty_rope), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&sm->s_full[x]), 1);
+      mbar_init(smem_u32(&sm->s_free[x]), 4);  // 2 softmax (the page's) + 2 forwarding warps
+      mbar_init(smem_u32(&sm->s_in[x]), 1);
+      mbar_init(smem_u32(&sm->rs_free[x]), 2);  // the peer's 2 softmax warps of the page
+      mbar_init(smem_u32(&sm->p_in[x]), 1);
+      mbar_init(smem_u32(&sm->rp_free[x]), 1);
+      mbar_init(smem_u32(&sm->m_bar[x]), 2);
+      mbar_init(smem_u32(&sm->pt_free[x]), 1);
+      mbar_init(smem_u32(&sm->p_ready[x]), 2);
+    }
     mbar_init(smem_u32(&sm->q_smem_full), 1);
     mbar_init(smem_u32(&sm->q_tm_full), 1);
-    for (int x = 0; x < 2; ++x) mbar_init(smem_u32(&sm->red_bar[x]), kSmxWarps);
-    mbar_init(smem_u32(&sm->sum_bar), kSmxWarps);
+    mbar_init(smem_u32(&sm->q_ready), kSmxWarps);
+    mbar_init(smem_u32(&sm->p_full), 4);  // 2 softmax (the page's) + 2 P-path warps
+    mbar_init(smem_u32(&sm->pv_done), 1);
+    mbar_init(smem_u32(&sm->o_done), 1);
+    mbar_init(smem_u32(&sm->sum_bar), 4);
+    mbar_init(smem_u32(&sm->l_bar), 1);
+    mbar_init(smem_u32(&sm->drain), 1);
     sm->abort_flag = 0;
     fence_mbar_init_cluster();
+    // the inboxes' first phases: expect the peer's bytes
+    for (int x = 0; x < 2 && x < n_tiles; ++x) {
+      mbar_arrive_expect_tx(smem_u32(&sm->s_in[x]), kSinBytes);
+      mbar_arrive_expect_tx(smem_u32(&sm->p_in[x]), kPinBytes);
+    }
+    mbar_arrive_expect_tx(smem_u32(&sm->l_bar), 64 * 4);
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmap);
     prefetch_tmap(&qmap);
+    prefetch_tmap(&rmap);
   }
   if (warp == 1) tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before any remote traffic
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
   volatile int32_t* abort_flag = &sm->abort_flag;
+  const int32_t col_half = static_cast<int32_t>(256u * r);  // first latent column of this CTA's half
 
-  // box groups of this CTA: B = its latent half (boxes 4*ohalf .. +3), A = the rest
-  const int a_first = ohalf == 0 ? 4 : 0;  // A = boxes a_first..a_first+3 and box 8
-  const int b_first = ohalf == 0 ? 0 : 4;
   if (warp == 0) {
     // ================= TMA producer
     if (lane == 0) {
-      // Q latent [256,512) -> shared memory (A operand); latent [0,256) -> stage 1,
-      // from where the softmax warps copy it into TMEM before page 1 is loaded
-      mbar_arrive_expect_tx(smem_u32(&sm->q_smem_full), 4 * kQBoxBytes);
-      for (int k = 0; k < 4; ++k)
-        tma_load_2d_nohint(smem_u32(sm->q[k]), &qmap, smem_u32(&sm->q_smem_full), 256 + 64 * k,
-                           static_cast<int32_t>(row0));
+      // Q's RoPE part -> qr; Q's own latent half -> slots 1-2, from where the
+      // softmax warps copy it into TMEM before pages 1 and 2 are loaded there
+      mbar_arrive_expect_tx(smem_u32(&sm->q_smem_full), kQBoxBytes);
+      tma_load_2d_nohint(smem_u32(sm->qr), &rmap, smem_u32(&sm->q_smem_full), 0, static_cast<int32_t>(row0));
       mbar_arrive_expect_tx(smem_u32(&sm->q_tm_full), 4 * kQBoxBytes);
       for (int k = 0; k < 4; ++k)
-        tma_load_2d_nohint(smem_u32(sm->stage[1]) + k * kQBoxBytes, &qmap, smem_u32(&sm->q_tm_full), 64 * k,
+        tma_load_2d_nohint(smem_u32(sm->kv[1]) + k * kQBoxBytes, &qmap, smem_u32(&sm->q_tm_full), col_half + 64 * k,
                            static_cast<int32_t>(row0));
       const uint64_t pol = l2_policy_evict_first();
       auto y_of = [&](int t) {  // pool row of tile t
         const int tok = tok_begin + t * kTileTok;
         return bt[tok / P] * P + (tok % P);
       };
-      // pages kPrefetch tiles ahead are pulled into L2 so that a stage refill
-      // (issued only when the stage frees) is an L2 hit
-      constexpr int kPrefetch = 2;
-      for (int t = 0; t < min(n_tiles, kPrefetch); ++t) {
+      auto prefetch = [&](int t) {
         const int32_t yp = y_of(t);
-        for (int k = 0; k < kBoxes; ++k) tma_prefetch_l2_2d(&tmap, 64 * k, yp);
-      }
-      int issued_a = 0, issued_b = 0;
+        for (int k = 0; k < 4; ++k) tma_prefetch_l2_2d(&tmap, col_half + 64 * k, yp);
+        if ((t & 1) == static_cast<int>(r)) tma_prefetch_l2_2d(&tmap, 512, yp);
+      };
+      constexpr int kPrefetch = 3;
+      for (int t = 0; t < min(n_tiles, kPrefetch); ++t) prefetch(t);
+      int issued_kv = 0, issued_rope = 0;
       int32_t y_next = y_of(0);
       for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % kStages;
-        const uint32_t ph = ((i / kStages) & 1) ^ 1;
         const int32_t y = y_next;
         if (i + 1 < n_tiles) y_next = y_of(i + 1);
-        if (i + kPrefetch < n_tiles) {
-          const int32_t yp = y_of(i + kPrefetch);
-          for (int k = 0; k < kBoxes; ++k) tma_prefetch_l2_2d(&tmap, 64 * k, yp);
-        }
+        if (i + kPrefetch < n_tiles) prefetch(i + kPrefetch);
         if (i == 1 && !mbar_wait<kSleep>(smem_u32(&sm->q_ready), 0, abort_flag, a.dev_error)) break;
-        const uint32_t dst = smem_u32(sm->stage[st]);
-        if (!mbar_wait<kSleep>(smem_u32(&sm->empty_a[st]), ph, abort_flag, a.dev_error)) break;
-        mbar_arrive_expect_tx(smem_u32(&sm->full_a[st]), 5 * kBoxBytes);
+        const int slot = i % kStages;
+        if (!mbar_wait<kSleep>(smem_u32(&sm->empty_kv[slot]), ((i / kStages) & 1) ^ 1, abort_flag, a.dev_error))
+          break;
+        mbar_arrive_expect_tx(smem_u32(&sm->full_kv[slot]), kHalfBytes);
         for (int k = 0; k < 4; ++k)
-          tma_load_2d(dst + (a_first + k) * kBoxBytes, &tmap, smem_u32(&sm->full_a[st]), 64 * (a_first + k), y, pol);
-        tma_load_2d(dst + 8 * kBoxBytes, &tmap, smem_u32(&sm->full_a[st]), 512, y, pol);
-        issued_a = i + 1;
-        if (!mbar_wait<kSleep>(smem_u32(&sm->empty_b[st]), ph, abort_flag, a.dev_error)) break;
-        mbar_arrive_expect_tx(smem_u32(&sm->full_b[st]), 4 * kBoxBytes);
-        for (int k = 0; k < 4; ++k)
-          tma_load_2d(dst + (b_first + k) * kBoxBytes, &tmap, smem_u32(&sm->full_b[st]), 64 * (b_first + k), y, pol);
-        issued_b = i + 1;
+          tma_load_2d(smem_u32(sm->kv[slot]) + k * kBoxBytes, &tmap, smem_u32(&sm->full_kv[slot]), col_half + 64 * k, y,
+                      pol);
+        issued_kv = i + 1;
+        if ((i & 1) == static_cast<int>(r)) {
+          // the k-th RoPE page of this CTA (k = i >> 1); the slot is free once QK of the previous one read it
+          if (!mbar_wait<kSleep>(smem_u32(&sm->empty_rope), ((i >> 1) & 1) ^ 1, abort_flag, a.dev_error)) break;
+          mbar_arrive_expect_tx(smem_u32(&sm->full_rope), kBoxBytes);
+          tma_load_2d(smem_u32(sm->rope), &tmap, smem_u32(&sm->full_rope), 512, y, pol);
+          issued_rope = i + 1;
+        }
       }
-      for (int i = max(0, issued_a - kStages); i < issued_a; ++i)
-        drain_wait(smem_u32(&sm->full_a[i % kStages]), (i / kStages) & 1, a.dev_error);
-      for (int i = max(0, issued_b - kStages); i < issued_b; ++i)
-        drain_wait(smem_u32(&sm->full_b[i % kStages]), (i / kStages) & 1, a.dev_error);
+      for (int i = max(0, issued_kv - kStages); i < issued_kv; ++i)
+        drain_wait(smem_u32(&sm->full_kv[i % kStages]), (i / kStages) & 1, a.dev_error);
+      if (issued_rope > 0) drain_wait(smem_u32(&sm->full_rope), ((issued_rope - 1) >> 1) & 1, a.dev_error);
       drain_wait(smem_u32(&sm->q_smem_full), 0, a.dev_error);
       drain_wait(smem_u32(&sm->q_tm_full), 0, a.dev_error);
     }
   } else if (warp == 1) {
-    // ================= MMA issuer: event loop over QK part 1 (A boxes), QK part 2
-    // (B boxes) and PV of successive pages
+    // ================= MMA issuer: PV(k) as soon as P(k) is complete, QK(k) as soon
+    // as score buffer k & 1 has been read out and page k has landed
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16_f32(128, kTileTok, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, 256, false, true);
       // descriptor start addresses advance in 16-byte units in the low bits
-      const uint64_t dPV0 = sdesc_sw128(smem_u32(sm->stage[0]) + ohalf * 4 * kBoxBytes, kBoxBytes, 1024);
-      const uint64_t dKB0 = sdesc_sw128(smem_u32(sm->stage[0]), 16, 1024);  // page as K-major B
-      const uint64_t dQA0 = sdesc_sw128(smem_u32(sm->q[0]), 16, 1024);      // Q latent [256,512) as A
-      constexpr uint64_t kStageDesc = kStageBytes >> 4;
-      // latent [0,256): A = Q from TMEM, B = page boxes 0-3
-      auto qk_low = [&](uint64_t db, uint32_t first_acc) {
+      const uint64_t dKV0 = sdesc_sw128(smem_u32(sm->kv[0]), 16, 1024);          // K-major B: page rows = N
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sm->kv[0]), kBoxBytes, 1024);    // MN-major B: V
+      const uint64_t dRope0 = sdesc_sw128(smem_u32(sm->rope), 16, 1024);
+      const uint64_t dQR = sdesc_sw128(smem_u32(sm->qr), 16, 1024);              // A: Q RoPE
+      const uint64_t dP0 = sdesc_sw128(smem_u32(sm->pt[0]), 16, 1024);           // A: P (K-major)
+      auto ready = [&](uint64_t* bar, uint32_t par) { return mbar_test_wait(smem_u32(bar), par); };
+      auto qk_ready = [&](int i) {
+        if (i >= 2 && !ready(&sm->s_free[i & 1], ((i - 2) >> 1) & 1)) return false;
+        if (!ready(&sm->full_kv[i % kStages], (i / kStages) & 1)) return false;
+        if ((i & 1) == static_cast<int>(r) && !ready(&sm->full_rope, (i >> 1) & 1)) return false;
+        return true;
+      };
+      auto issue_qk = [&](int i) {
+        const uint32_t dS = tmem + kTmS + static_cast<uint32_t>(i & 1) * 64u;
+        const uint64_t db = dKV0 + static_cast<uint64_t>(((i % kStages) * kHalfBytes) >> 4);
 #pragma unroll
         for (uint32_t kk = 0; kk < 16; ++kk)
-          mma_ts(tmem + kTmS, tmem + kTmQ + kk * 8u, db + (((kk >> 2) * kBoxBytes + (kk & 3u) * 32u) >> 4), kIdQK,
-                 (kk > 0 || first_acc) ? 1u : 0u);
-      };
-      // latent [256,512): A = Q from shared memory, B = page boxes 4-7
-      auto qk_high = [&](uint64_t db, uint32_t first_acc) {
+          mma_ts(dS, tmem + kTmQ + kk * 8u, db + (((kk >> 2) * kBoxBytes + (kk & 3u) * 32u) >> 4), kIdQK,
+                 kk > 0 ? 1u : 0u);
+        if ((i & 1) == static_cast<int>(r)) {
 #pragma unroll
-        for (uint32_t kk = 0; kk < 16; ++kk)
-          mma_ss(tmem + kTmS, dQA0 + (((kk >> 2) * kQBoxBytes + (kk & 3u) * 32u) >> 4),
-                 db + (((4 + (kk >> 2)) * kBoxBytes + (kk & 3u) * 32u) >> 4), kIdQK, (kk > 0 || first_acc) ? 1u : 0u);
+          for (uint32_t kk = 0; kk < 4; ++kk)
+            mma_ss(dS, dQR + ((kk * 32u) >> 4), dRope0 + ((kk * 32u) >> 4), kIdQK, 1u);
+          mma_commit(smem_u32(&sm->empty_rope));
+        }
+        mma_commit(smem_u32(&sm->s_full[i & 1]));
       };
-      // RoPE [512,576): A = Q from TMEM, B = page box 8
-      auto qk_rope = [&](uint64_t db) {
+      auto issue_pv = [&](int i) {
+        const int slot = i % kStages;
+        const uint64_t dv = dV0 + static_cast<uint64_t>((slot * kHalfBytes) >> 4);
+        const uint64_t dp = dP0 + static_cast<uint64_t>(((i & 1) * kPTileBytes) >> 4);
 #pragma unroll
-        for (uint32_t kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + kTmS, tmem + kTmQ + 128u + kk * 8u, db + ((8 * kBoxBytes + kk * 32u) >> 4), kIdQK, 1u);
+        for (uint32_t kk = 0; kk < kTileTok / 16; ++kk)
+          mma_ss(tmem + kTmO, dp + ((kk * 32u) >> 4), dv + ((kk * 16u * 128u) >> 4), kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&sm->empty_kv[slot]));
+        mma_commit(smem_u32(&sm->pt_free[i & 1]));
+        mma_commit(smem_u32(&sm->pv_done));
+        if (i == n_tiles - 1) mma_commit(smem_u32(&sm->o_done));
       };
-      bool ok = mbar_wait<kSleep>(smem_u32(&sm->q_ready), 0, abort_flag, a.dev_error) &&
-                mbar_wait<kSleep>(smem_u32(&sm->q_smem_full), 0, abort_flag, a.dev_error);
+      bool ok = mbar_wait<kPlain>(smem_u32(&sm->q_ready), 0, abort_flag, a.dev_error) &&
+                mbar_wait<kPlain>(smem_u32(&sm->q_smem_full), 0, abort_flag, a.dev_error);
       tc_fence_after();
-      int q1 = 0, q2 = 0, pv = 0;  // next page for QK part 1, QK part 2, PV
+      int nq = 0, np = 0;  // next QK, next PV
       long long idle_since = 0;
-      while (ok && pv < n_tiles) {
+      while (ok && np < n_tiles) {
         bool did = false;
-        if (pv < q2 && mbar_test_wait(smem_u32(&sm->p_full), pv & 1)) {
+        if (np < nq && ready(&sm->p_full, np & 1)) {
           tc_fence_after();
-          const uint64_t d0 = dPV0 + static_cast<uint64_t>(pv % kStages) * kStageDesc;
-#pragma unroll
-          for (uint32_t kk = 0; kk < kTileTok / 16; ++kk)
-            mma_ts(tmem + kTmO, tmem + kTmP + kk * 8u, d0 + kk * (16u * 128u >> 4), kIdPV,
-                   (pv > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&sm->empty_b[pv % kStages]));
-          mma_commit(smem_u32(&sm->pv_done));
-          ++pv;
+          issue_pv(np++);
           did = true;
-        }
-        if (q2 < q1 && mbar_test_wait(smem_u32(&sm->full_b[q2 % kStages]), (q2 / kStages) & 1)) {
+        } else if (nq < n_tiles && qk_ready(nq)) {
           tc_fence_after();
-          const uint64_t db = dKB0 + static_cast<uint64_t>(q2 % kStages) * kStageDesc;
-          if (ohalf == 0) qk_low(db, 1u); else qk_high(db, 1u);
-          mma_commit(smem_u32(&sm->s_full));
-          ++q2;
-          did = true;
-        }
-        // S(q1) may be written once S(q1-1) has been read out of TMEM
-        if (q1 == q2 && q1 < n_tiles && mbar_test_wait(smem_u32(&sm->full_a[q1 % kStages]), (q1 / kStages) & 1) &&
-            (q1 == 0 || mbar_test_wait(smem_u32(&sm->s_empty), (q1 - 1) & 1))) {
-          tc_fence_after();
-          const uint64_t db = dKB0 + static_cast<uint64_t>(q1 % kStages) * kStageDesc;
-          if (ohalf == 0) qk_high(db, 0u); else qk_low(db, 0u);
-          qk_rope(db);
-          mma_commit(smem_u32(&sm->empty_a[q1 % kStages]));
-          ++q1;
+          issue_qk(nq++);
           did = true;
         }
         if (did) {
@@ -321,162 +347,274 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       drain_wait(smem_u32(&sm->drain), 0, a.dev_error);
     }
   } else {
-    // ================= softmax / epilogue
-    // thread = (head h = TMEM lane, half of the page's 64 tokens)
-    const uint32_t q4 = static_cast<uint32_t>(warp & 3);
-    const int half = (warp - 2) >> 2;
-    const int h = static_cast<int>(q4 * 32u) + lane;
+    // ================= softmax (own heads) / forwarding (peer's heads), epilogue
+    const uint32_t q4 = static_cast<uint32_t>(warp & 3);  // TMEM lane quarter
+    const int t = (warp - 2) >> 2;                        // token half of a page; O column half
+    const bool own = (q4 >> 1) == r;                      // rows of this CTA's heads
+    const int h = static_cast<int>(q4 * 32u) + lane;      // head = TMEM lane
+    const int hl = h & 63;                                // index among the owner's 64 heads
     const uint32_t lanes = (q4 * 32u) << 16;
-    const uint32_t tS = tmem + lanes + kTmS + half * 32, tP = tmem + lanes + kTmP + half * 16;
-    const uint32_t tO = tmem + lanes + kTmO + half * 128, tQ = tmem + lanes + kTmQ;
+    const uint32_t tO = tmem + lanes + kTmO + t * 128, tQ = tmem + lanes + kTmQ;
     auto wwait = [&](uint64_t* bar, uint32_t par) {
       return __all_sync(0xffffffffu, mbar_wait<kPlain>(smem_u32(bar), par, abort_flag, a.dev_error));
     };
-    // Q of this head into TMEM (bf16 pairs, lower K index in the low half). The
-    // producer staged latent [0,256) in stage 1 (four 128 x 64 boxes, 128-byte
-    // swizzle: 16-byte chunk c of row h sits at chunk c ^ (h mod 8)); half 0
-    // copies latent [0,128) and the RoPE part (from global memory), half 1
-    // latent [128,256). Latent [256,512) stays in shared memory (A operand).
+    // Barriers the peer completes: by the complete_tx of its st.async stores or
+    // bulk copies (their bytes have landed in this CTA's shared memory once the
+    // phase completes, like TMA data) or by a relaxed "buffer free" arrive that
+    // carries no data; a CTA-scope wait suffices for both.
+    auto wwait_cl = [&](uint64_t* bar, uint32_t par) {
+      return __all_sync(0xffffffffu, mbar_wait<kPlain>(smem_u32(bar), par, abort_flag, a.dev_error));
+    };
+    // Q's own latent half of this head into TMEM (bf16 pairs, lower K index in
+    // the low half). Staged in slots 1-2 as four 128 x 64 boxes with 128-byte
+    // swizzle (16-byte chunk c of row h at chunk c ^ (h mod 8)); token half t
+    // copies boxes 2t, 2t+1.
     {
-      uint4 xr[8];
-      if (half == 0) {
-        const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_rope) + (row0 + h) * kDRope);
-#pragma unroll
-        for (int v = 0; v < 8; ++v) xr[v] = qr[v];
-      }
       const bool qok = wwait(&sm->q_tm_full, 0);
       if (qok) {
-        uint32_t r[32];
+        uint32_t rq[32];
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
-          const uint8_t* box = sm->stage[1] + (half * 2 + bb) * kQBoxBytes + h * 128;
+          const uint8_t* box = sm->kv[1] + (t * 2 + bb) * kQBoxBytes + h * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 x = *reinterpret_cast<const uint4*>(box + ((c ^ (h & 7)) << 4));
-            r[4 * c] = x.x;
-            r[4 * c + 1] = x.y;
-            r[4 * c + 2] = x.z;
-            r[4 * c + 3] = x.w;
+            rq[4 * c] = x.x;
+            rq[4 * c + 1] = x.y;
+            rq[4 * c + 2] = x.z;
+            rq[4 * c + 3] = x.w;
           }
-          tmem_st32(tQ + static_cast<uint32_t>((half * 2 + bb) * 32), r);
-        }
-        if (half == 0) {
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            r[4 * v] = xr[v].x;
-            r[4 * v + 1] = xr[v].y;
-            r[4 * v + 2] = xr[v].z;
-            r[4 * v + 3] = xr[v].w;
-          }
-          tmem_st32(tQ + 128u, r);
+          tmem_st32(tQ + static_cast<uint32_t>((t * 2 + bb) * 32), rq);
         }
         tmem_wait_st();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm->q_ready));  // also frees stage 1 for page 1
+      if (lane == 0) mbar_arrive(smem_u32(&sm->q_ready));  // also frees slots 1-2
     }
-    const float c2 = a.softmax_scale * kLog2e;  // scores in log2 units
-    float m = -CUDART_INF_F, l = 0.0f;          // l: this thread's half of the row sum
-    bool ok = true;
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      if (!wwait(&sm->s_full, i & 1)) { ok = false; break; }
-      tc_fence_after();
-      float s[32];
-      tmem_ld32_sync(tS, s);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm->s_empty));  // S may be overwritten by QK(i+1)
+    // cluster addresses of the peer's inboxes
+    const uint32_t peer_sin = map_to_rank(smem_u32(&sm->sin[0][0][0]), peer);
+    const uint32_t peer_s_in = map_to_rank(smem_u32(&sm->s_in[0]), peer);
+    const uint32_t peer_rs_free = map_to_rank(smem_u32(&sm->rs_free[0]), peer);
+    const uint32_t peer_pt = map_to_rank(smem_u32(sm->pt[0]), peer);
+    const uint32_t peer_alpha = map_to_rank(smem_u32(&sm->alpha_in[0][0]), peer);
+    const uint32_t peer_p_in = map_to_rank(smem_u32(&sm->p_in[0]), peer);
+    const uint32_t peer_rp_free = map_to_rank(smem_u32(&sm->rp_free[0]), peer);
+    const uint32_t peer_l_in = map_to_rank(smem_u32(&sm->l_in[0]), peer);
+    const uint32_t peer_l_bar = map_to_rank(smem_u32(&sm->l_bar), peer);
 
-      // ---- online softmax over this tile
-      const int tok0 = tok_begin + i * kTileTok + half * 32;
-      const int valid = min(32, tok_end - tok0);  // may be <= 0 for the upper half
-      if (valid < 32) {
+    const float c2 = a.softmax_scale * kLog2e;  // scores in log2 units
+    float m = -CUDART_INF_F, l = 0.0f;          // own rows: running max (log2 units), half row sum
+    bool ok = true;
+    auto rescale_o = [&](float alpha, int first_col, int ncols) {
+      for (int c = first_col; c < first_col + ncols; c += 32) {
+        float o[32];
+        tmem_ld32_sync(tmem + lanes + kTmO + static_cast<uint32_t>(c), o);
+        uint32_t w32[32];
 #pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (t >= valid) s[t] = -CUDART_INF_F;
+        for (int k = 0; k < 32; ++k) w32[k] = __float_as_uint(o[k] * alpha);
+        tmem_st32(tmem + lanes + kTmO + static_cast<uint32_t>(c), w32);
       }
-      float mx;
-      {
-        float t16[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) t16[t] = fmaxf(s[t], s[t + 16]);
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int t = 0; t < w; ++t) t16[t] = fmaxf(t16[t], t16[t + w]);
-        mx = t16[0];
-      }
-      // row max over both token halves (the other half lives in another warp);
-      // an mbarrier rather than bar.sync, so that an aborting warp cannot hang the rest
-      sm->red[i & 1][half][h] = mx;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm->red_bar[i & 1]));
-      if (!wwait(&sm->red_bar[i & 1], (i >> 1) & 1)) { ok = false; break; }
-      mx = fmaxf(mx, sm->red[i & 1][half ^ 1][h]);
-      const bool first = (i == 0);
-      const float m_new = fmaxf(m, mx * c2);
-      const bool resc = !first && (m_new > m + kRescaleLog2);
-      const float m_use = (first || resc) ? m_new : m;
-      const float alpha = resc ? fast_exp2(m - m_use) : 1.0f;
-      float rsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      uint32_t pw[16];
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const float p0 = fast_exp2(fmaf(s[2 * t], c2, -m_use));
-        const float p1 = fast_exp2(fmaf(s[2 * t + 1], c2, -m_use));
-        pw[t] = pack_bf16x2(p0, p1);
-        // normalise by the weights the PV product actually uses (bf16-rounded)
-        rsum[t & 3] += __uint_as_float(pw[t] << 16) + __uint_as_float(pw[t] & 0xffff0000u);
-      }
-      l = l * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
-      m = m_use;
-      if (!first) {
-        if (!wwait(&sm->pv_done, (i - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-      }
-      if (__any_sync(0xffffffffu, resc)) {
-        for (int c = 0; c < 4; ++c) {
-          float o[32];
-          tmem_ld32_sync(tO + c * 32u, o);
-          uint32_t r[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(o[k] * alpha);
-          tmem_st32(tO + c * 32u, r);
-        }
-        tmem_wait_st();
-      }
-      const int page_valid = min(kTileTok, tok_end - (tok_begin + i * kTileTok));
-      if (page_valid < kTileTok) {
-        // rows past the sequence end may hold anything (NaN): zero them in this
-        // CTA's V columns so that 0 * row stays 0 in the PV product
-        uint4* base = reinterpret_cast<uint4*>(sm->stage[i % kStages] + ohalf * 4 * kBoxBytes);
-        const int rows = kTileTok - page_valid;
-        const int t_id = half * 128 + h;
-        for (int e = t_id; e < rows * 4 * 8; e += kSmxThreads) {
-          const int box = e / (rows * 8), rem = e % (rows * 8);
-          base[(box * kBoxBytes + (page_valid + rem / 8) * 128) / 16 + (rem % 8)] = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      tmem_st16(tP, pw);
       tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm->p_full));
+    };
+    if (own) {
+      // ================= softmax of this CTA's heads, all 64 tokens of the pages i = t mod 2
+      const bool armer = (lane == 0) && ((q4 & 1) == 0);
+      float m_mine = -CUDART_INF_F;  // the max this warp's row sum l refers to
+      for (int i = t; ok && i < n_tiles; i += 2) {
+        const int sb = i & 1;
+        const uint32_t ph2 = (i >> 1) & 1;  // phase parity of the per-parity barriers for page i
+        const int page_valid = min(kTileTok, tok_end - (tok_begin + i * kTileTok));
+        if (!wwait(&sm->s_full[sb], ph2)) { ok = false; break; }
+        tc_fence_after();
+        float s[64];
+        {
+          float (&s0)[32] = *reinterpret_cast<float (*)[32]>(&s[0]);
+          float (&s1)[32] = *reinterpret_cast<float (*)[32]>(&s[32]);
+          tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u, s0);
+          tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u + 32u, s1);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
+        // ---- full scores of this CTA's heads: own partial + the peer's
+        if (!wwait_cl(&sm->s_in[sb], ph2)) { ok = false; break; }
+        if (armer && i + 2 < n_tiles) mbar_arrive_expect_tx(smem_u32(&sm->s_in[sb]), kSinBytes);
+        {
+          const float4* src = reinterpret_cast<const float4*>(&sm->sin[sb][hl][0]);
+#pragma unroll
+          for (int v = 0; v < 16; ++v) {
+            const float4 x = src[v];
+            s[4 * v] += x.x;
+            s[4 * v + 1] += x.y;
+            s[4 * v + 2] += x.z;
+            s[4 * v + 3] += x.w;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_relaxed(peer_rs_free + sb * 8);  // the peer may refill this inbox
+        // ---- online softmax over this page
+        if (page_valid < kTileTok) {
+#pragma unroll
+          for (int x = 0; x < 64; ++x)
+            if (x >= page_valid) s[x] = -CUDART_INF_F;
+        }
+        float mx;
+        {
+          float t32[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) t32[x] = fmaxf(s[x], s[x + 32]);
+#pragma unroll
+          for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+            for (int x = 0; x < w; ++x) t32[x] = fmaxf(t32[x], t32[x + w]);
+          mx = t32[0];
+        }
+        // the running max after page i-1 comes from the other warp of this quarter
+        float m_prev = -CUDART_INF_F;
+        if (i > 0) {
+          if (!wwait(&sm->m_bar[(i - 1) & 1], ((i - 1) >> 1) & 1)) { ok = false; break; }
+          m_prev = sm->mh[(i - 1) & 1][hl];
+        }
+        const bool first = (i == 0);
+        const float m_new = fmaxf(m_prev, mx * c2);
+        const bool resc = !first && (m_new > m_prev + kRescaleLog2);
+        const float m_use = (first || resc) ? m_new : m_prev;
+        sm->mh[sb][hl] = m_use;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->m_bar[sb]));
+        const float alpha = resc ? fast_exp2(m_prev - m_use) : 1.0f;  // for O, relative to page i-1
+        float rsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        uint32_t pw[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const float p0 = fast_exp2(fmaf(s[2 * x], c2, -m_use));
+          const float p1 = fast_exp2(fmaf(s[2 * x + 1], c2, -m_use));
+          pw[x] = pack_bf16x2(p0, p1);
+          // normalise by the weights the PV product actually uses (bf16-rounded)
+          rsum[x & 3] += __uint_as_float(pw[x] << 16) + __uint_as_float(pw[x] & 0xffff0000u);
+        }
+        // this warp's row sum, carried from its previous page's max to this one's
+        l = (first ? 0.0f : l * fast_exp2(m_mine - m_use)) + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+        m_mine = m_use;
+        const bool resc_any = __any_sync(0xffffffffu, resc);
+        // ---- P row of this head (64 tokens) and the rescale factor. Tile sb was
+        // last used for page i-2: by this CTA's PV(i-2) and, once the peer's
+        // PV(i-2) is done, no longer by the peer.
+        if (i >= 2 && (!wwait(&sm->pt_free[sb], ((i - 2) >> 1) & 1) ||
+                       !wwait_cl(&sm->rp_free[sb], ((i - 2) >> 1) & 1))) { ok = false; break; }
+        uint8_t* prow = sm->pt[sb] + h * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
+              make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+        sm->alpha_out[sb][hl] = alpha;
+        fence_proxy_async_smem();  // generic writes -> the bulk copy's and the MMAs' reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->p_ready[sb]));
+        if (armer) {
+          // one bulk copy of this CTA's 64 P rows (8 KB) and 64 rescale factors
+          if (!mbar_wait<kPlain>(smem_u32(&sm->p_ready[sb]), ph2, abort_flag, a.dev_error)) {
+            ok = false;
+          } else {
+            const uint32_t rows = static_cast<uint32_t>(sb * kPTileBytes) + r * 64u * 128u;
+            bulk_copy_to_peer(peer_pt + rows, smem_u32(sm->pt[0]) + rows, 64 * 128, peer_p_in + sb * 8);
+            bulk_copy_to_peer(peer_alpha + sb * 64 * 4, smem_u32(&sm->alpha_out[sb][0]), 64 * 4, peer_p_in + sb * 8);
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        // O rows of this CTA's heads may be rescaled (and PV(i) issued) only after PV(i-1)
+        if (!first) {
+          if (!wwait(&sm->pv_done, (i - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+        }
+        if (resc_any) rescale_o(alpha, 0, 256);
+        if (page_valid < kTileTok) {
+          // rows past the sequence end may hold anything (NaN): zero them in this
+          // CTA's V half so that 0 * row stays 0 in the PV product
+          uint4* base = reinterpret_cast<uint4*>(sm->kv[i % kStages]);
+          const int rows = kTileTok - page_valid;
+          for (int e = hl; e < rows * 4 * 8; e += 64) {
+            const int box = e / (rows * 8), rem = e % (rows * 8);
+            base[(box * kBoxBytes + (page_valid + rem / 8) * 128) / 16 + (rem % 8)] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->p_full));
+      }
+      sm->mlast[t][hl] = m_mine;
+    } else if (t == 0) {
+      // ================= forwarding: partial scores of the peer's heads -> its inbox
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int sb = i & 1;
+        if (!wwait(&sm->s_full[sb], (i >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        float s0[32], s1[32];
+        tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u, s0);
+        tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u + 32u, s1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
+        if (i >= 2 && !wwait_cl(&sm->rs_free[sb], ((i - 2) >> 1) & 1)) { ok = false; break; }
+        const uint32_t dst = peer_sin + ((sb * 64 + hl) * kSinStride) * 4;
+        const uint32_t sbar = peer_s_in + sb * 8;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) st_async_v4(dst + v * 16, s0[4 * v], s0[4 * v + 1], s0[4 * v + 2], s0[4 * v + 3], sbar);
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          st_async_v4(dst + 128 + v * 16, s1[4 * v], s1[4 * v + 1], s1[4 * v + 2], s1[4 * v + 3], sbar);
+      }
+    } else {
+      // ================= the peer's P rows and rescale factors for its heads
+      const bool armer = (lane == 0) && ((q4 & 1) == 0);
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int sb = i & 1;
+        if (i > 0) {
+          // PV(i-1) done: the peer may refill this CTA's P tile (i-1) & 1
+          if (!wwait(&sm->pv_done, (i - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          if (armer) mbar_arrive_remote_relaxed(peer_rp_free + ((i - 1) & 1) * 8);
+        }
+        if (!wwait_cl(&sm->p_in[sb], (i >> 1) & 1)) { ok = false; break; }
+        if (armer && i + 2 < n_tiles) mbar_arrive_expect_tx(smem_u32(&sm->p_in[sb]), kPinBytes);
+        const float alpha = sm->alpha_in[sb][hl];
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) rescale_o(alpha, 0, 256);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->p_full));
+      }
     }
-    // ---- epilogue: u = O / l (this CTA's 256 columns; this thread's 128), lse
-    sm->lsum[half][h] = l;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&sm->sum_bar));
-    if (ok && !wwait(&sm->sum_bar, 0)) ok = false;
-    const float l_row = sm->lsum[0][h] + sm->lsum[1][h];
-    if (ok && wwait(&sm->pv_done, (n_tiles - 1) & 1)) {
+    // ---- epilogue: u = O / l (this CTA's 256 columns; this warp's 128), lse
+    float l_row = 1.0f;
+    if (own) {
+      sm->lsum[t][hl] = l;  // (a warp that saw no page keeps l = 0 and m_mine = -inf)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm->sum_bar));
+      if (ok && !wwait(&sm->sum_bar, 0)) ok = false;
+      // both warps' sums brought to the final max (that of the last page)
+      m = sm->mh[(n_tiles - 1) & 1][hl];
+      l_row = 0.0f;
+      for (int x = 0; x < 2; ++x)
+        if (sm->mlast[x][hl] != -CUDART_INF_F) l_row += sm->lsum[x][hl] * fast_exp2(sm->mlast[x][hl] - m);
+      if (t == 0) st_async_b32(peer_l_in + hl * 4, __float_as_uint(l_row), peer_l_bar);
+      const float lse = (m + log2f(l_row)) * kLn2;
+      if (t == 0 && ok) {
+        if (S == 1) {
+          if (a.lse_out != nullptr) a.lse_out[row0 + h] = lse;
+        } else {
+          a.part_lse[(static_cast<int64_t>(bj) * S + split) * 128 + h] = lse;
+        }
+      }
+    } else {
+      if (ok && !wwait_cl(&sm->l_bar, 0)) ok = false;
+      l_row = sm->l_in[hl];
+    }
+    if (ok && wwait(&sm->o_done, 0)) {
       tc_fence_after();
       const float inv_l = 1.0f / l_row;
-      const float lse = (m + log2f(l_row)) * kLn2;
-      const uint32_t c_out = col0 + half * 128;
+      const uint32_t c_out = static_cast<uint32_t>(col_half) + t * 128;
       if (S == 1) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.u_out) + (row0 + h) * kDC + c_out);
         for (int c = 0; c < 4; ++c) {
@@ -488,7 +626,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int v = 0; v < 4; ++v) dst[c * 4 + v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
         }
-        if (ohalf == 0 && half == 0 && a.lse_out != nullptr) a.lse_out[row0 + h] = lse;
       } else {
         const int64_t prow = (static_cast<int64_t>(bj) * S + split) * 128 + h;
         float4* dst = reinterpret_cast<float4*>(a.part_u + prow * kDC + c_out);
@@ -500,15 +637,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             dst[c * 8 + v] = make_float4(o[4 * v] * inv_l, o[4 * v + 1] * inv_l, o[4 * v + 2] * inv_l,
                                          o[4 * v + 3] * inv_l);
         }
-        if (ohalf == 0 && half == 0) a.part_lse[prow] = lse;
       }
     }
   }
 
-  // ---- teardown
+  // ---- teardown: nothing of this CTA may still be in flight towards the peer
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -589,14 +726,15 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set_for_device = dev;
   }
-  CUtensorMap map, qmap;
+  CUtensorMap map, qmap, rmap;
+  const uint64_t q_rows = static_cast<uint64_t>(a.batch) * a.q_len * 128;
   // cache as [num_pages*page_size rows][576] bf16, 64 x 64 boxes; q_lat as
-  // [batch*q_len*128 rows][512] bf16, 128 x 64 boxes
+  // [batch*q_len*128 rows][512] and q_rope as [..][64], 128 x 64 boxes
   if (!cache.get(a.cache, static_cast<uint64_t>(a.num_pages) * a.page_size, kRow, kTileTok, &map) ||
-      !cache.get(a.q_lat, static_cast<uint64_t>(a.batch) * a.q_len * 128, kDC, 128, &qmap))
+      !cache.get(a.q_lat, q_rows, kDC, 128, &qmap) || !cache.get(a.q_rope, q_rows, kDRope, 128, &rmap))
     return cudaErrorInvalidValue;
   const int64_t items = static_cast<int64_t>(a.batch) * a.q_len * a.num_splits;
-  decode_tc_kernel<<<dim3(static_cast<unsigned>(2 * items)), kThreads, kSmemBytes, s>>>(map, qmap, a);
+  decode_tc_kernel<<<dim3(static_cast<unsigned>(2 * items)), kThreads, kSmemBytes, s>>>(map, qmap, rmap, a);
   return cudaGetLastError();
 }
 
