@@ -36,8 +36,8 @@
 // buffer has been read and its data landed); 2-9 = two warps per TMEM lane
 // quarter. On the quarters of this CTA's heads the two run the softmax of
 // alternate pages (the running max passes between them through shared
-// memory); on the other quarters one warp forwards the
-// peer's partial scores and the other receives the peer's P rows and applies
+// memory); on the other quarters both forward half of the peer's partial
+// scores each, and one of them also receives the peer's P rows and applies
 // its rescale factors to those O rows. In the epilogue each warp normalises
 // one half of the O columns of its quarter.
 //
@@ -93,9 +93,9 @@ struct __align__(1024) Smem {
   uint64_t s_full[2], s_free[2];    // partial scores in TMEM: written / read by all 8 warps
   uint64_t s_in[2], rs_free[2];     // score inbox: filled by the peer / the peer's inbox is free
   uint64_t p_in[2], rp_free[2];     // P rows from the peer landed / the peer's P tile is free
-  uint64_t p_ready[2];              // this CTA's P rows and rescale factors written (4 softmax warps)
   uint64_t pt_free[2];              // PV of the page that last used P tile x is done
-  uint64_t m_bar[2], p_full, pv_done, o_done, sum_bar, l_bar, drain;
+  uint64_t p_full[2];               // P of page i complete in tile i & 1 and O rescaled (4 warps)
+  uint64_t m_bar[2], pv_done, o_done, sum_bar, l_bar, drain;
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -175,19 +175,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm->empty_rope), 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&sm->s_full[x]), 1);
-      mbar_init(smem_u32(&sm->s_free[x]), 4);  // 2 softmax (the page's) + 2 forwarding warps
+      mbar_init(smem_u32(&sm->s_free[x]), 6);  // 2 softmax (the page's) + 4 forwarding warps
       mbar_init(smem_u32(&sm->s_in[x]), 1);
       mbar_init(smem_u32(&sm->rs_free[x]), 2);  // the peer's 2 softmax warps of the page
       mbar_init(smem_u32(&sm->p_in[x]), 1);
       mbar_init(smem_u32(&sm->rp_free[x]), 1);
       mbar_init(smem_u32(&sm->m_bar[x]), 2);
       mbar_init(smem_u32(&sm->pt_free[x]), 1);
-      mbar_init(smem_u32(&sm->p_ready[x]), 2);
+      mbar_init(smem_u32(&sm->p_full[x]), 4);  // 2 softmax (the page's) + 2 P-path warps
     }
     mbar_init(smem_u32(&sm->q_smem_full), 1);
     mbar_init(smem_u32(&sm->q_tm_full), 1);
     mbar_init(smem_u32(&sm->q_ready), kSmxWarps);
-    mbar_init(smem_u32(&sm->p_full), 4);  // 2 softmax (the page's) + 2 P-path warps
     mbar_init(smem_u32(&sm->pv_done), 1);
     mbar_init(smem_u32(&sm->o_done), 1);
     mbar_init(smem_u32(&sm->sum_bar), 4);
@@ -321,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       long long idle_since = 0;
       while (ok && np < n_tiles) {
         bool did = false;
-        if (np < nq && ready(&sm->p_full, np & 1)) {
+        if (np < nq && ready(&sm->p_full[np & 1], (np >> 1) & 1)) {
           tc_fence_after();
           issue_pv(np++);
           did = true;
@@ -511,24 +510,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         sm->alpha_out[sb][hl] = alpha;
         fence_proxy_async_smem();  // generic writes -> the bulk copy's and the MMAs' reads
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm->p_ready[sb]));
-        if (armer) {
-          // one bulk copy of this CTA's 64 P rows (8 KB) and 64 rescale factors
-          if (!mbar_wait<kPlain>(smem_u32(&sm->p_ready[sb]), ph2, abort_flag, a.dev_error)) {
-            ok = false;
-          } else {
-            const uint32_t rows = static_cast<uint32_t>(sb * kPTileBytes) + r * 64u * 128u;
-            bulk_copy_to_peer(peer_pt + rows, smem_u32(sm->pt[0]) + rows, 64 * 128, peer_p_in + sb * 8);
-            bulk_copy_to_peer(peer_alpha + sb * 64 * 4, smem_u32(&sm->alpha_out[sb][0]), 64 * 4, peer_p_in + sb * 8);
-          }
+        if (lane == 0) {
+          // this quarter's 32 P rows (4 KB) and 32 rescale factors, one bulk copy each
+          const uint32_t rows = static_cast<uint32_t>(sb * kPTileBytes) + q4 * 32u * 128u;
+          const uint32_t al = static_cast<uint32_t>((sb * 64 + (q4 & 1) * 32) * 4);
+          bulk_copy_to_peer(peer_pt + rows, smem_u32(sm->pt[0]) + rows, 32 * 128, peer_p_in + sb * 8);
+          bulk_copy_to_peer(peer_alpha + al, smem_u32(&sm->alpha_out[0][0]) + al, 32 * 4, peer_p_in + sb * 8);
         }
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        // O rows of this CTA's heads may be rescaled (and PV(i) issued) only after PV(i-1)
-        if (!first) {
+        // O rows of this CTA's heads may be rescaled only after PV(i-1). (PV(i-2)
+        // is complete -- the P tile wait above -- so pv_done is at most one phase
+        // behind and its parity wait cannot alias.)
+        if (resc_any) {
           if (!wwait(&sm->pv_done, (i - 1) & 1)) { ok = false; break; }
           tc_fence_after();
+          rescale_o(alpha, 0, 256);
         }
-        if (resc_any) rescale_o(alpha, 0, 256);
         if (page_valid < kTileTok) {
           // rows past the sequence end may hold anything (NaN): zero them in this
           // CTA's V half so that 0 * row stays 0 in the PV product
@@ -542,48 +538,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm->p_full));
+        if (lane == 0) mbar_arrive(smem_u32(&sm->p_full[sb]));
       }
       sm->mlast[t][hl] = m_mine;
-    } else if (t == 0) {
-      // ================= forwarding: partial scores of the peer's heads -> its inbox
-      for (int i = 0; ok && i < n_tiles; ++i) {
+    } else {
+      // ================= forwarding (columns [32t, 32t+32) of each page's partial
+      // scores of the peer's heads -> its inbox); warp t == 1 also receives the
+      // peer's P rows and applies its rescale factors, page i after forwarding i+1
+      auto forward = [&](int i) -> bool {
         const int sb = i & 1;
-        if (!wwait(&sm->s_full[sb], (i >> 1) & 1)) { ok = false; break; }
+        if (!wwait(&sm->s_full[sb], (i >> 1) & 1)) return false;
         tc_fence_after();
-        float s0[32], s1[32];
-        tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u, s0);
-        tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u + 32u, s1);
+        float sv[32];
+        tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u + t * 32u, sv);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
-        if (i >= 2 && !wwait_cl(&sm->rs_free[sb], ((i - 2) >> 1) & 1)) { ok = false; break; }
-        const uint32_t dst = peer_sin + ((sb * 64 + hl) * kSinStride) * 4;
+        if (i >= 2 && !wwait_cl(&sm->rs_free[sb], ((i - 2) >> 1) & 1)) return false;
+        const uint32_t dst = peer_sin + ((sb * 64 + hl) * kSinStride + t * 32) * 4;
         const uint32_t sbar = peer_s_in + sb * 8;
 #pragma unroll
-        for (int v = 0; v < 8; ++v) st_async_v4(dst + v * 16, s0[4 * v], s0[4 * v + 1], s0[4 * v + 2], s0[4 * v + 3], sbar);
-#pragma unroll
-        for (int v = 0; v < 8; ++v)
-          st_async_v4(dst + 128 + v * 16, s1[4 * v], s1[4 * v + 1], s1[4 * v + 2], s1[4 * v + 3], sbar);
-      }
-    } else {
-      // ================= the peer's P rows and rescale factors for its heads
-      const bool armer = (lane == 0) && ((q4 & 1) == 0);
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int sb = i & 1;
-        if (i > 0) {
-          // PV(i-1) done: the peer may refill this CTA's P tile (i-1) & 1
-          if (!wwait(&sm->pv_done, (i - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          if (armer) mbar_arrive_remote_relaxed(peer_rp_free + ((i - 1) & 1) * 8);
+        for (int v = 0; v < 8; ++v) st_async_v4(dst + v * 16, sv[4 * v], sv[4 * v + 1], sv[4 * v + 2], sv[4 * v + 3], sbar);
+        return true;
+      };
+      if (t == 0) {
+        for (int i = 0; ok && i < n_tiles; ++i) ok = forward(i);
+      } else {
+        const bool armer = (lane == 0) && ((q4 & 1) == 0);
+        ok = forward(0);
+        for (int i = 0; ok && i < n_tiles; ++i) {
+          const int sb = i & 1;
+          if (i + 1 < n_tiles && !forward(i + 1)) { ok = false; break; }
+          if (!wwait_cl(&sm->p_in[sb], (i >> 1) & 1)) { ok = false; break; }
+          if (armer && i + 2 < n_tiles) mbar_arrive_expect_tx(smem_u32(&sm->p_in[sb]), kPinBytes);
+          const float alpha = sm->alpha_in[sb][hl];
+          // PV(i-1) done (P tile (i-1) & 1 free): needed before a rescale of these
+          // O rows, and to let the peer refill that tile. pt_free advances once per
+          // two pages and this warp waits on it in page order, so it cannot alias.
+          bool signalled = (i == 0);
+          auto tile_free = [&]() -> bool {
+            if (signalled) return true;
+            if (!wwait(&sm->pt_free[(i - 1) & 1], ((i - 1) >> 1) & 1)) return false;
+            tc_fence_after();
+            if (armer) mbar_arrive_remote_relaxed(peer_rp_free + ((i - 1) & 1) * 8);
+            signalled = true;
+            return true;
+          };
+          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+            if (!tile_free()) { ok = false; break; }
+            rescale_o(alpha, 0, 256);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm->p_full[sb]));
+          if (!tile_free()) { ok = false; break; }
         }
-        if (!wwait_cl(&sm->p_in[sb], (i >> 1) & 1)) { ok = false; break; }
-        if (armer && i + 2 < n_tiles) mbar_arrive_expect_tx(smem_u32(&sm->p_in[sb]), kPinBytes);
-        const float alpha = sm->alpha_in[sb][hl];
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) rescale_o(alpha, 0, 256);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm->p_full));
       }
     }
     // ---- epilogue: u = O / l (this CTA's 256 columns; this warp's 128), lse
