@@ -140,32 +140,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int b = item / (Lq * S);
   const int bj = b * Lq + j;
   const int64_t row0 = static_cast<int64_t>(bj) * 128;
-  const int L = a.seq_lens[b];
-  const bool bad_len = (L < Lq) || (static_cast<int64_t>(L) > static_cast<int64_t>(a.max_pages) * P);
-  if (bad_len && r == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_SEQLEN);
-  const int n_vis = bad_len ? 0 : L - Lq + j + 1;
-  const int tok_begin = split * a.pages_per_split * P;
-  const int tok_end = min(n_vis, (split + 1) * a.pages_per_split * P);
-  const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
-  int n_tiles = 0;
-  if (tok_begin < tok_end) {
-    int local_bad = 0;
-    for (int pg = tok_begin / P + static_cast<int>(threadIdx.x); pg <= (tok_end - 1) / P; pg += kThreads) {
-      const int32_t pp = bt[pg];
-      local_bad |= (pp < 0 || pp >= a.num_pages) ? 1 : 0;
-    }
-    if (__syncthreads_or(local_bad)) {
-      if (r == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_PAGE);
-    } else {
-      n_tiles = (tok_end - tok_begin + kTileTok - 1) / kTileTok;
-    }
-  }
-  if (n_tiles == 0) {  // both CTAs of the pair take this exit together
-    write_empty(a, row0, bj, split, r);
-    return;
-  }
+  const int32_t col_half = static_cast<int32_t>(256u * r);  // first latent column of this CTA's half
 
-  // ---- set-up
+  // ---- set-up that needs no data of the work item, overlapped with reading it
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm->full_kv[s]), 1);
@@ -194,6 +171,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm->drain), 1);
     sm->abort_flag = 0;
     fence_mbar_init_cluster();
+    // Q's RoPE part -> qr; Q's own latent half -> slots 1-2, from where the
+    // softmax warps copy it into TMEM before pages 1 and 2 are loaded there
+    prefetch_tmap(&tmap);
+    prefetch_tmap(&qmap);
+    prefetch_tmap(&rmap);
+    mbar_arrive_expect_tx(smem_u32(&sm->q_smem_full), kQBoxBytes);
+    tma_load_2d_nohint(smem_u32(sm->qr), &rmap, smem_u32(&sm->q_smem_full), 0, static_cast<int32_t>(row0));
+    mbar_arrive_expect_tx(smem_u32(&sm->q_tm_full), 4 * kQBoxBytes);
+    for (int k = 0; k < 4; ++k)
+      tma_load_2d_nohint(smem_u32(sm->kv[1]) + k * kQBoxBytes, &qmap, smem_u32(&sm->q_tm_full), col_half + 64 * k,
+                         static_cast<int32_t>(row0));
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
+
+  const int L = a.seq_lens[b];
+  const bool bad_len = (L < Lq) || (static_cast<int64_t>(L) > static_cast<int64_t>(a.max_pages) * P);
+  if (bad_len && r == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_SEQLEN);
+  const int n_vis = bad_len ? 0 : L - Lq + j + 1;
+  const int tok_begin = split * a.pages_per_split * P;
+  const int tok_end = min(n_vis, (split + 1) * a.pages_per_split * P);
+  const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
+  int n_tiles = 0;
+  {
+    int local_bad = 0;
+    if (tok_begin < tok_end)
+      for (int pg = tok_begin / P + static_cast<int>(threadIdx.x); pg <= (tok_end - 1) / P; pg += kThreads) {
+        const int32_t pp = bt[pg];
+        local_bad |= (pp < 0 || pp >= a.num_pages) ? 1 : 0;
+      }
+    if (__syncthreads_or(local_bad)) {
+      if (r == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_PAGE);
+    } else if (tok_begin < tok_end) {
+      n_tiles = (tok_end - tok_begin + kTileTok - 1) / kTileTok;
+    }
+  }
+  if (threadIdx.x == 0) {
     // the inboxes' first phases: expect the peer's bytes
     for (int x = 0; x < 2 && x < n_tiles; ++x) {
       mbar_arrive_expect_tx(smem_u32(&sm->s_in[x]), kSinBytes);
@@ -201,31 +214,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_arrive_expect_tx(smem_u32(&sm->l_bar), 64 * 4);
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmap);
-    prefetch_tmap(&qmap);
-    prefetch_tmap(&rmap);
-  }
-  if (warp == 1) tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the peer's barriers are initialised before any remote traffic
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
   volatile int32_t* abort_flag = &sm->abort_flag;
-  const int32_t col_half = static_cast<int32_t>(256u * r);  // first latent column of this CTA's half
 
-  if (warp == 0) {
+  if (n_tiles == 0) {
+    // nothing to attend to (or rejected data; both CTAs of the pair agree):
+    // let Q's loads land, write the empty outputs, tear down
+    if (threadIdx.x == 0) {
+      drain_wait(smem_u32(&sm->q_smem_full), 0, a.dev_error);
+      drain_wait(smem_u32(&sm->q_tm_full), 0, a.dev_error);
+    }
+    write_empty(a, row0, bj, split, r);
+  } else if (warp == 0) {
     // ================= TMA producer
     if (lane == 0) {
-      // Q's RoPE part -> qr; Q's own latent half -> slots 1-2, from where the
-      // softmax warps copy it into TMEM before pages 1 and 2 are loaded there
-      mbar_arrive_expect_tx(smem_u32(&sm->q_smem_full), kQBoxBytes);
-      tma_load_2d_nohint(smem_u32(sm->qr), &rmap, smem_u32(&sm->q_smem_full), 0, static_cast<int32_t>(row0));
-      mbar_arrive_expect_tx(smem_u32(&sm->q_tm_full), 4 * kQBoxBytes);
-      for (int k = 0; k < 4; ++k)
-        tma_load_2d_nohint(smem_u32(sm->kv[1]) + k * kQBoxBytes, &qmap, smem_u32(&sm->q_tm_full), col_half + 64 * k,
-                           static_cast<int32_t>(row0));
       const uint64_t pol = l2_policy_evict_first();
       auto y_of = [&](int t) {  // pool row of tile t
         const int tok = tok_begin + t * kTileTok;
@@ -237,13 +243,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if ((t & 1) == static_cast<int>(r)) tma_prefetch_l2_2d(&tmap, 512, yp);
       };
       constexpr int kPrefetch = 3;
-      for (int t = 0; t < min(n_tiles, kPrefetch); ++t) prefetch(t);
       int issued_kv = 0, issued_rope = 0;
       int32_t y_next = y_of(0);
       for (int i = 0; i < n_tiles; ++i) {
         const int32_t y = y_next;
         if (i + 1 < n_tiles) y_next = y_of(i + 1);
-        if (i + kPrefetch < n_tiles) prefetch(i + kPrefetch);
         if (i == 1 && !mbar_wait<kSleep>(smem_u32(&sm->q_ready), 0, abort_flag, a.dev_error)) break;
         const int slot = i % kStages;
         if (!mbar_wait<kSleep>(smem_u32(&sm->empty_kv[slot]), ((i / kStages) & 1) ^ 1, abort_flag, a.dev_error))
@@ -253,6 +257,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tma_load_2d(smem_u32(sm->kv[slot]) + k * kBoxBytes, &tmap, smem_u32(&sm->full_kv[slot]), col_half + 64 * k, y,
                       pol);
         issued_kv = i + 1;
+        // pages ahead are pulled into L2 once this page's load is on its way
+        for (int t = (i == 0 ? 1 : i + kPrefetch); t <= i + kPrefetch && t < n_tiles; ++t) prefetch(t);
         if ((i & 1) == static_cast<int>(r)) {
           // the k-th RoPE page of this CTA (k = i >> 1); the slot is free once QK of the previous one read it
           if (!mbar_wait<kSleep>(smem_u32(&sm->empty_rope), ((i >> 1) & 1) ^ 1, abort_flag, a.dev_error)) break;
@@ -624,8 +630,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = 1.0f / l_row;
       const uint32_t c_out = static_cast<uint32_t>(col_half) + t * 128;
+      // The page ring is idle once O is complete: each warp stages its 32 rows x
+      // 128 columns there (16-byte chunks XOR-swizzled by row against bank
+      // conflicts) and copies them out with consecutive lanes on consecutive
+      // addresses, instead of one row per lane.
+      const int wl = warp - 2;
       if (S == 1) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.u_out) + (row0 + h) * kDC + c_out);
+        uint8_t* stage = sm->kv[0] + wl * (32 * 256);
         for (int c = 0; c < 4; ++c) {
           float o[32];
           tmem_ld32_sync(tO + c * 32u, o);
@@ -633,19 +644,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(o[2 * k] * inv_l, o[2 * k + 1] * inv_l);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[c * 4 + v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          for (int v = 0; v < 4; ++v) {
+            const int cc = c * 4 + v;
+            *reinterpret_cast<uint4*>(stage + lane * 256 + ((cc ^ (lane & 15)) << 4)) =
+                make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          }
+        }
+        __syncwarp();
+        uint8_t* u = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(a.u_out) + (row0 + q4 * 32) * kDC + c_out);
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+          const int row = k * 2 + (lane >> 4), ch = lane & 15;
+          *reinterpret_cast<uint4*>(u + static_cast<size_t>(row) * kDC * 2 + ch * 16) =
+              *reinterpret_cast<const uint4*>(stage + row * 256 + ((ch ^ (row & 15)) << 4));
         }
       } else {
-        const int64_t prow = (static_cast<int64_t>(bj) * S + split) * 128 + h;
-        float4* dst = reinterpret_cast<float4*>(a.part_u + prow * kDC + c_out);
+        uint8_t* stage = sm->kv[0] + wl * (32 * 512);
         for (int c = 0; c < 4; ++c) {
           float o[32];
           tmem_ld32_sync(tO + c * 32u, o);
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[c * 8 + v] = make_float4(o[4 * v] * inv_l, o[4 * v + 1] * inv_l, o[4 * v + 2] * inv_l,
-                                         o[4 * v + 3] * inv_l);
+          for (int v = 0; v < 8; ++v) {
+            const int cc = c * 8 + v;
+            *reinterpret_cast<float4*>(stage + lane * 512 + ((cc ^ lane) << 4)) =
+                make_float4(o[4 * v] * inv_l, o[4 * v + 1] * inv_l, o[4 * v + 2] * inv_l, o[4 * v + 3] * inv_l);
+          }
         }
+        __syncwarp();
+        const int64_t prow0 = (static_cast<int64_t>(bj) * S + split) * 128 + q4 * 32;
+        uint8_t* pu = reinterpret_cast<uint8_t*>(a.part_u + prow0 * kDC + c_out);
+#pragma unroll 4
+        for (int row = 0; row < 32; ++row)
+          *reinterpret_cast<uint4*>(pu + static_cast<size_t>(row) * kDC * 4 + lane * 16) =
+              *reinterpret_cast<const uint4*>(stage + row * 512 + ((lane ^ row) << 4));
       }
     }
   }
