@@ -159,58 +159,65 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
   }
 }
 
-// One CTA per (head, sequence*query); 128 threads x 4 latent columns.
+// Split-KV merge ("Model Architecture Driving Inference Systems" §4.1, split
+// KV with a log-sum-exp combine): u = sum_s e^(lse_s - lse*) u_s / sum_s
+// e^(lse_s - lse*), lse = lse* + log sum_s e^(lse_s - lse*). One warp per
+// (query, head): the lanes reduce the split log-sum-exps with shuffles, then
+// each lane merges 16 consecutive columns of the 512 with 16-byte loads.
 template <typename T>
 __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
-  extern __shared__ float wsh[];  // [S]
-  __shared__ float red[2];
-  const int h = blockIdx.x, bj = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x * 4 + warp, bj = blockIdx.y;
+  if (h >= a.heads) return;
   const int S = a.num_splits;
-  const float* lse_s = a.part_lse;
-  auto lse_at = [&](int s) { return lse_s[(static_cast<int64_t>(bj) * S + s) * a.heads + h]; };
+  const float* lse_s = a.part_lse + static_cast<int64_t>(bj) * S * a.heads + h;  // stride a.heads
   float mx = -CUDART_INF_F;
-  for (int s = threadIdx.x; s < S; s += blockDim.x) mx = fmaxf(mx, lse_at(s));
+  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lse_s[static_cast<int64_t>(s) * a.heads]);
   mx = warp_max(mx);
-  if ((threadIdx.x & 31) == 0) wsh[S + (threadIdx.x >> 5)] = mx;  // scratch after weights
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float v = -CUDART_INF_F;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) v = fmaxf(v, wsh[S + w]);
-    red[0] = v;
-  }
-  __syncthreads();
-  mx = red[0];
   const bool none = (mx == -CUDART_INF_F);
   float sum = 0.0f;
-  for (int s = threadIdx.x; s < S; s += blockDim.x) {
-    const float ls = lse_at(s);
-    const float wv = (none || ls == -CUDART_INF_F) ? 0.0f : fast_exp2((ls - mx) * kLog2e);
-    wsh[s] = wv;
-    sum += wv;
+  for (int s = lane; s < S; s += 32) {
+    const float ls = lse_s[static_cast<int64_t>(s) * a.heads];
+    sum += (none || ls == -CUDART_INF_F) ? 0.0f : fast_exp2((ls - mx) * kLog2e);
   }
   sum = warp_sum(sum);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) wsh[S + (threadIdx.x >> 5)] = sum;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float v = 0.0f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) v += wsh[S + w];
-    red[1] = v;
-  }
-  __syncthreads();
-  const float tot = red[1];
-  const float inv = none ? 0.0f : 1.0f / tot;
-  const int64_t row = static_cast<int64_t>(bj) * a.heads + h;
-  T* u = static_cast<T*>(a.u_out) + row * kDC;
-  for (int c = threadIdx.x; c < kDC; c += blockDim.x) {
-    float v = 0.0f;
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+  if (!none) {
     for (int s = 0; s < S; ++s) {
-      const float wv = wsh[s];
-      if (wv != 0.0f) v = fmaf(wv, a.part_u[((static_cast<int64_t>(bj) * S + s) * a.heads + h) * kDC + c], v);
+      const float ls = lse_s[static_cast<int64_t>(s) * a.heads];
+      if (ls == -CUDART_INF_F) continue;
+      const float wv = fast_exp2((ls - mx) * kLog2e);
+      const float4* src = reinterpret_cast<const float4*>(
+          a.part_u + ((static_cast<int64_t>(bj) * S + s) * a.heads + h) * kDC + lane * 16);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const float4 x = src[v];
+        acc[4 * v] = fmaf(wv, x.x, acc[4 * v]);
+        acc[4 * v + 1] = fmaf(wv, x.y, acc[4 * v + 1]);
+        acc[4 * v + 2] = fmaf(wv, x.z, acc[4 * v + 2]);
+        acc[4 * v + 3] = fmaf(wv, x.w, acc[4 * v + 3]);
+      }
     }
-    ActIO<T>::store(u + c, v * inv);
   }
-  if (threadIdx.x == 0 && a.lse_out != nullptr) a.lse_out[row] = none ? -CUDART_INF_F : mx + logf(tot);
+  const float inv = none ? 0.0f : 1.0f / sum;
+  const int64_t row = static_cast<int64_t>(bj) * a.heads + h;
+  T* u = static_cast<T*>(a.u_out) + row * kDC + lane * 16;
+  if constexpr (sizeof(T) == 2) {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = pack_bf16x2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+    uint4* d = reinterpret_cast<uint4*>(u);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  } else {
+    float4* d = reinterpret_cast<float4*>(u);
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      d[v] = make_float4(acc[4 * v] * inv, acc[4 * v + 1] * inv, acc[4 * v + 2] * inv, acc[4 * v + 3] * inv);
+  }
+  if (lane == 0 && a.lse_out != nullptr) a.lse_out[row] = none ? -CUDART_INF_F : mx + logf(sum);
 }
 
 // Opt the kernel into its dynamic shared memory once per device (a host call
@@ -254,12 +261,11 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s) {
 
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
   if (a.batch == 0 || a.num_splits == 1) return cudaSuccess;
-  dim3 grid(a.heads, a.batch * a.q_len);
-  const size_t smem = (a.num_splits + 8) * sizeof(float);
+  dim3 grid((a.heads + 3) / 4, a.batch * a.q_len);
   if (a.act == MLA_F32)
-    combine_kernel<float><<<grid, 128, smem, s>>>(a);
+    combine_kernel<float><<<grid, 128, 0, s>>>(a);
   else
-    combine_kernel<__nv_bfloat16><<<grid, 128, smem, s>>>(a);
+    combine_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 
