@@ -186,7 +186,9 @@ size_t mla_decode_workspace_size(int32_t batch, int32_t q_len, int32_t max_pages
  *
  * Rows past seq_len in a sequence's last page are never read into the result
  * (they may hold anything, NaN included). act is MLA_F32 or MLA_BF16;
- * cache_dtype is act, or MLA_E4M3 with act == MLA_BF16.
+ * cache_dtype is act, or MLA_E4M3 with act == MLA_BF16. An E4M3 value enters
+ * the scores and the latent sum as bf16: fl32(code * scale) rounded to
+ * nearest-even, the operand type of the bf16 activations it pairs with.
  */
 mla_status_t mla_decode_paged(const void *q_lat, const void *q_rope, const void *cache,
                               const float *scales, const int32_t *block_table,

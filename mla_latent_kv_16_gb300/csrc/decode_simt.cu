@@ -44,7 +44,9 @@ __device__ __forceinline__ void load_row(const void* cache, const float* scales,
   } else {
     const uint8_t* r = static_cast<const uint8_t*>(cache) + slot * kRow;
     const float* sc = scales + slot * kGroups;
-    for (int k = k0 + lane; k < kRow; k += 32) dst[k] = e4m3_to_f32(r[k]) * sc[k >> 7];
+    // dequantised value rounded to the bf16 operand type the E4M3 cache pairs with
+    for (int k = k0 + lane; k < kRow; k += 32)
+      dst[k] = bf16_bits_to_f32(f32_to_bf16_bits(e4m3_to_f32(r[k]) * sc[k >> 7]));
   }
 }
 

@@ -41,6 +41,12 @@
 // its rescale factors to those O rows. In the epilogue each warp normalises
 // one half of the O columns of its quarter.
 //
+// E4M3 cache ("Multi-Head Latent Attention (MLA): ..." "High-Throughput Serving
+// Kernels": FP8 latent cache with per-block scales): the TMA brings each page
+// half as bytes into the upper half of its slot, and two more warps decode it
+// in place to bf16 x (per-token, per-group) scale in the same swizzled layout
+// before the slot is marked full; everything after that is the bf16 path.
+//
 // Every wait is bounded: on a timeout the CTA raises an error bit, stops, waits
 // for its own copies and MMAs and frees TMEM.
 #include <cuda.h>
@@ -59,6 +65,9 @@ using namespace tc;
 constexpr int kSmxWarps = 8;
 constexpr int kSmxThreads = kSmxWarps * 32;
 constexpr int kThreads = 64 + kSmxThreads;
+constexpr int kCvtWarp0 = 2 + kSmxWarps;  // first of the two E4M3 converter warps
+__host__ __device__ constexpr int threads_for(bool fp8) { return kThreads + (fp8 ? 64 : 0); }
+constexpr int kFp8BoxBytes = 64 * 64;  // 64 rows x 64 bytes of E4M3
 constexpr int kTileTok = 64;
 constexpr int kStages = 4;                  // ring of page halves
 constexpr int kBoxBytes = kTileTok * 128;   // 64 rows x 64 bf16, 128-byte swizzled
@@ -96,6 +105,8 @@ struct __align__(1024) Smem {
   uint64_t pt_free[2];              // PV of the page that last used P tile x is done
   uint64_t p_full[2];               // P of page i complete in tile i & 1 and O rescaled (4 warps)
   uint64_t m_bar[2], pv_done, o_done, sum_bar, l_bar, drain;
+  uint64_t raw_full[kStages], raw_rope_full;  // E4M3 bytes landed (TMA)
+  uint64_t cvt_bar;                           // both converter warps have read their page
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -123,7 +134,8 @@ __device__ void write_empty(const DecodeArgs& a, int64_t row0, int bj, int split
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool kFp8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap rmap, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -144,11 +156,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---- set-up that needs no data of the work item, overlapped with reading it
   if (threadIdx.x == 0) {
+    // E4M3: the converter warps (2) complete full_kv / full_rope, the TMA raw_full
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sm->full_kv[s]), 1);
+      mbar_init(smem_u32(&sm->full_kv[s]), kFp8 ? 2 : 1);
       mbar_init(smem_u32(&sm->empty_kv[s]), 1);
+      mbar_init(smem_u32(&sm->raw_full[s]), 1);
     }
-    mbar_init(smem_u32(&sm->full_rope), 1);
+    mbar_init(smem_u32(&sm->raw_rope_full), 1);
+    mbar_init(smem_u32(&sm->cvt_bar), 2);
+    mbar_init(smem_u32(&sm->full_rope), kFp8 ? 2 : 1);
     mbar_init(smem_u32(&sm->empty_rope), 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&sm->s_full[x]), 1);
@@ -196,7 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   {
     int local_bad = 0;
     if (tok_begin < tok_end)
-      for (int pg = tok_begin / P + static_cast<int>(threadIdx.x); pg <= (tok_end - 1) / P; pg += kThreads) {
+      for (int pg = tok_begin / P + static_cast<int>(threadIdx.x); pg <= (tok_end - 1) / P; pg += threads_for(kFp8)) {
         const int32_t pp = bt[pg];
         local_bad |= (pp < 0 || pp >= a.num_pages) ? 1 : 0;
       }
@@ -252,24 +268,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int slot = i % kStages;
         if (!mbar_wait<kSleep>(smem_u32(&sm->empty_kv[slot]), ((i / kStages) & 1) ^ 1, abort_flag, a.dev_error))
           break;
-        mbar_arrive_expect_tx(smem_u32(&sm->full_kv[slot]), kHalfBytes);
-        for (int k = 0; k < 4; ++k)
-          tma_load_2d(smem_u32(sm->kv[slot]) + k * kBoxBytes, &tmap, smem_u32(&sm->full_kv[slot]), col_half + 64 * k, y,
-                      pol);
+        if constexpr (kFp8) {
+          // E4M3 bytes into the upper half of the slot
+          mbar_arrive_expect_tx(smem_u32(&sm->raw_full[slot]), 4 * kFp8BoxBytes);
+          for (int k = 0; k < 4; ++k)
+            tma_load_2d(smem_u32(sm->kv[slot]) + kHalfBytes / 2 + k * kFp8BoxBytes, &tmap, smem_u32(&sm->raw_full[slot]),
+                        col_half + 64 * k, y, pol);
+        } else {
+          mbar_arrive_expect_tx(smem_u32(&sm->full_kv[slot]), kHalfBytes);
+          for (int k = 0; k < 4; ++k)
+            tma_load_2d(smem_u32(sm->kv[slot]) + k * kBoxBytes, &tmap, smem_u32(&sm->full_kv[slot]), col_half + 64 * k,
+                        y, pol);
+        }
         issued_kv = i + 1;
         // pages ahead are pulled into L2 once this page's load is on its way
         for (int t = (i == 0 ? 1 : i + kPrefetch); t <= i + kPrefetch && t < n_tiles; ++t) prefetch(t);
         if ((i & 1) == static_cast<int>(r)) {
           // the k-th RoPE page of this CTA (k = i >> 1); the slot is free once QK of the previous one read it
           if (!mbar_wait<kSleep>(smem_u32(&sm->empty_rope), ((i >> 1) & 1) ^ 1, abort_flag, a.dev_error)) break;
-          mbar_arrive_expect_tx(smem_u32(&sm->full_rope), kBoxBytes);
-          tma_load_2d(smem_u32(sm->rope), &tmap, smem_u32(&sm->full_rope), 512, y, pol);
+          if constexpr (kFp8) {
+            mbar_arrive_expect_tx(smem_u32(&sm->raw_rope_full), kFp8BoxBytes);
+            tma_load_2d(smem_u32(sm->rope) + kBoxBytes / 2, &tmap, smem_u32(&sm->raw_rope_full), 512, y, pol);
+          } else {
+            mbar_arrive_expect_tx(smem_u32(&sm->full_rope), kBoxBytes);
+            tma_load_2d(smem_u32(sm->rope), &tmap, smem_u32(&sm->full_rope), 512, y, pol);
+          }
           issued_rope = i + 1;
         }
       }
       for (int i = max(0, issued_kv - kStages); i < issued_kv; ++i)
-        drain_wait(smem_u32(&sm->full_kv[i % kStages]), (i / kStages) & 1, a.dev_error);
-      if (issued_rope > 0) drain_wait(smem_u32(&sm->full_rope), ((issued_rope - 1) >> 1) & 1, a.dev_error);
+        drain_wait(smem_u32(kFp8 ? &sm->raw_full[i % kStages] : &sm->full_kv[i % kStages]), (i / kStages) & 1,
+                   a.dev_error);
+      if (issued_rope > 0)
+        drain_wait(smem_u32(kFp8 ? &sm->raw_rope_full : &sm->full_rope), ((issued_rope - 1) >> 1) & 1, a.dev_error);
       drain_wait(smem_u32(&sm->q_smem_full), 0, a.dev_error);
       drain_wait(smem_u32(&sm->q_tm_full), 0, a.dev_error);
     }
@@ -350,6 +381,90 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       mma_commit(smem_u32(&sm->drain));
       drain_wait(smem_u32(&sm->drain), 0, a.dev_error);
+    }
+  } else if (kFp8 && warp >= kCvtWarp0) {
+    // ================= E4M3 -> bf16 (x scale) in place, one page row per lane
+    const int row = (warp - kCvtWarp0) * 32 + lane;
+    const float* scales = a.scales;
+    bool ok = true;
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      const int slot = i % kStages;
+      const bool rope_page = (i & 1) == static_cast<int>(r);
+      const int tok = tok_begin + i * kTileTok;
+      const int64_t y = static_cast<int64_t>(bt[tok / P]) * P + (tok % P) + row;  // pool row
+      // this row's scales: groups 2r, 2r+1 (this CTA's latent half) and 4 (RoPE)
+      const float sc0 = scales[y * MLA_E4M3_GROUPS + 2 * r];
+      const float sc1 = scales[y * MLA_E4M3_GROUPS + 2 * r + 1];
+      const float scr = rope_page ? scales[y * MLA_E4M3_GROUPS + 4] : 0.0f;
+      if (!__all_sync(0xffffffffu, mbar_wait<kPlain>(smem_u32(&sm->raw_full[slot]), (i / kStages) & 1, abort_flag,
+                                                      a.dev_error))) { ok = false; break; }
+      if (rope_page && !__all_sync(0xffffffffu, mbar_wait<kPlain>(smem_u32(&sm->raw_rope_full), (i >> 1) & 1,
+                                                                   abort_flag, a.dev_error))) { ok = false; break; }
+      // read the whole row first: the bf16 output overlaps the bytes of other rows
+      uint8_t* kvs = sm->kv[slot];
+      uint4 raw[16], rraw[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          raw[4 * k + v] = *reinterpret_cast<const uint4*>(kvs + kHalfBytes / 2 + k * kFp8BoxBytes + row * 64 + v * 16);
+      if (rope_page) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          rraw[v] = *reinterpret_cast<const uint4*>(sm->rope + kBoxBytes / 2 + row * 64 + v * 16);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm->cvt_bar));
+      if (!__all_sync(0xffffffffu, mbar_wait<kPlain>(smem_u32(&sm->cvt_bar), i & 1, abort_flag, a.dev_error))) {
+        ok = false;
+        break;
+      }
+      // 16 E4M3 values (one uint4) -> 16 bf16 x scale (two 16-byte chunks)
+      auto convert16 = [&](const uint4& x, float sc, uint4& lo, uint4& hi) {
+        const uint32_t wds[4] = {x.x, x.y, x.z, x.w};
+        uint32_t outw[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint16_t pair = static_cast<uint16_t>(wds[q] >> (16 * hh));
+            uint32_t h2;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+            outw[2 * q + hh] = pack_bf16x2(f.x * sc, f.y * sc);
+          }
+        }
+        lo = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        hi = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+      };
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float sc = k < 2 ? sc0 : sc1;  // 64-column boxes 0,1 in group 2r, 2,3 in group 2r+1
+        uint8_t* dst = kvs + k * kBoxBytes + row * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 lo, hi;
+          convert16(raw[4 * k + v], sc, lo, hi);
+          *reinterpret_cast<uint4*>(dst + (((2 * v) ^ (row & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((2 * v + 1) ^ (row & 7)) << 4)) = hi;
+        }
+      }
+      if (rope_page) {
+        uint8_t* dst = sm->rope + row * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 lo, hi;
+          convert16(rraw[v], scr, lo, hi);
+          *reinterpret_cast<uint4*>(dst + (((2 * v) ^ (row & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((2 * v + 1) ^ (row & 7)) << 4)) = hi;
+        }
+      }
+      fence_proxy_async_smem();  // generic writes -> the MMAs' operand reads
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sm->full_kv[slot]));
+        if (rope_page) mbar_arrive(smem_u32(&sm->full_rope));
+      }
     }
   } else {
     // ================= softmax (own heads) / forwarding (peer's heads), epilogue
@@ -710,7 +825,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }  // namespace
 
 bool decode_tc_supported(const DecodeArgs& a) {
-  return a.heads == 128 && a.act == MLA_BF16 && a.cache_dtype == MLA_BF16 && a.page_size % kTileTok == 0 &&
+  return a.heads == 128 && a.act == MLA_BF16 &&
+         (a.cache_dtype == MLA_BF16 || (a.cache_dtype == MLA_E4M3 && a.scales != nullptr)) &&
+         a.page_size % kTileTok == 0 &&
          (reinterpret_cast<uintptr_t>(a.cache) & 15u) == 0 &&
          a.num_pages * static_cast<int64_t>(a.page_size) < (int64_t(1) << 31) && tensor_map_encoder() != nullptr;
 }
@@ -725,22 +842,26 @@ struct MapCache {
     const void* ptr = nullptr;
     uint64_t rows = 0;
     uint32_t cols = 0, box_rows = 0;
+    bool bytes = false;
     CUtensorMap map;
   } e[kSlots];
   int next = 0;
-  bool get(const void* ptr, uint64_t rows, uint32_t cols, uint32_t box_rows, CUtensorMap* out) {
+  // bf16 elements, 64 x box_rows boxes, 128-byte swizzle; or (bytes) uint8
+  // elements, 64-byte x box_rows boxes, no swizzle
+  bool get(const void* ptr, uint64_t rows, uint32_t cols, uint32_t box_rows, CUtensorMap* out, bool bytes = false) {
     for (auto& x : e)
-      if (x.ptr == ptr && x.rows == rows && x.cols == cols && x.box_rows == box_rows) {
+      if (x.ptr == ptr && x.rows == rows && x.cols == cols && x.box_rows == box_rows && x.bytes == bytes) {
         *out = x.map;
         return true;
       }
     Entry& n = e[next];
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * (bytes ? 1 : 2)};
     const cuuint32_t box[2] = {64, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    if (tensor_map_encoder()(&n.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (tensor_map_encoder()(&n.map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
       n.ptr = nullptr;
       return false;
@@ -749,6 +870,7 @@ struct MapCache {
     n.rows = rows;
     n.cols = cols;
     n.box_rows = box_rows;
+    n.bytes = bytes;
     next = (next + 1) % kSlots;
     *out = n.map;
     return true;
@@ -761,20 +883,28 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
   if (attr_set_for_device != dev) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(kSmemBytes));
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_set_for_device = dev;
   }
+  const bool fp8 = a.cache_dtype == MLA_E4M3;
   CUtensorMap map, qmap, rmap;
   const uint64_t q_rows = static_cast<uint64_t>(a.batch) * a.q_len * 128;
   // cache as [num_pages*page_size rows][576] bf16, 64 x 64 boxes; q_lat as
   // [batch*q_len*128 rows][512] and q_rope as [..][64], 128 x 64 boxes
-  if (!cache.get(a.cache, static_cast<uint64_t>(a.num_pages) * a.page_size, kRow, kTileTok, &map) ||
+  if (!cache.get(a.cache, static_cast<uint64_t>(a.num_pages) * a.page_size, kRow, kTileTok, &map, fp8) ||
       !cache.get(a.q_lat, q_rows, kDC, 128, &qmap) || !cache.get(a.q_rope, q_rows, kDRope, 128, &rmap))
     return cudaErrorInvalidValue;
   const int64_t items = static_cast<int64_t>(a.batch) * a.q_len * a.num_splits;
-  decode_tc_kernel<<<dim3(static_cast<unsigned>(2 * items)), kThreads, kSmemBytes, s>>>(map, qmap, rmap, a);
+  const dim3 grid(static_cast<unsigned>(2 * items));
+  if (fp8)
+    decode_tc_kernel<true><<<grid, threads_for(true), kSmemBytes, s>>>(map, qmap, rmap, a);
+  else
+    decode_tc_kernel<false><<<grid, threads_for(false), kSmemBytes, s>>>(map, qmap, rmap, a);
   return cudaGetLastError();
 }
 

@@ -249,7 +249,9 @@ def append(pool, scales, c_kv, k_r, positions, slots, cos_t, sin_t, act_dtype: s
 def gather_rows(pool, scales, block_table_row, n_tokens: int, page_size: int,
                 cache_dtype: str) -> np.ndarray:
     """Logical rows 0..n_tokens-1 of one sequence, decoded to fp64, read through
-    its block table (paged layout, [P1] §4.1 'block size 64 page allocations')."""
+    its block table (paged layout, [P1] §4.1 'block size 64 page allocations').
+    E4M3 rows come back dequantised and rounded to bf16, the operand type of
+    the activations an E4M3 cache is used with."""
     pos = np.arange(n_tokens)
     pages = np.asarray(block_table_row, dtype=np.int64)[pos // page_size]
     slots = pages * page_size + pos % page_size
@@ -262,7 +264,10 @@ def gather_rows(pool, scales, block_table_row, n_tokens: int, page_size: int,
     sc = scales[slots].astype(np.float64)
     for gi, (a, b) in enumerate(E4M3_GROUPS):
         vals[:, a:b] *= sc[:, gi:gi + 1]
-    return vals
+    # An E4M3 cache pairs with bf16 activations, and the dequantised value
+    # code * scale (exact in fp64) enters the products as a bf16 operand:
+    # rounded to fp32 and then to bf16, both to nearest-even.
+    return round_bf16(vals)
 
 
 # ---------------------------------------------------------------------------

@@ -320,6 +320,27 @@ def test_decode_independent_of_page_permutation():
         assert np.array_equal(outs[0][b][0], outs[1][b][0])
 
 
+def test_e4m3_readback_values_by_hand():
+    """E4M3 rows read back as fl32(code * scale) rounded to bf16 (nearest-even),
+    each element scaled by its own group's factor. Expected values worked by hand:
+    0x38 is 1.0 and 0x3A is 1.25 (exponent field 7, mantissa 010); 0x7E is 448.
+    fl32(0.1) = 1.6000000238 * 2^-4 -> bf16 mantissa 205/128 -> 0.10009765625;
+    1.25 * fl32(1/3) = 0.41666668 -> 213/512 = 0.416015625; 448 * 3 = 1344 exact."""
+    pool = np.full((2, O.ROW), 0x38, dtype=np.uint8)
+    sc = np.ones((2, len(O.E4M3_GROUPS)), dtype=np.float32)
+    sc[1] = [0.1, 1.0 / 3.0, 3.0, 2.0, 0.5]
+    pool[1, 128] = 0x3A
+    pool[1, 256] = 0x7E
+    pool[1, 512] = 0xB8                      # -1.0 in the RoPE group
+    rows = O.gather_rows(pool, sc, np.array([0]), 2, 2, "e4m3")
+    assert np.all(rows[0] == 1.0)            # power-of-two scale: no rounding
+    assert rows[1, 0] == 0.10009765625 and rows[1, 127] == 0.10009765625
+    assert rows[1, 128] == 0.416015625
+    assert rows[1, 256] == 1344.0
+    assert rows[1, 511] == 2.0               # last latent element: group 3
+    assert rows[1, 512] == -0.5 and rows[1, 575] == 0.5   # RoPE part: group 4
+
+
 def test_e4m3_append_bounds():
     from mla_latent_kv_16_gb300 import workloads as W
     w = W.preset("fp8_lq2", batch=2, heads=8, seq_lens=[77, 64])
