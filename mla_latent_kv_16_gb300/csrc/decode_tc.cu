@@ -36,10 +36,11 @@
 // buffer has been read and its data landed); 2-9 = two warps per TMEM lane
 // quarter. On the quarters of this CTA's heads the two run the softmax of
 // alternate pages (the running max passes between them through shared
-// memory); on the other quarters both forward half of the peer's partial
-// scores each, and one of them also receives the peer's P rows and applies
-// its rescale factors to those O rows. In the epilogue each warp normalises
-// one half of the O columns of its quarter.
+// memory); on the other quarters one forwards the peer's partial scores as
+// soon as they are written (so that the score buffer is released early) and
+// the other receives the peer's P rows and applies its rescale factors to those
+// O rows. In the epilogue each warp normalises one half of the O columns of
+// its quarter.
 //
 // E4M3 cache ("Multi-Head Latent Attention (MLA): ..." "High-Throughput Serving
 // Kernels": FP8 latent cache with per-block scales): the TMA brings each page
@@ -168,7 +169,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
     mbar_init(smem_u32(&sm->empty_rope), 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&sm->s_full[x]), 1);
-      mbar_init(smem_u32(&sm->s_free[x]), 6);  // 2 softmax (the page's) + 4 forwarding warps
+      mbar_init(smem_u32(&sm->s_free[x]), 4);  // 2 softmax (the page's) + 2 forwarding warps
       mbar_init(smem_u32(&sm->s_in[x]), 1);
       mbar_init(smem_u32(&sm->rs_free[x]), 2);  // the peer's 2 softmax warps of the page
       mbar_init(smem_u32(&sm->p_in[x]), 1);
@@ -201,19 +202,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
   }
   if (warp == 1) tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
 
+  // The split's first page depends only on the split, so its block-table
+  // entries are read together with seq_lens, and thread 0 issues the TMA load
+  // of the first page before the work item's bounds are known. An entry that
+  // later proves bad (or a split past the sequence end) only moves that box out
+  // of the pool, where TMA reads the fill value; the load is drained on every path.
+  const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
+  const int pg_lo = split * a.pages_per_split;
+  const int pg_hi = min(a.max_pages, pg_lo + a.pages_per_split);
+  const int my_pg = pg_lo + static_cast<int>(threadIdx.x);
+  const int32_t my_entry = my_pg < pg_hi ? bt[my_pg] : 0;
+  bool spec0 = false;  // thread 0: page 0 of the split already requested
+  if (threadIdx.x == 0 && pg_lo < pg_hi) {
+    const int64_t yl = static_cast<int64_t>(my_entry) * P;
+    const int32_t y0 = (yl < 0 || yl >= a.num_pages * static_cast<int64_t>(P)) ? -kTileTok : static_cast<int32_t>(yl);
+    if constexpr (kFp8) {
+      mbar_arrive_expect_tx(smem_u32(&sm->raw_full[0]), 4 * kFp8BoxBytes);
+      for (int k = 0; k < 4; ++k)
+        tma_load_2d_nohint(smem_u32(sm->kv[0]) + kHalfBytes / 2 + k * kFp8BoxBytes, &tmap, smem_u32(&sm->raw_full[0]),
+                           col_half + 64 * k, y0);
+      if (r == 0) {
+        mbar_arrive_expect_tx(smem_u32(&sm->raw_rope_full), kFp8BoxBytes);
+        tma_load_2d_nohint(smem_u32(sm->rope) + kBoxBytes / 2, &tmap, smem_u32(&sm->raw_rope_full), 512, y0);
+      }
+    } else {
+      mbar_arrive_expect_tx(smem_u32(&sm->full_kv[0]), kHalfBytes);
+      for (int k = 0; k < 4; ++k)
+        tma_load_2d_nohint(smem_u32(sm->kv[0]) + k * kBoxBytes, &tmap, smem_u32(&sm->full_kv[0]), col_half + 64 * k,
+                           y0);
+      if (r == 0) {
+        mbar_arrive_expect_tx(smem_u32(&sm->full_rope), kBoxBytes);
+        tma_load_2d_nohint(smem_u32(sm->rope), &tmap, smem_u32(&sm->full_rope), 512, y0);
+      }
+    }
+    spec0 = true;
+  }
+
   const int L = a.seq_lens[b];
   const bool bad_len = (L < Lq) || (static_cast<int64_t>(L) > static_cast<int64_t>(a.max_pages) * P);
   if (bad_len && r == 0 && threadIdx.x == 0) flag_error(a.dev_error, MLA_DEVERR_BAD_SEQLEN);
   const int n_vis = bad_len ? 0 : L - Lq + j + 1;
-  const int tok_begin = split * a.pages_per_split * P;
+  const int tok_begin = pg_lo * P;
   const int tok_end = min(n_vis, (split + 1) * a.pages_per_split * P);
-  const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
   int n_tiles = 0;
   {
     int local_bad = 0;
     if (tok_begin < tok_end)
-      for (int pg = tok_begin / P + static_cast<int>(threadIdx.x); pg <= (tok_end - 1) / P; pg += threads_for(kFp8)) {
-        const int32_t pp = bt[pg];
+      for (int pg = my_pg; pg <= (tok_end - 1) / P; pg += threads_for(kFp8)) {
+        const int32_t pp = pg == my_pg ? my_entry : bt[pg];
         local_bad |= (pp < 0 || pp >= a.num_pages) ? 1 : 0;
       }
     if (__syncthreads_or(local_bad)) {
@@ -243,6 +279,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
     if (threadIdx.x == 0) {
       drain_wait(smem_u32(&sm->q_smem_full), 0, a.dev_error);
       drain_wait(smem_u32(&sm->q_tm_full), 0, a.dev_error);
+      if (spec0) {
+        drain_wait(smem_u32(kFp8 ? &sm->raw_full[0] : &sm->full_kv[0]), 0, a.dev_error);
+        if (r == 0) drain_wait(smem_u32(kFp8 ? &sm->raw_rope_full : &sm->full_rope), 0, a.dev_error);
+      }
     }
     write_empty(a, row0, bj, split, r);
   } else if (warp == 0) {
@@ -259,33 +299,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
         if ((t & 1) == static_cast<int>(r)) tma_prefetch_l2_2d(&tmap, 512, yp);
       };
       constexpr int kPrefetch = 3;
-      int issued_kv = 0, issued_rope = 0;
-      int32_t y_next = y_of(0);
-      for (int i = 0; i < n_tiles; ++i) {
-        const int32_t y = y_next;
-        if (i + 1 < n_tiles) y_next = y_of(i + 1);
-        if (i == 1 && !mbar_wait<kSleep>(smem_u32(&sm->q_ready), 0, abort_flag, a.dev_error)) break;
-        const int slot = i % kStages;
-        if (!mbar_wait<kSleep>(smem_u32(&sm->empty_kv[slot]), ((i / kStages) & 1) ^ 1, abort_flag, a.dev_error))
-          break;
-        if constexpr (kFp8) {
-          // E4M3 bytes into the upper half of the slot
-          mbar_arrive_expect_tx(smem_u32(&sm->raw_full[slot]), 4 * kFp8BoxBytes);
-          for (int k = 0; k < 4; ++k)
-            tma_load_2d(smem_u32(sm->kv[slot]) + kHalfBytes / 2 + k * kFp8BoxBytes, &tmap, smem_u32(&sm->raw_full[slot]),
-                        col_half + 64 * k, y, pol);
-        } else {
-          mbar_arrive_expect_tx(smem_u32(&sm->full_kv[slot]), kHalfBytes);
-          for (int k = 0; k < 4; ++k)
-            tma_load_2d(smem_u32(sm->kv[slot]) + k * kBoxBytes, &tmap, smem_u32(&sm->full_kv[slot]), col_half + 64 * k,
-                        y, pol);
+      // Two independent streams: the KV half of page i into ring slot i % 4 once
+      // PV(i-4) has released it, and this CTA's RoPE boxes (pages i = r mod 2)
+      // into the single RoPE buffer once QK of the previous one has read it.
+      int ik = spec0 ? 1 : 0;                             // next page whose KV half to load
+      int ir = (spec0 && r == 0) ? 2 : static_cast<int>(r);  // next RoPE page of this CTA
+      if (spec0)
+        for (int t = 1; t <= kPrefetch && t < n_tiles; ++t) prefetch(t);
+      bool q_in = false;  // Q has left slots 1-2 (they may take pages)
+      long long idle_since = 0;
+      bool ok = true;
+      while (ok && (ik < n_tiles || ir < n_tiles)) {
+        bool did = false;
+        if (ik < n_tiles) {
+          const int slot = ik % kStages;
+          if (ik == 1 && !q_in) q_in = mbar_test_wait(smem_u32(&sm->q_ready), 0);
+          if ((ik != 1 || q_in) &&
+              mbar_test_wait(smem_u32(&sm->empty_kv[slot]), ((ik / kStages) & 1) ^ 1)) {
+            const int32_t y = y_of(ik);
+            if constexpr (kFp8) {
+              // E4M3 bytes into the upper half of the slot
+              mbar_arrive_expect_tx(smem_u32(&sm->raw_full[slot]), 4 * kFp8BoxBytes);
+              for (int k = 0; k < 4; ++k)
+                tma_load_2d(smem_u32(sm->kv[slot]) + kHalfBytes / 2 + k * kFp8BoxBytes, &tmap,
+                            smem_u32(&sm->raw_full[slot]), col_half + 64 * k, y, pol);
+            } else {
+              mbar_arrive_expect_tx(smem_u32(&sm->full_kv[slot]), kHalfBytes);
+              for (int k = 0; k < 4; ++k)
+                tma_load_2d(smem_u32(sm->kv[slot]) + k * kBoxBytes, &tmap, smem_u32(&sm->full_kv[slot]),
+                            col_half + 64 * k, y, pol);
+            }
+            // pages ahead are pulled into L2 once this page's load is on its way
+            for (int t = (ik == 0 ? 1 : ik + kPrefetch); t <= ik + kPrefetch && t < n_tiles; ++t) prefetch(t);
+            ++ik;
+            did = true;
+          }
         }
-        issued_kv = i + 1;
-        // pages ahead are pulled into L2 once this page's load is on its way
-        for (int t = (i == 0 ? 1 : i + kPrefetch); t <= i + kPrefetch && t < n_tiles; ++t) prefetch(t);
-        if ((i & 1) == static_cast<int>(r)) {
-          // the k-th RoPE page of this CTA (k = i >> 1); the slot is free once QK of the previous one read it
-          if (!mbar_wait<kSleep>(smem_u32(&sm->empty_rope), ((i >> 1) & 1) ^ 1, abort_flag, a.dev_error)) break;
+        if (ir < n_tiles && mbar_test_wait(smem_u32(&sm->empty_rope), ((ir >> 1) & 1) ^ 1)) {
+          const int32_t y = y_of(ir);
           if constexpr (kFp8) {
             mbar_arrive_expect_tx(smem_u32(&sm->raw_rope_full), kFp8BoxBytes);
             tma_load_2d(smem_u32(sm->rope) + kBoxBytes / 2, &tmap, smem_u32(&sm->raw_rope_full), 512, y, pol);
@@ -293,14 +344,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
             mbar_arrive_expect_tx(smem_u32(&sm->full_rope), kBoxBytes);
             tma_load_2d(smem_u32(sm->rope), &tmap, smem_u32(&sm->full_rope), 512, y, pol);
           }
-          issued_rope = i + 1;
+          ir += 2;
+          did = true;
+        }
+        if (did) {
+          idle_since = 0;
+        } else {
+          // nothing to issue: suspend briefly on the next ring slot (or the RoPE buffer)
+          if (ik < n_tiles)
+            (void)mbar_try_wait_ns<200>(smem_u32(&sm->empty_kv[ik % kStages]), ((ik / kStages) & 1) ^ 1);
+          else
+            (void)mbar_try_wait_ns<200>(smem_u32(&sm->empty_rope), ((ir >> 1) & 1) ^ 1);
+          const long long now = clock64();
+          if (idle_since == 0) idle_since = now;
+          if (*abort_flag) ok = false;
+          if (now - idle_since > kWaitTimeoutCycles) {
+            *abort_flag = 1;
+            flag_error(a.dev_error, kDevErrTimeout);
+            ok = false;
+          }
         }
       }
-      for (int i = max(0, issued_kv - kStages); i < issued_kv; ++i)
+      // our own loads must land before the CTA tears down
+      for (int i = max(0, ik - kStages); i < ik; ++i)
         drain_wait(smem_u32(kFp8 ? &sm->raw_full[i % kStages] : &sm->full_kv[i % kStages]), (i / kStages) & 1,
                    a.dev_error);
-      if (issued_rope > 0)
-        drain_wait(smem_u32(kFp8 ? &sm->raw_rope_full : &sm->full_rope), ((issued_rope - 1) >> 1) & 1, a.dev_error);
+      if (ir - 2 >= 0)
+        drain_wait(smem_u32(kFp8 ? &sm->raw_rope_full : &sm->full_rope), ((ir - 2) >> 1) & 1, a.dev_error);
       drain_wait(smem_u32(&sm->q_smem_full), 0, a.dev_error);
       drain_wait(smem_u32(&sm->q_tm_full), 0, a.dev_error);
     }
@@ -663,33 +733,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       }
       sm->mlast[t][hl] = m_mine;
     } else {
-      // ================= forwarding (columns [32t, 32t+32) of each page's partial
-      // scores of the peer's heads -> its inbox); warp t == 1 also receives the
-      // peer's P rows and applies its rescale factors, page i after forwarding i+1
-      auto forward = [&](int i) -> bool {
-        const int sb = i & 1;
-        if (!wwait(&sm->s_full[sb], (i >> 1) & 1)) return false;
-        tc_fence_after();
-        float sv[32];
-        tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u + t * 32u, sv);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
-        if (i >= 2 && !wwait_cl(&sm->rs_free[sb], ((i - 2) >> 1) & 1)) return false;
-        const uint32_t dst = peer_sin + ((sb * 64 + hl) * kSinStride + t * 32) * 4;
-        const uint32_t sbar = peer_s_in + sb * 8;
-#pragma unroll
-        for (int v = 0; v < 8; ++v) st_async_v4(dst + v * 16, sv[4 * v], sv[4 * v + 1], sv[4 * v + 2], sv[4 * v + 3], sbar);
-        return true;
-      };
+      // ================= forwarding: warp t == 0 sends each page's partial scores
+      // of the peer's heads (all 64 columns) to its inbox, as soon as they are
+      // written, so that the score buffer is released early; warp t == 1 receives
+      // the peer's P rows and applies its rescale factors
       if (t == 0) {
-        for (int i = 0; ok && i < n_tiles; ++i) ok = forward(i);
-      } else {
-        const bool armer = (lane == 0) && ((q4 & 1) == 0);
-        ok = forward(0);
         for (int i = 0; ok && i < n_tiles; ++i) {
           const int sb = i & 1;
-          if (i + 1 < n_tiles && !forward(i + 1)) { ok = false; break; }
+          if (!wwait(&sm->s_full[sb], (i >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          float sv[64];
+          {
+            float (&s0)[32] = *reinterpret_cast<float (*)[32]>(&sv[0]);
+            float (&s1)[32] = *reinterpret_cast<float (*)[32]>(&sv[32]);
+            tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u, s0);
+            tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u + 32u, s1);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
+          if (i >= 2 && !wwait_cl(&sm->rs_free[sb], ((i - 2) >> 1) & 1)) { ok = false; break; }
+          const uint32_t dst = peer_sin + ((sb * 64 + hl) * kSinStride) * 4;
+          const uint32_t sbar = peer_s_in + sb * 8;
+#pragma unroll
+          for (int v = 0; v < 16; ++v)
+            st_async_v4(dst + v * 16, sv[4 * v], sv[4 * v + 1], sv[4 * v + 2], sv[4 * v + 3], sbar);
+        }
+      } else {
+        const bool armer = (lane == 0) && ((q4 & 1) == 0);
+        for (int i = 0; ok && i < n_tiles; ++i) {
+          const int sb = i & 1;
           if (!wwait_cl(&sm->p_in[sb], (i >> 1) & 1)) { ok = false; break; }
           if (armer && i + 2 < n_tiles) mbar_arrive_expect_tx(smem_u32(&sm->p_in[sb]), kPinBytes);
           const float alpha = sm->alpha_in[sb][hl];

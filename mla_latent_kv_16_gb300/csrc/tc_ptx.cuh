@@ -71,6 +71,21 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
+// Same with a suspend-time hint of kNs nanoseconds: a role that polls several
+// barriers parks on the likeliest one for at most that long.
+template <int kNs>
+__device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(kNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Acquire at cluster scope: for barriers a peer CTA arrives on remotely.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
