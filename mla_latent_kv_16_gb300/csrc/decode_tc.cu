@@ -105,7 +105,7 @@ struct __align__(1024) Smem {
   uint64_t p_in[2], rp_free[2];     // P rows from the peer landed / the peer's P tile is free
   uint64_t pt_free[2];              // PV of the page that last used P tile x is done
   uint64_t p_full[2];               // P of page i complete in tile i & 1 and O rescaled (4 warps)
-  uint64_t m_bar[2], pv_done, o_done, sum_bar, l_bar, drain;
+  uint64_t m_bar[2], o_done, sum_bar, l_bar, drain;
   uint64_t raw_full[kStages], raw_rope_full;  // E4M3 bytes landed (TMA)
   uint64_t cvt_bar;                           // both converter warps have read their page
   uint32_t tmem_base;
@@ -181,7 +181,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
     mbar_init(smem_u32(&sm->q_smem_full), 1);
     mbar_init(smem_u32(&sm->q_tm_full), 1);
     mbar_init(smem_u32(&sm->q_ready), kSmxWarps);
-    mbar_init(smem_u32(&sm->pv_done), 1);
     mbar_init(smem_u32(&sm->o_done), 1);
     mbar_init(smem_u32(&sm->sum_bar), 4);
     mbar_init(smem_u32(&sm->l_bar), 1);
@@ -386,12 +385,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       const uint64_t dRope0 = sdesc_sw128(smem_u32(sm->rope), 16, 1024);
       const uint64_t dQR = sdesc_sw128(smem_u32(sm->qr), 16, 1024);              // A: Q RoPE
       const uint64_t dP0 = sdesc_sw128(smem_u32(sm->pt[0]), 16, 1024);           // A: P (K-major)
+      // A barrier test costs a shared-memory round trip (hundreds of cycles under
+      // load), so every test of a polling round is issued unconditionally and
+      // the results are combined afterwards: their latencies overlap instead of
+      // adding up. Testing a barrier that does not apply is harmless.
       auto ready = [&](uint64_t* bar, uint32_t par) { return mbar_test_wait(smem_u32(bar), par); };
       auto qk_ready = [&](int i) {
-        if (i >= 2 && !ready(&sm->s_free[i & 1], ((i - 2) >> 1) & 1)) return false;
-        if (!ready(&sm->full_kv[i % kStages], (i / kStages) & 1)) return false;
-        if ((i & 1) == static_cast<int>(r) && !ready(&sm->full_rope, (i >> 1) & 1)) return false;
-        return true;
+        const bool f = ready(&sm->s_free[i & 1], ((i - 2) >> 1) & 1);
+        const bool k = ready(&sm->full_kv[i % kStages], (i / kStages) & 1);
+        const bool q = ready(&sm->full_rope, (i >> 1) & 1);
+        return (f | (i < 2)) & k & (q | ((i & 1) != static_cast<int>(r)));
       };
       auto issue_qk = [&](int i) {
         const uint32_t dS = tmem + kTmS + static_cast<uint32_t>(i & 1) * 64u;
@@ -417,7 +420,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           mma_ss(tmem + kTmO, dp + ((kk * 32u) >> 4), dv + ((kk * 16u * 128u) >> 4), kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(smem_u32(&sm->empty_kv[slot]));
         mma_commit(smem_u32(&sm->pt_free[i & 1]));
-        mma_commit(smem_u32(&sm->pv_done));
         if (i == n_tiles - 1) mma_commit(smem_u32(&sm->o_done));
       };
       bool ok = mbar_wait<kPlain>(smem_u32(&sm->q_ready), 0, abort_flag, a.dev_error) &&
@@ -427,11 +429,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       long long idle_since = 0;
       while (ok && np < n_tiles) {
         bool did = false;
-        if (np < nq && ready(&sm->p_full[np & 1], (np >> 1) & 1)) {
+        const bool pv_ok = ready(&sm->p_full[np & 1], (np >> 1) & 1) & (np < nq);
+        const bool qk_ok = qk_ready(min(nq, n_tiles - 1)) & (nq < n_tiles);
+        if (pv_ok) {
           tc_fence_after();
           issue_pv(np++);
           did = true;
-        } else if (nq < n_tiles && qk_ready(nq)) {
+        } else if (qk_ok) {
           tc_fence_after();
           issue_qk(nq++);
           did = true;
@@ -708,11 +712,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           bulk_copy_to_peer(peer_pt + rows, smem_u32(sm->pt[0]) + rows, 32 * 128, peer_p_in + sb * 8);
           bulk_copy_to_peer(peer_alpha + al, smem_u32(&sm->alpha_out[0][0]) + al, 32 * 4, peer_p_in + sb * 8);
         }
-        // O rows of this CTA's heads may be rescaled only after PV(i-1). (PV(i-2)
-        // is complete -- the P tile wait above -- so pv_done is at most one phase
+        // O rows of this CTA's heads may be rescaled only after PV(i-1), which
+        // completes phase (i-1) >> 1 of pt_free[(i-1) & 1]. (PV(i+1) cannot run
+        // before this page's P is complete, so that barrier is at most one phase
         // behind and its parity wait cannot alias.)
         if (resc_any) {
-          if (!wwait(&sm->pv_done, (i - 1) & 1)) { ok = false; break; }
+          if (!wwait(&sm->pt_free[(i - 1) & 1], ((i - 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           rescale_o(alpha, 0, 256);
         }
