@@ -74,6 +74,8 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
 
 template <typename InT, int kCache>
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  pdl_trigger();
+  pdl_wait();  // the previous step's readers of the cache are done
   const int token = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (token >= a.n_tokens) return;
@@ -145,16 +147,12 @@ cudaError_t launch_in(const AppendArgs& a, cudaStream_t s) {
   const int blocks = (a.n_tokens + 7) / 8;
   switch (a.cache_dtype) {
     case MLA_F32:
-      append_kernel<InT, kCacheF32><<<blocks, threads, 0, s>>>(a);
-      break;
+      return launch_pdl(append_kernel<InT, kCacheF32>, dim3(blocks), dim3(threads), 0, s, a);
     case MLA_BF16:
-      append_kernel<InT, kCacheBF16><<<blocks, threads, 0, s>>>(a);
-      break;
+      return launch_pdl(append_kernel<InT, kCacheBF16>, dim3(blocks), dim3(threads), 0, s, a);
     default:
-      append_kernel<InT, kCacheE4M3><<<blocks, threads, 0, s>>>(a);
-      break;
+      return launch_pdl(append_kernel<InT, kCacheE4M3>, dim3(blocks), dim3(threads), 0, s, a);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace

@@ -20,6 +20,12 @@ constexpr float kE4M3Max = 448.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Programmatic dependent launch (see launch_pdl): let the next kernel in the
+// stream start, and wait until every earlier kernel has completed and its
+// writes are visible.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void flag_error(int32_t* flag, int32_t bits) {
   if (flag != nullptr) atomicOr(flag, bits);
 }

@@ -52,6 +52,8 @@ __device__ __forceinline__ void load_row(const void* cache, const float* scales,
 
 template <typename T, int kCache>
 __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float smem[];
   float* rs = smem;                          // [kTile][kRowPad]
   float* qs = smem + kTile * kRowPad;        // [kHG][kRow]
@@ -168,6 +170,8 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
 // each lane merges 16 consecutive columns of the 512 with 16-byte loads.
 template <typename T>
 __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x * 4 + warp, bj = blockIdx.y;
   if (h >= a.heads) return;
@@ -240,8 +244,7 @@ cudaError_t launch_decode_c(const DecodeArgs& a, cudaStream_t s) {
   const cudaError_t e = ensure_smem(decode_simt_kernel<T, kCache>, kSimtSmem, done_for);
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_splits, (a.heads + kHG - 1) / kHG, a.batch * a.q_len);
-  decode_simt_kernel<T, kCache><<<grid, 256, kSimtSmem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(decode_simt_kernel<T, kCache>, grid, dim3(256), kSimtSmem, s, a);
 }
 
 template <typename T>
@@ -264,11 +267,8 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s) {
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
   if (a.batch == 0 || a.num_splits == 1) return cudaSuccess;
   dim3 grid((a.heads + 3) / 4, a.batch * a.q_len);
-  if (a.act == MLA_F32)
-    combine_kernel<float><<<grid, 128, 0, s>>>(a);
-  else
-    combine_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.act == MLA_F32) return launch_pdl(combine_kernel<float>, grid, dim3(128), 0, s, a);
+  return launch_pdl(combine_kernel<__nv_bfloat16>, grid, dim3(128), 0, s, a);
 }
 
 }  // namespace mla

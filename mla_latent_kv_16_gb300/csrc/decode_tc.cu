@@ -155,7 +155,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
   const int64_t row0 = static_cast<int64_t>(bj) * 128;
   const int32_t col_half = static_cast<int32_t>(256u * r);  // first latent column of this CTA's half
 
-  // ---- set-up that needs no data of the work item, overlapped with reading it
+  // ---- set-up that reads no data of the previous kernels (it may run while
+  // they finish: programmatic dependent launch), then the wait for them
+  pdl_trigger();
   if (threadIdx.x == 0) {
     // E4M3: the converter warps (2) complete full_kv / full_rope, the TMA raw_full
     for (int s = 0; s < kStages; ++s) {
@@ -187,11 +189,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
     mbar_init(smem_u32(&sm->drain), 1);
     sm->abort_flag = 0;
     fence_mbar_init_cluster();
-    // Q's RoPE part -> qr; Q's own latent half -> slots 1-2, from where the
-    // softmax warps copy it into TMEM before pages 1 and 2 are loaded there
     prefetch_tmap(&tmap);
     prefetch_tmap(&qmap);
     prefetch_tmap(&rmap);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
+  pdl_wait();
+
+  if (threadIdx.x == 0) {
+    // Q's RoPE part -> qr; Q's own latent half -> slots 1-2, from where the
+    // softmax warps copy it into TMEM before pages 1 and 2 are loaded there
     mbar_arrive_expect_tx(smem_u32(&sm->q_smem_full), kQBoxBytes);
     tma_load_2d_nohint(smem_u32(sm->qr), &rmap, smem_u32(&sm->q_smem_full), 0, static_cast<int32_t>(row0));
     mbar_arrive_expect_tx(smem_u32(&sm->q_tm_full), 4 * kQBoxBytes);
@@ -199,7 +206,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       tma_load_2d_nohint(smem_u32(sm->kv[1]) + k * kQBoxBytes, &qmap, smem_u32(&sm->q_tm_full), col_half + 64 * k,
                          static_cast<int32_t>(row0));
   }
-  if (warp == 1) tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
 
   // The split's first page depends only on the split, so its block-table
   // entries are read together with seq_lens, and thread 0 issues the TMA load
@@ -979,11 +985,8 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const int64_t items = static_cast<int64_t>(a.batch) * a.q_len * a.num_splits;
   const dim3 grid(static_cast<unsigned>(2 * items));
-  if (fp8)
-    decode_tc_kernel<true><<<grid, threads_for(true), kSmemBytes, s>>>(map, qmap, rmap, a);
-  else
-    decode_tc_kernel<false><<<grid, threads_for(false), kSmemBytes, s>>>(map, qmap, rmap, a);
-  return cudaGetLastError();
+  if (fp8) return launch_pdl(decode_tc_kernel<true>, grid, dim3(threads_for(true)), kSmemBytes, s, map, qmap, rmap, a);
+  return launch_pdl(decode_tc_kernel<false>, grid, dim3(threads_for(false)), kSmemBytes, s, map, qmap, rmap, a);
 }
 
 }  // namespace mla

@@ -5,9 +5,34 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "mla.h"
 
 namespace mla {
+
+// Every kernel of the library is launched with programmatic stream
+// serialization: it may start while the previous kernel in the stream is still
+// running, does only work that touches no data an earlier kernel writes
+// (barrier set-up, TMEM allocation, static weights), and executes
+// griddepcontrol.wait (pdl_wait) before anything else. Each kernel triggers its
+// own dependents at entry (pdl_trigger). A kernel the caller launched before
+// ours never triggers early, so our kernels start early only behind our own.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct AppendArgs {
   const void* c_kv;

@@ -18,6 +18,8 @@ constexpr int kOutTok = 16;
 // grid (512/128, H, ceil(n/32)), block 128: thread = one latent column c.
 template <typename T>
 __global__ void __launch_bounds__(128) absorb_simt_kernel(ProjArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float qs[kAbsorbTok][kDNope];
   const int c = blockIdx.x * 128 + threadIdx.x;
   const int h = blockIdx.y;
@@ -49,6 +51,8 @@ __global__ void __launch_bounds__(128) absorb_simt_kernel(ProjArgs a) {
 // Lane l owns latent columns l + 32 i.
 template <typename T>
 __global__ void __launch_bounds__(128) out_proj_simt_kernel(ProjArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float us[kOutTok][kDC];
   const int h = blockIdx.x;
   const int t0 = blockIdx.y * kOutTok;
@@ -83,21 +87,15 @@ __global__ void __launch_bounds__(128) out_proj_simt_kernel(ProjArgs a) {
 cudaError_t launch_absorb_simt(const ProjArgs& a, cudaStream_t s) {
   if (a.n_tokens == 0) return cudaSuccess;
   dim3 grid(kDC / 128, a.heads, (a.n_tokens + kAbsorbTok - 1) / kAbsorbTok);
-  if (a.act == MLA_F32)
-    absorb_simt_kernel<float><<<grid, 128, 0, s>>>(a);
-  else
-    absorb_simt_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.act == MLA_F32) return launch_pdl(absorb_simt_kernel<float>, grid, dim3(128), 0, s, a);
+  return launch_pdl(absorb_simt_kernel<__nv_bfloat16>, grid, dim3(128), 0, s, a);
 }
 
 cudaError_t launch_out_proj_simt(const ProjArgs& a, cudaStream_t s) {
   if (a.n_tokens == 0) return cudaSuccess;
   dim3 grid(a.heads, (a.n_tokens + kOutTok - 1) / kOutTok);
-  if (a.act == MLA_F32)
-    out_proj_simt_kernel<float><<<grid, 128, 0, s>>>(a);
-  else
-    out_proj_simt_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.act == MLA_F32) return launch_pdl(out_proj_simt_kernel<float>, grid, dim3(128), 0, s, a);
+  return launch_pdl(out_proj_simt_kernel<__nv_bfloat16>, grid, dim3(128), 0, s, a);
 }
 
 }  // namespace mla

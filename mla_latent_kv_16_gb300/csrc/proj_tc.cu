@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kThreads) proj_tc_kernel(const __grid_constant
   const int n_tok = min(kMaxTok, p.n_tokens - t0);
   constexpr int kK = kKind == 0 ? kDNope : kDC;
   constexpr int kChunks = kK / kChunkK;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -80,30 +81,41 @@ __global__ void __launch_bounds__(kThreads) proj_tc_kernel(const __grid_constant
   const uint32_t tmem = ctl->tmem_base;
   volatile int32_t* abort_flag = &ctl->abort_flag;
 
+  // Chunk k of the weight slice (A) and of the activations (B) into stage s,
+  // one barrier for both. The weights are static, so the first stages' A
+  // boxes are requested before waiting for the previous kernels; the
+  // activations they produced only after.
+  auto load_a = [&](int k, int s) {
+    const uint32_t a_dst = smem_u32(base + s * stage_bytes);
+    const uint32_t bar = smem_u32(&ctl->full[s]);
+    mbar_arrive_expect_tx(bar, kABytes + b_bytes);
+    if constexpr (kKind == 0) {
+      // W_UK[h] rows d in [64k, 64k+64), columns c in [128 m, 128 m + 128): two 64-column boxes
+      tma_load_2d_nohint(a_dst, &amap, bar, 128 * mslice, h * kDNope + kChunkK * k);
+      tma_load_2d_nohint(a_dst + kABytes / 2, &amap, bar, 128 * mslice + 64, h * kDNope + kChunkK * k);
+    } else {
+      // W_UV[h] rows d in [0,128), columns c in [64k, 64k+64)
+      tma_load_2d_nohint(a_dst, &amap, bar, kChunkK * k, h * kDV);
+    }
+  };
+  auto load_b = [&](int k, int s) {
+    const uint32_t b_dst = smem_u32(base + s * stage_bytes) + kABytes;
+    const uint32_t bar = smem_u32(&ctl->full[s]);
+    // X[:, h, 64k : 64k+64] for tokens t0 .. t0+n_tile (rows past n_tokens read as zero)
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+            b_dst),
+        "l"(reinterpret_cast<uint64_t>(&bmap)), "r"(bar), "r"(kChunkK * k), "r"(h), "r"(t0)
+        : "memory");
+  };
+  const int pre = min(stages, kChunks);
+  if (threadIdx.x == 0)
+    for (int k = 0; k < pre; ++k) load_a(k, k);
+  pdl_wait();
+
   if (threadIdx.x == 0) {
     const uint32_t idesc = idesc_bf16_f32(128, n_tile, kKind == 0, false);
-    auto load_chunk = [&](int k, int s) {
-      const uint32_t a_dst = smem_u32(base + s * stage_bytes);
-      const uint32_t b_dst = a_dst + kABytes;
-      const uint32_t bar = smem_u32(&ctl->full[s]);
-      mbar_arrive_expect_tx(bar, kABytes + b_bytes);
-      if constexpr (kKind == 0) {
-        // W_UK[h] rows d in [64k, 64k+64), columns c in [128 m, 128 m + 128): two 64-column boxes
-        tma_load_2d_nohint(a_dst, &amap, bar, 128 * mslice, h * kDNope + kChunkK * k);
-        tma_load_2d_nohint(a_dst + kABytes / 2, &amap, bar, 128 * mslice + 64, h * kDNope + kChunkK * k);
-      } else {
-        // W_UV[h] rows d in [0,128), columns c in [64k, 64k+64)
-        tma_load_2d_nohint(a_dst, &amap, bar, kChunkK * k, h * kDV);
-      }
-      // X[:, h, 64k : 64k+64] for tokens t0 .. t0+n_tile (rows past n_tokens read as zero)
-      asm volatile(
-          "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
-              b_dst),
-          "l"(reinterpret_cast<uint64_t>(&bmap)), "r"(bar), "r"(kChunkK * k), "r"(h), "r"(t0)
-          : "memory");
-    };
-    const int pre = min(stages, kChunks);
-    for (int k = 0; k < pre; ++k) load_chunk(k, k);
+    for (int k = 0; k < pre; ++k) load_b(k, k);
     bool ok = true;
     for (int k = 0; k < kChunks && ok; ++k) {
       const int s = k % stages;
@@ -129,7 +141,8 @@ __global__ void __launch_bounds__(kThreads) proj_tc_kernel(const __grid_constant
           ok = false;
           break;
         }
-        load_chunk(k + stages, s);
+        load_a(k + stages, s);
+        load_b(k + stages, s);
       }
     }
     mma_commit(smem_u32(&ctl->done));
@@ -242,8 +255,7 @@ cudaError_t launch_proj(const ProjArgs& a, cudaStream_t s) {
     attr_dev = dev;
   }
   const dim3 grid(a.heads, kKind == 0 ? kDC / 128 : 1, (a.n_tokens + kMaxTok - 1) / kMaxTok);
-  proj_tc_kernel<kKind><<<grid, kThreads, smem, s>>>(am, bm, a, n_tile, stages, cols);
-  return cudaGetLastError();
+  return launch_pdl(proj_tc_kernel<kKind>, grid, dim3(kThreads), smem, s, am, bm, a, n_tile, stages, cols);
 }
 
 }  // namespace
