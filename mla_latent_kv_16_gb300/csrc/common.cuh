@@ -37,8 +37,10 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
+// Two fp32 -> bf16 (round to nearest even), lo in the low half: one paired conversion.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return uint32_t(f32_to_bf16_bits(lo)) | (uint32_t(f32_to_bf16_bits(hi)) << 16);
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // Exact E4M3FN -> fp32 decode of one byte (bias 7, subnormals, no inf).

@@ -628,12 +628,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
         if (!wwait(&sm->s_full[sb], ph2)) { ok = false; break; }
         tc_fence_after();
         float s[64];
-        {
-          float (&s0)[32] = *reinterpret_cast<float (*)[32]>(&s[0]);
-          float (&s1)[32] = *reinterpret_cast<float (*)[32]>(&s[32]);
-          tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u, s0);
-          tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u + 32u, s1);
-        }
+        tmem_ld64_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u, s);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
@@ -754,12 +749,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           if (!wwait(&sm->s_full[sb], (i >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           float sv[64];
-          {
-            float (&s0)[32] = *reinterpret_cast<float (*)[32]>(&sv[0]);
-            float (&s1)[32] = *reinterpret_cast<float (*)[32]>(&sv[32]);
-            tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u, s0);
-            tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u + 32u, s1);
-          }
+          tmem_ld64_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u, sv);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
