@@ -463,35 +463,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       drain_wait(smem_u32(&sm->drain), 0, a.dev_error);
     }
   } else if (kFp8 && warp >= kCvtWarp0) {
-    // ================= E4M3 -> bf16 (x scale) in place, one page row per lane
-    const int row = (warp - kCvtWarp0) * 32 + lane;
+    // ================= E4M3 -> bf16 (x scale) in place
+    // The raw bytes of box k (64 rows x 64 B, unswizzled) sit at kHalfBytes/2 +
+    // k * 4 KB of the slot. Converter thread c (0..63) takes the 16-byte chunks
+    // g = 64 j + c, j = 0..15 (box g / 256, row (g / 4) mod 64, chunk g mod 4), so
+    // every warp-wide load reads 512 contiguous bytes (no bank conflicts); the
+    // RoPE box's 256 chunks go the same way, j = 0..3. A thread's chunks cover
+    // rows c/4 + 16m (m = 0..3) of every box, so it needs 8 latent scales (groups
+    // 2r for boxes 0-1, 2r+1 for boxes 2-3) and, on RoPE pages, 4 RoPE scales.
+    const int c = (warp - kCvtWarp0) * 32 + lane;
+    const int row_base = c >> 2, chunk = c & 3;
     const float* scales = a.scales;
     bool ok = true;
+    // 16 E4M3 values (one uint4) x scale -> 16 bf16 (two 16-byte chunks)
+    auto convert16 = [&](const uint4& x, float sc, uint4& lo, uint4& hi) {
+      const uint32_t wds[4] = {x.x, x.y, x.z, x.w};
+      uint32_t outw[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint16_t pair = static_cast<uint16_t>(wds[q] >> (16 * hh));
+          uint32_t h2;
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+          outw[2 * q + hh] = pack_bf16x2(f.x * sc, f.y * sc);
+        }
+      }
+      lo = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+      hi = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+    };
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int slot = i % kStages;
       const bool rope_page = (i & 1) == static_cast<int>(r);
       const int tok = tok_begin + i * kTileTok;
-      const int64_t y = static_cast<int64_t>(bt[tok / P]) * P + (tok % P) + row;  // pool row
-      // this row's scales: groups 2r, 2r+1 (this CTA's latent half) and 4 (RoPE)
-      const float sc0 = scales[y * MLA_E4M3_GROUPS + 2 * r];
-      const float sc1 = scales[y * MLA_E4M3_GROUPS + 2 * r + 1];
-      const float scr = rope_page ? scales[y * MLA_E4M3_GROUPS + 4] : 0.0f;
+      const int64_t y0 = static_cast<int64_t>(bt[tok / P]) * P + (tok % P);  // pool row of page row 0
+      float sc_lat[4][2], sc_rope[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float* srow = scales + (y0 + row_base + 16 * m) * MLA_E4M3_GROUPS;
+        sc_lat[m][0] = srow[2 * r];
+        sc_lat[m][1] = srow[2 * r + 1];
+        sc_rope[m] = rope_page ? srow[4] : 0.0f;
+      }
       if (!__all_sync(0xffffffffu, mbar_wait<kPlain>(smem_u32(&sm->raw_full[slot]), (i / kStages) & 1, abort_flag,
                                                       a.dev_error))) { ok = false; break; }
       if (rope_page && !__all_sync(0xffffffffu, mbar_wait<kPlain>(smem_u32(&sm->raw_rope_full), (i >> 1) & 1,
                                                                    abort_flag, a.dev_error))) { ok = false; break; }
-      // read the whole row first: the bf16 output overlaps the bytes of other rows
+      // read every chunk first: the bf16 output overlaps the raw bytes of other chunks
       uint8_t* kvs = sm->kv[slot];
       uint4 raw[16], rraw[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          raw[4 * k + v] = *reinterpret_cast<const uint4*>(kvs + kHalfBytes / 2 + k * kFp8BoxBytes + row * 64 + v * 16);
+      for (int j = 0; j < 16; ++j) raw[j] = *reinterpret_cast<const uint4*>(kvs + kHalfBytes / 2 + (j * 64 + c) * 16);
       if (rope_page) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          rraw[v] = *reinterpret_cast<const uint4*>(sm->rope + kBoxBytes / 2 + row * 64 + v * 16);
+        for (int j = 0; j < 4; ++j) rraw[j] = *reinterpret_cast<const uint4*>(sm->rope + kBoxBytes / 2 + (j * 64 + c) * 16);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm->cvt_bar));
@@ -499,44 +525,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
         ok = false;
         break;
       }
-      // 16 E4M3 values (one uint4) -> 16 bf16 x scale (two 16-byte chunks)
-      auto convert16 = [&](const uint4& x, float sc, uint4& lo, uint4& hi) {
-        const uint32_t wds[4] = {x.x, x.y, x.z, x.w};
-        uint32_t outw[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint16_t pair = static_cast<uint16_t>(wds[q] >> (16 * hh));
-            uint32_t h2;
-            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-            outw[2 * q + hh] = pack_bf16x2(f.x * sc, f.y * sc);
-          }
-        }
-        lo = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-        hi = make_uint4(outw[4], outw[5], outw[6], outw[7]);
-      };
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float sc = k < 2 ? sc0 : sc1;  // 64-column boxes 0,1 in group 2r, 2,3 in group 2r+1
-        uint8_t* dst = kvs + k * kBoxBytes + row * 128;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 lo, hi;
-          convert16(raw[4 * k + v], sc, lo, hi);
-          *reinterpret_cast<uint4*>(dst + (((2 * v) ^ (row & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(dst + (((2 * v + 1) ^ (row & 7)) << 4)) = hi;
-        }
+      for (int j = 0; j < 16; ++j) {
+        const int k = j >> 2, m = j & 3;  // box; which of this thread's rows
+        const int rr = row_base + 16 * m;
+        uint4 lo, hi;
+        convert16(raw[j], sc_lat[m][k >> 1], lo, hi);
+        uint8_t* dst = kvs + k * kBoxBytes + rr * 128;
+        *reinterpret_cast<uint4*>(dst + (((2 * chunk) ^ (rr & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4*>(dst + (((2 * chunk + 1) ^ (rr & 7)) << 4)) = hi;
       }
       if (rope_page) {
-        uint8_t* dst = sm->rope + row * 128;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
+        for (int j = 0; j < 4; ++j) {
+          const int rr = row_base + 16 * j;
           uint4 lo, hi;
-          convert16(rraw[v], scr, lo, hi);
-          *reinterpret_cast<uint4*>(dst + (((2 * v) ^ (row & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(dst + (((2 * v + 1) ^ (row & 7)) << 4)) = hi;
+          convert16(rraw[j], sc_rope[j], lo, hi);
+          uint8_t* dst = sm->rope + rr * 128;
+          *reinterpret_cast<uint4*>(dst + (((2 * chunk) ^ (rr & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((2 * chunk + 1) ^ (rr & 7)) << 4)) = hi;
         }
       }
       fence_proxy_async_smem();  // generic writes -> the MMAs' operand reads
