@@ -93,7 +93,7 @@ struct __align__(1024) Smem {
   float sin[2][64][kSinStride];     // peer's partial scores for this CTA's heads
   float alpha_in[2][64];            // peer's rescale factors for the peer's heads
   float alpha_out[2][64];           // this CTA's rescale factors, bulk-copied to the peer
-  float mh[2][64];                  // running max after page i (log2 units), in mh[i & 1]
+  float mx_part[2][2][64];          // page i's row max over the token half t of each own head, in [i & 1][t]
   float lsum[2][64];                // each softmax warp's row sum, for the epilogue
   float mlast[2][64];               // the max each softmax warp's row sum refers to
   float l_in[64];                   // peer's row sums for the peer's heads
@@ -105,7 +105,7 @@ struct __align__(1024) Smem {
   uint64_t p_in[2], rp_free[2];     // P rows from the peer landed / the peer's P tile is free
   uint64_t pt_free[2];              // PV of the page that last used P tile x is done
   uint64_t p_full[2];               // P of page i complete in tile i & 1 and O rescaled (4 warps)
-  uint64_t m_bar[2], o_done, sum_bar, l_bar, drain;
+  uint64_t o_done, sum_bar, l_bar, drain;
   uint64_t raw_full[kStages], raw_rope_full;  // E4M3 bytes landed (TMA)
   uint64_t cvt_bar;                           // both converter warps have read their page
   uint32_t tmem_base;
@@ -171,14 +171,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
     mbar_init(smem_u32(&sm->empty_rope), 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&sm->s_full[x]), 1);
-      mbar_init(smem_u32(&sm->s_free[x]), 4);  // 2 softmax (the page's) + 2 forwarding warps
+      mbar_init(smem_u32(&sm->s_free[x]), 6);  // 4 softmax + 2 forwarding warps
       mbar_init(smem_u32(&sm->s_in[x]), 1);
-      mbar_init(smem_u32(&sm->rs_free[x]), 2);  // the peer's 2 softmax warps of the page
+      mbar_init(smem_u32(&sm->rs_free[x]), 4);  // the peer's 4 softmax warps
       mbar_init(smem_u32(&sm->p_in[x]), 1);
       mbar_init(smem_u32(&sm->rp_free[x]), 1);
-      mbar_init(smem_u32(&sm->m_bar[x]), 2);
       mbar_init(smem_u32(&sm->pt_free[x]), 1);
-      mbar_init(smem_u32(&sm->p_full[x]), 4);  // 2 softmax (the page's) + 2 P-path warps
+      mbar_init(smem_u32(&sm->p_full[x]), 6);  // 4 softmax + 2 P-path warps
     }
     mbar_init(smem_u32(&sm->q_smem_full), 1);
     mbar_init(smem_u32(&sm->q_tm_full), 1);
@@ -625,126 +624,136 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       tmem_wait_st();
     };
     if (own) {
-      // ================= softmax of this CTA's heads, all 64 tokens of the pages i = t mod 2
-      const bool armer = (lane == 0) && ((q4 & 1) == 0);
-      float m_mine = -CUDART_INF_F;  // the max this warp's row sum l refers to
-      for (int i = t; ok && i < n_tiles; i += 2) {
+      // ================= softmax of this CTA's heads. Both warps of the quarter
+      // take every page, warp t the token columns [32t, 32t+32). They meet twice
+      // per page on a named barrier that also ANDs their status: for the page's
+      // row max (each then derives the same running max, so no state passes
+      // between pages) and once both halves of the P rows are written (before the
+      // bulk copy to the peer). A failed (timed-out) wait is carried to the next
+      // meeting, so both warps leave the loop together.
+      const int qo = static_cast<int>(q4 & 1);
+      // named barriers 1, 2 (row max) and 3, 4 (P written) for own quarters 0, 1
+      auto meet = [&](int which, bool v) -> bool {
+        if (which == 0) return qo == 0 ? bar_red_and<1, 64>(v) : bar_red_and<2, 64>(v);
+        return qo == 0 ? bar_red_and<3, 64>(v) : bar_red_and<4, 64>(v);
+      };
+      const bool armer = (lane == 0) && (qo == 0) && (t == 0);
+      for (int i = 0; i < n_tiles; ++i) {
         const int sb = i & 1;
         const uint32_t ph2 = (i >> 1) & 1;  // phase parity of the per-parity barriers for page i
         const int page_valid = min(kTileTok, tok_end - (tok_begin + i * kTileTok));
-        if (!wwait(&sm->s_full[sb], ph2)) { ok = false; break; }
-        tc_fence_after();
-        float s[64];
-        tmem_ld64_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u, s);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
+        bool good = ok && wwait(&sm->s_full[sb], ph2);
+        float s[32];
+        if (good) {
+          tc_fence_after();
+          tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 64u + t * 32u, s);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
+        }
         // ---- full scores of this CTA's heads: own partial + the peer's
-        if (!wwait_cl(&sm->s_in[sb], ph2)) { ok = false; break; }
-        if (armer && i + 2 < n_tiles) mbar_arrive_expect_tx(smem_u32(&sm->s_in[sb]), kSinBytes);
-        {
-          const float4* src = reinterpret_cast<const float4*>(&sm->sin[sb][hl][0]);
+        good = good && wwait_cl(&sm->s_in[sb], ph2);
+        if (good) {
+          if (armer && i + 2 < n_tiles) mbar_arrive_expect_tx(smem_u32(&sm->s_in[sb]), kSinBytes);
+          const float4* src = reinterpret_cast<const float4*>(&sm->sin[sb][hl][32 * t]);
 #pragma unroll
-          for (int v = 0; v < 16; ++v) {
+          for (int v = 0; v < 8; ++v) {
             const float4 x = src[v];
             s[4 * v] += x.x;
             s[4 * v + 1] += x.y;
             s[4 * v + 2] += x.z;
             s[4 * v + 3] += x.w;
           }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote_relaxed(peer_rs_free + sb * 8);  // the peer may refill this inbox
-        // ---- online softmax over this page
-        if (page_valid < kTileTok) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote_relaxed(peer_rs_free + sb * 8);  // the peer may refill this inbox
+          // ---- online softmax over this page
+          if (page_valid < kTileTok) {
 #pragma unroll
-          for (int x = 0; x < 64; ++x)
-            if (x >= page_valid) s[x] = -CUDART_INF_F;
-        }
-        float mx;
-        {
-          float t32[32];
+            for (int x = 0; x < 32; ++x)
+              if (32 * t + x >= page_valid) s[x] = -CUDART_INF_F;
+          }
+          float t16[16];
 #pragma unroll
-          for (int x = 0; x < 32; ++x) t32[x] = fmaxf(s[x], s[x + 32]);
+          for (int x = 0; x < 16; ++x) t16[x] = fmaxf(s[x], s[x + 16]);
 #pragma unroll
-          for (int w = 16; w >= 1; w >>= 1)
+          for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
-            for (int x = 0; x < w; ++x) t32[x] = fmaxf(t32[x], t32[x + w]);
-          mx = t32[0];
+            for (int x = 0; x < w; ++x) t16[x] = fmaxf(t16[x], t16[x + w]);
+          sm->mx_part[sb][t][hl] = t16[0];
         }
-        // the running max after page i-1 comes from the other warp of this quarter
-        float m_prev = -CUDART_INF_F;
-        if (i > 0) {
-          if (!wwait(&sm->m_bar[(i - 1) & 1], ((i - 1) >> 1) & 1)) { ok = false; break; }
-          m_prev = sm->mh[(i - 1) & 1][hl];
-        }
+        if (!meet(0, good)) { ok = false; break; }
+        const float mx = fmaxf(sm->mx_part[sb][0][hl], sm->mx_part[sb][1][hl]);
         const bool first = (i == 0);
+        const float m_prev = m;
         const float m_new = fmaxf(m_prev, mx * c2);
         const bool resc = !first && (m_new > m_prev + kRescaleLog2);
         const float m_use = (first || resc) ? m_new : m_prev;
-        sm->mh[sb][hl] = m_use;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm->m_bar[sb]));
         const float alpha = resc ? fast_exp2(m_prev - m_use) : 1.0f;  // for O, relative to page i-1
         float rsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        uint32_t pw[32];
+        uint32_t pw[16];
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
+        for (int x = 0; x < 16; ++x) {
           const float p0 = fast_exp2(fmaf(s[2 * x], c2, -m_use));
           const float p1 = fast_exp2(fmaf(s[2 * x + 1], c2, -m_use));
           pw[x] = pack_bf16x2(p0, p1);
           // normalise by the weights the PV product actually uses (bf16-rounded)
           rsum[x & 3] += __uint_as_float(pw[x] << 16) + __uint_as_float(pw[x] & 0xffff0000u);
         }
-        // this warp's row sum, carried from its previous page's max to this one's
-        l = (first ? 0.0f : l * fast_exp2(m_mine - m_use)) + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
-        m_mine = m_use;
+        // this warp's row sum over its columns, carried to the new max
+        l = (first ? 0.0f : l * fast_exp2(m_prev - m_use)) + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+        m = m_use;
         const bool resc_any = __any_sync(0xffffffffu, resc);
-        // ---- P row of this head (64 tokens) and the rescale factor. Tile sb was
-        // last used for page i-2: by this CTA's PV(i-2) and, once the peer's
-        // PV(i-2) is done, no longer by the peer.
-        if (i >= 2 && (!wwait(&sm->pt_free[sb], ((i - 2) >> 1) & 1) ||
-                       !wwait_cl(&sm->rp_free[sb], ((i - 2) >> 1) & 1))) { ok = false; break; }
-        uint8_t* prow = sm->pt[sb] + h * 128;
+        // ---- P of this head (this warp's 32 tokens) and the rescale factor. Tile
+        // sb was last used for page i-2: by this CTA's PV(i-2) and, once the
+        // peer's PV(i-2) is done, no longer by the peer.
+        good = i < 2 || (wwait(&sm->pt_free[sb], ((i - 2) >> 1) & 1) && wwait_cl(&sm->rp_free[sb], ((i - 2) >> 1) & 1));
+        if (good) {
+          uint8_t* prow = sm->pt[sb] + h * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
-              make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-        sm->alpha_out[sb][hl] = alpha;
-        fence_proxy_async_smem();  // generic writes -> the bulk copy's and the MMAs' reads
-        __syncwarp();
-        if (lane == 0) {
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(prow + (((4 * t + c) ^ (h & 7)) << 4)) =
+                make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+          if (t == 0) sm->alpha_out[sb][hl] = alpha;
+          fence_proxy_async_smem();  // generic writes -> the bulk copy's and the MMAs' reads
+        }
+        if (!meet(1, good)) { ok = false; break; }
+        if (t == 0 && lane == 0) {
           // this quarter's 32 P rows (4 KB) and 32 rescale factors, one bulk copy each
           const uint32_t rows = static_cast<uint32_t>(sb * kPTileBytes) + q4 * 32u * 128u;
-          const uint32_t al = static_cast<uint32_t>((sb * 64 + (q4 & 1) * 32) * 4);
+          const uint32_t al = static_cast<uint32_t>((sb * 64 + qo * 32) * 4);
           bulk_copy_to_peer(peer_pt + rows, smem_u32(sm->pt[0]) + rows, 32 * 128, peer_p_in + sb * 8);
           bulk_copy_to_peer(peer_alpha + al, smem_u32(&sm->alpha_out[0][0]) + al, 32 * 4, peer_p_in + sb * 8);
         }
-        // O rows of this CTA's heads may be rescaled only after PV(i-1), which
-        // completes phase (i-1) >> 1 of pt_free[(i-1) & 1]. (PV(i+1) cannot run
-        // before this page's P is complete, so that barrier is at most one phase
-        // behind and its parity wait cannot alias.)
+        // O rows of this CTA's heads (this warp's 128 of the 256 columns) may be
+        // rescaled only after PV(i-1), which completes phase (i-1) >> 1 of
+        // pt_free[(i-1) & 1]. (PV(i+1) cannot run before this page's P is complete,
+        // so that barrier is at most one phase behind and its wait cannot alias.)
         if (resc_any) {
-          if (!wwait(&sm->pt_free[(i - 1) & 1], ((i - 1) >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          rescale_o(alpha, 0, 256);
-        }
-        if (page_valid < kTileTok) {
-          // rows past the sequence end may hold anything (NaN): zero them in this
-          // CTA's V half so that 0 * row stays 0 in the PV product
-          uint4* base = reinterpret_cast<uint4*>(sm->kv[i % kStages]);
-          const int rows = kTileTok - page_valid;
-          for (int e = hl; e < rows * 4 * 8; e += 64) {
-            const int box = e / (rows * 8), rem = e % (rows * 8);
-            base[(box * kBoxBytes + (page_valid + rem / 8) * 128) / 16 + (rem % 8)] = make_uint4(0, 0, 0, 0);
+          if (wwait(&sm->pt_free[(i - 1) & 1], ((i - 1) >> 1) & 1)) {
+            tc_fence_after();
+            rescale_o(alpha, 128 * t, 128);
+          } else {
+            ok = false;  // carried to the next meeting
           }
-          fence_proxy_async_smem();
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm->p_full[sb]));
+        if (ok) {
+          if (page_valid < kTileTok) {
+            // rows past the sequence end may hold anything (NaN): zero them in this
+            // CTA's V half so that 0 * row stays 0 in the PV product
+            uint4* base = reinterpret_cast<uint4*>(sm->kv[i % kStages]);
+            const int rows = kTileTok - page_valid;
+            for (int e = qo * 64 + t * 32 + lane; e < rows * 4 * 8; e += 128) {
+              const int box = e / (rows * 8), rem = e % (rows * 8);
+              base[(box * kBoxBytes + (page_valid + rem / 8) * 128) / 16 + (rem % 8)] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm->p_full[sb]));
+        }
       }
-      sm->mlast[t][hl] = m_mine;
+      sm->mlast[t][hl] = m;
     } else {
       // ================= forwarding: warp t == 0 sends each page's partial scores
       // of the peer's heads (all 64 columns) to its inbox, as soon as they are
@@ -804,8 +813,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm->sum_bar));
       if (ok && !wwait(&sm->sum_bar, 0)) ok = false;
-      // both warps' sums brought to the final max (that of the last page)
-      m = sm->mh[(n_tiles - 1) & 1][hl];
+      // both warps' sums (over their token halves) at the final max m
       l_row = 0.0f;
       for (int x = 0; x < 2; ++x)
         if (sm->mlast[x][hl] != -CUDART_INF_F) l_row += sm->lsum[x][hl] * fast_exp2(sm->mlast[x][hl] - m);

@@ -183,6 +183,23 @@ __device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v, 
                : "memory");
 }
 
+// Named-barrier sync of kThreads threads (a multiple of 32) on barrier kId that
+// also returns the AND of their predicates: every participant learns whether
+// all of them succeeded, so they can leave a loop together.
+template <int kId, int kThreads>
+__device__ __forceinline__ bool bar_red_and(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "barrier.cta.red.and.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "n"(kId), "n"(kThreads)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 __device__ __forceinline__ void cluster_sync() {
