@@ -166,6 +166,28 @@ def test_decode_and_step_small(name):
     _check_o(w, d, f64(o), full, pool, sc, hs, tol)
 
 
+@pytest.mark.parametrize("cache", ["bf16", "e4m3"])
+@pytest.mark.parametrize("page_size,splits", [(128, 0), (128, 2), (256, 3)])
+def test_pages_larger_than_a_tile(cache, page_size, splits):
+    """Pages of 128 and 256 tokens: the tensor-core kernel walks them in 64-token
+    tiles that start inside a page (row offset 64, 128, 192), including the
+    E4M3 converter's per-row scales and ragged last pages."""
+    W = _W()
+    name = "dsv3_bf16" if cache == "bf16" else "fp8_lq2"
+    w = W.preset(name, batch=3, seq_lens=[1000, 129, 300], page_size=page_size, num_splits=splits)
+    d = W.make_inputs(w)
+    layer = _layer(w, d)
+    _step(layer, d)
+    assert layer.device_error() == 0
+    pool, sc = oracle_pool(w, d)
+    ref = _oracle_latent(w, d, layer.q_lat, pool, sc)
+    u = f64(layer.u)
+    lse = layer.lse.cpu().numpy()
+    for b, (ru, rl) in ref.items():
+        assert_close(u[b], ru, what=f"u seq {b}")
+        assert np.max(np.abs(lse[b] - rl)) <= 1e-3 * max(1.0, np.max(np.abs(rl))), f"lse seq {b}"
+
+
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
 def test_split_count_invariance(splits):
     w = _W().preset("ragged_bf16", batch=4, seq_lens=[3000, 17, 640, 2049], num_splits=splits)
