@@ -75,7 +75,6 @@ constexpr int kBoxBytes = kTileTok * 128;   // 64 rows x 64 bf16, 128-byte swizz
 constexpr int kHalfBytes = 4 * kBoxBytes;   // one page, one latent half
 constexpr int kQBoxBytes = 128 * 128;       // 128 heads x 64 bf16
 constexpr int kPTileBytes = 128 * 128;      // P: 128 heads x 64 tokens bf16
-constexpr int kSinStride = 68;              // floats per row of a score inbox (padded: 272 B)
 constexpr uint32_t kSinBytes = 64 * 64 * 4; // payload of one score inbox
 constexpr uint32_t kPinBytes = 64 * 128 + 64 * 4;  // peer's P rows + rescale factors
 constexpr uint32_t kTmemCols = 512;
@@ -90,7 +89,10 @@ struct __align__(1024) Smem {
   uint8_t rope[kBoxBytes];          // RoPE box of this CTA's next RoPE page (i = r mod 2)
   uint8_t qr[kQBoxBytes];           // Q RoPE part (A of the RoPE MMAs)
   uint8_t pt[2][kPTileBytes];       // P tile per page parity (A of the PV MMAs)
-  float sin[2][64][kSinStride];     // peer's partial scores for this CTA's heads
+  // the peer's partial scores for this CTA's 64 heads, chunk-major: 16-byte chunk v
+  // (tokens 4v .. 4v+3) of head hl at sin[buffer][v][hl], so that a warp-wide
+  // store or load of one chunk of 32 heads covers 512 contiguous bytes
+  float4 sin[2][16][64];
   float alpha_in[2][64];            // peer's rescale factors for the peer's heads
   float alpha_out[2][64];           // this CTA's rescale factors, bulk-copied to the peer
   float mx_part[2][2][64];          // page i's row max over the token half t of each own head, in [i & 1][t]
@@ -599,7 +601,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       if (lane == 0) mbar_arrive(smem_u32(&sm->q_ready));  // also frees slots 1-2
     }
     // cluster addresses of the peer's inboxes
-    const uint32_t peer_sin = map_to_rank(smem_u32(&sm->sin[0][0][0]), peer);
+    const uint32_t peer_sin = map_to_rank(smem_u32(&sm->sin[0][0][0]), peer);  // chunk-major inbox
     const uint32_t peer_s_in = map_to_rank(smem_u32(&sm->s_in[0]), peer);
     const uint32_t peer_rs_free = map_to_rank(smem_u32(&sm->rs_free[0]), peer);
     const uint32_t peer_pt = map_to_rank(smem_u32(sm->pt[0]), peer);
@@ -655,10 +657,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
         good = good && wwait_cl(&sm->s_in[sb], ph2);
         if (good) {
           if (armer && i + 2 < n_tiles) mbar_arrive_expect_tx(smem_u32(&sm->s_in[sb]), kSinBytes);
-          const float4* src = reinterpret_cast<const float4*>(&sm->sin[sb][hl][32 * t]);
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
-            const float4 x = src[v];
+            const float4 x = sm->sin[sb][8 * t + v][hl];
             s[4 * v] += x.x;
             s[4 * v + 1] += x.y;
             s[4 * v + 2] += x.z;
@@ -770,11 +771,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
           if (i >= 2 && !wwait_cl(&sm->rs_free[sb], ((i - 2) >> 1) & 1)) { ok = false; break; }
-          const uint32_t dst = peer_sin + ((sb * 64 + hl) * kSinStride) * 4;
+          const uint32_t dst = peer_sin + static_cast<uint32_t>((sb * 16 * 64 + hl) * 16);
           const uint32_t sbar = peer_s_in + sb * 8;
 #pragma unroll
           for (int v = 0; v < 16; ++v)
-            st_async_v4(dst + v * 16, sv[4 * v], sv[4 * v + 1], sv[4 * v + 2], sv[4 * v + 3], sbar);
+            st_async_v4(dst + v * (64 * 16), sv[4 * v], sv[4 * v + 1], sv[4 * v + 2], sv[4 * v + 3], sbar);
         }
       } else {
         const bool armer = (lane == 0) && ((q4 & 1) == 0);
