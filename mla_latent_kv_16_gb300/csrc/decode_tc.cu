@@ -94,7 +94,6 @@ struct __align__(1024) Smem {
   // store or load of one chunk of 32 heads covers 512 contiguous bytes
   float4 sin[2][16][64];
   float alpha_in[2][64];            // peer's rescale factors for the peer's heads
-  float alpha_out[2][64];           // this CTA's rescale factors, bulk-copied to the peer
   float mx_part[2][2][64];          // page i's row max over the token half t of each own head, in [i & 1][t]
   float lsum[2][64];                // each softmax warp's row sum, for the epilogue
   float mlast[2][64];               // the max each softmax warp's row sum refers to
@@ -634,11 +633,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       // bulk copy to the peer). A failed (timed-out) wait is carried to the next
       // meeting, so both warps leave the loop together.
       const int qo = static_cast<int>(q4 & 1);
-      // named barriers 1, 2 (row max) and 3, 4 (P written) for own quarters 0, 1
-      auto meet = [&](int which, bool v) -> bool {
-        if (which == 0) return qo == 0 ? bar_red_and<1, 64>(v) : bar_red_and<2, 64>(v);
-        return qo == 0 ? bar_red_and<3, 64>(v) : bar_red_and<4, 64>(v);
-      };
+      // named barriers 1, 2 (row max) for own quarters 0, 1
+      auto meet = [&](int, bool v) -> bool { return qo == 0 ? bar_red_and<1, 64>(v) : bar_red_and<2, 64>(v); };
       const bool armer = (lane == 0) && (qo == 0) && (t == 0);
       for (int i = 0; i < n_tiles; ++i) {
         const int sb = i & 1;
@@ -708,22 +704,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
         // sb was last used for page i-2: by this CTA's PV(i-2) and, once the
         // peer's PV(i-2) is done, no longer by the peer.
         good = i < 2 || (wwait(&sm->pt_free[sb], ((i - 2) >> 1) & 1) && wwait_cl(&sm->rp_free[sb], ((i - 2) >> 1) & 1));
+        if (!good) ok = false;  // carried to the next meeting
         if (good) {
+          // P into this CTA's tile (128-byte swizzled rows, the PV operand) and into
+          // the peer's: there the same 4 KB of this quarter's rows take the chunks
+          // chunk-major ([16-byte chunk][32 rows]), so that each warp-wide st.async
+          // writes 512 contiguous bytes; the peer's P-path warp swizzles them in place.
           uint8_t* prow = sm->pt[sb] + h * 128;
+          const uint32_t remote = peer_pt + static_cast<uint32_t>(sb * kPTileBytes) + q4 * 32u * 128u + lane * 16u;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(prow + (((4 * t + c) ^ (h & 7)) << 4)) =
+          for (int c = 0; c < 4; ++c) {
+            const int ch = 4 * t + c;
+            *reinterpret_cast<uint4*>(prow + ((ch ^ (h & 7)) << 4)) =
                 make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-          if (t == 0) sm->alpha_out[sb][hl] = alpha;
-          fence_proxy_async_smem();  // generic writes -> the bulk copy's and the MMAs' reads
-        }
-        if (!meet(1, good)) { ok = false; break; }
-        if (t == 0 && lane == 0) {
-          // this quarter's 32 P rows (4 KB) and 32 rescale factors, one bulk copy each
-          const uint32_t rows = static_cast<uint32_t>(sb * kPTileBytes) + q4 * 32u * 128u;
-          const uint32_t al = static_cast<uint32_t>((sb * 64 + qo * 32) * 4);
-          bulk_copy_to_peer(peer_pt + rows, smem_u32(sm->pt[0]) + rows, 32 * 128, peer_p_in + sb * 8);
-          bulk_copy_to_peer(peer_alpha + al, smem_u32(&sm->alpha_out[0][0]) + al, 32 * 4, peer_p_in + sb * 8);
+            st_async_v4(remote + static_cast<uint32_t>(ch * 32 * 16), __uint_as_float(pw[4 * c]),
+                        __uint_as_float(pw[4 * c + 1]), __uint_as_float(pw[4 * c + 2]), __uint_as_float(pw[4 * c + 3]),
+                        peer_p_in + sb * 8);
+          }
+          if (t == 0)
+            st_async_b32(peer_alpha + static_cast<uint32_t>((sb * 64 + qo * 32 + lane) * 4), __float_as_uint(alpha),
+                         peer_p_in + sb * 8);
+          fence_proxy_async_smem();  // generic writes -> the MMAs' reads
         }
         // O rows of this CTA's heads (this warp's 128 of the 256 columns) may be
         // rescaled only after PV(i-1), which completes phase (i-1) >> 1 of
@@ -783,6 +784,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           const int sb = i & 1;
           if (!wwait_cl(&sm->p_in[sb], (i >> 1) & 1)) { ok = false; break; }
           if (armer && i + 2 < n_tiles) mbar_arrive_expect_tx(smem_u32(&sm->p_in[sb]), kPinBytes);
+          {
+            // the peer sent this quarter's P rows chunk-major; into the MMA's layout in place
+            uint8_t* qbase = sm->pt[sb] + q4 * 32u * 128u;
+            uint4 x[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) x[c] = *reinterpret_cast<const uint4*>(qbase + (c * 32 + lane) * 16);
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qbase + lane * 128 + ((c ^ (h & 7)) << 4)) = x[c];
+            fence_proxy_async_smem();  // generic writes -> the MMAs' reads
+          }
           const float alpha = sm->alpha_in[sb][hl];
           // PV(i-1) done (P tile (i-1) & 1 free): needed before a rescale of these
           // O rows, and to let the peer refill that tile. pt_free advances once per
