@@ -34,13 +34,17 @@
 // Warps: 0 = TMA producer; 1 = TMEM allocation and MMA issue (PV of a page as
 // soon as its P is complete, else the next page's QK as soon as its score
 // buffer has been read and its data landed); 2-9 = two warps per TMEM lane
-// quarter. On the quarters of this CTA's heads the two run the softmax of
-// alternate pages (the running max passes between them through shared
-// memory); on the other quarters one forwards the peer's partial scores as
-// soon as they are written (so that the score buffer is released early) and
-// the other receives the peer's P rows and applies its rescale factors to those
-// O rows. In the epilogue each warp normalises one half of the O columns of
-// its quarter.
+// quarter. On the quarters of this CTA's heads both run the softmax of every
+// page, warp t over the tokens [32t, 32t+32); on the other quarters one
+// forwards the peer's partial scores as soon as they are written (so that the
+// score buffer is released early) and the other receives the peer's P rows and
+// applies its rescale factors to those O rows. In the epilogue each warp
+// normalises one half of the O columns of its quarter.
+//
+// Distributed shared memory carries the partial scores and P. Both land
+// chunk-major ([16-byte chunk][head]) so that every warp-wide st.async writes
+// 512 contiguous bytes; scattered 16-byte pieces cost twice their size on the
+// link and several times the time.
 //
 // E4M3 cache ("Multi-Head Latent Attention (MLA): ..." "High-Throughput Serving
 // Kernels": FP8 latent cache with per-block scales): the TMA brings each page
