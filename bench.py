@@ -52,6 +52,25 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value: the job's time is that of its slowest
+    rank. Identity on one rank; otherwise an all-reduce over the process group
+    (NCCL on the GPU machine, gloo in the CPU tests)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: float, ms_per_step: float) -> float:
+    """Whole-job throughput: the units every rank processed per second of the
+    slowest rank's step (independent replicas, fixed work per rank)."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -253,11 +272,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    tot = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([tot], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot = float(t.item())
+    tot = max_over_ranks(sum(step_ms), world, "cuda")
     for _ in range(args.warmup):
         flush.sum()
         g_dec.replay()
@@ -282,16 +297,12 @@ def run_ours(args):
         flush.sum()
         g_e2e.replay()
     e2e_ms = timed(g_e2e, args.steps)
-    e2e_tot = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_tot], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_tot = float(t.item())
+    e2e_tot = max_over_ranks(sum(e2e_ms), world, "cuda")
 
     cache_bytes = sum(int(L) for L in w.seq_lens) * w.row_bytes()
     ms = tot / args.steps
-    gbs = world * cache_bytes / (ms * 1e-3) / 1e9
-    tok_s = world * w.batch * w.q_len / (ms * 1e-3)
+    gbs = job_rate(world, cache_bytes, ms) / 1e9
+    tok_s = job_rate(world, w.batch * w.q_len, ms)
     e2e_msps = e2e_tot / args.steps
     dec = statistics.mean(dec_ms)
     peaks, src = measured_peaks()
@@ -316,7 +327,7 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "mla_decode_paged (decode + combine), algorithmic bytes = cache rows + q + u + lse",
                      "peak_source": f"hbm_gbs of {src}"},
-        "e2e": {"value": round(world * cache_bytes / (e2e_msps * 1e-3) / 1e9, 2), "unit": UNIT,
+        "e2e": {"value": round(job_rate(world, cache_bytes, e2e_msps) / 1e9, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_msps, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
