@@ -15,7 +15,10 @@ Recipe (every workload):
   * pages: sequence b owns ceil(L_b / page_size) pages; the physical page ids
     are a seeded permutation of the pool; unused block-table entries are -1;
   * the optional outlier fraction multiplies the c_KV and k_R rows of a seeded
-    subset of tokens by 4.0 (a power of two, exact in every dtype used here).
+    subset of tokens by 4.0 (a power of two, exact in every dtype used here);
+  * the output projection W_O [d_model, H, 128] (d_model = 7168 for the
+    DeepSeek-V3 shape) ~ N(0,1) * (1/sqrt(H*128)), from a generator of its own
+    so that drawing it leaves every other input unchanged.
 
 The named presets are the five decode workloads the method is measured on:
 a tiny fp32 case, the DeepSeek-V3-shaped bf16 decode, a ragged bf16 batch, a
@@ -34,6 +37,7 @@ D_ROPE = 64
 D_C = 512
 D_V = 128
 ROW = D_C + D_ROPE  # 576 values per cached token
+D_MODEL = 7168      # hidden size of the DeepSeek-V3 shape
 
 # dtype names shared with the C ABI (mla_dtype_t)
 F32, BF16, E4M3 = "f32", "bf16", "e4m3"
@@ -194,6 +198,14 @@ def make_inputs(w: Workload, with_context: bool = True):
         new = [starts[b] + int(w.seq_lens[b]) - Lq + torch.arange(Lq) for b in range(B)]
         d["new_index"] = torch.cat(new)
     return d
+
+
+def make_out_weight(w: Workload, d_model: int = D_MODEL) -> torch.Tensor:
+    """W_O [d_model, H, 128] (act dtype), the output projection over the
+    concatenated head outputs, seeded independently of make_inputs."""
+    g = torch.Generator().manual_seed(w.seed * 1000003 + 29)
+    std = 1.0 / math.sqrt(w.heads * D_V)
+    return (torch.randn(d_model, w.heads, D_V, generator=g) * std).to(TORCH_DTYPE[w.act_dtype])
 
 
 def sample_sequences(w: Workload, k: int, seed: int = 12345):

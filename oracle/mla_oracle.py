@@ -34,6 +34,8 @@ Readings taken where the pages are silent (each one is also a test):
     (1.0 when amax is 0); byte = E4M3FN(fl32(x/scale)) rounded to nearest even,
     saturating to +-448; value = decode(byte) * scale.
   * lse is the natural-log log-sum-exp of the scaled scores.
+  * W_O in R^{d x (H d_v)} is stored [d][H][d_v] (the view(d_model, n_heads,
+    d_head) of [P2]); the fused weight W~ is [d][H][d_c].
 """
 from __future__ import annotations
 
@@ -408,3 +410,32 @@ def decode_full(q_nope, q_rope, w_uk, w_uv, pool, scales, block_table, seq_lens,
             ls.append(lse)
         out[b] = (np.stack(os_), np.stack(us), np.stack(ls))
     return out
+
+
+# ---------------------------------------------------------------------------
+# Output projection with W_UV folded in (the weights are fused at load time)
+# ---------------------------------------------------------------------------
+
+def fuse_out_weights(w_o: np.ndarray, w_uv: np.ndarray) -> np.ndarray:
+    """Pre-fused output weight, per head the d x d_v column block of W_O times
+    W_UV[h] (d_v x d_c): W~[m, h, c] = sum_e W_O[m, h, e] W_UV[h, e, c].
+    [P1] §3.2 (W~^O_i = W^O_i W^UV_i in R^{d x d_c}, fused before decoding);
+    [P2] "Value Output Matrix Absorption" (W_O^i W_UV,i is static and computed
+    once). w_o [d, H, d_v] is W_O in R^{d x (H d_v)} viewed per head."""
+    return np.einsum("mhe,hec->mhc", np.asarray(w_o, np.float64), np.asarray(w_uv, np.float64))
+
+
+def out_proj_fused(u: np.ndarray, w_fused: np.ndarray) -> np.ndarray:
+    """y[..., m] = sum_h sum_c W~[m, h, c] u[..., h, c]: the attention block's
+    output in the model dimension straight from the latent outputs u.
+    [P1] §3.2 (the 512-dimensional latent sum times the pre-fused matrix);
+    [P2] "Value Output Matrix Absorption" (final projection from latent space)."""
+    return np.einsum("...hc,mhc->...m", np.asarray(u, np.float64), np.asarray(w_fused, np.float64))
+
+
+def out_proj_model(o: np.ndarray, w_o: np.ndarray) -> np.ndarray:
+    """y[..., m] = sum_h sum_e W_O[m, h, e] o[..., h, e]: the unfused output
+    projection over the concatenated head outputs o [..., H, d_v].
+    [P2] "Value Output Matrix Absorption" (W_O = [W_O^1, ..., W_O^nh] in
+    R^{d x (nh d_v)})."""
+    return np.einsum("...he,mhe->...m", np.asarray(o, np.float64), np.asarray(w_o, np.float64))
