@@ -31,6 +31,10 @@ if ROOT not in sys.path:
 METRIC = "MLA decode latent-cache GB/s & tokens/s at 1 GB300; % of HBM roofline"
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "dsv3_bf16"
+# The output projection with W_UV folded into W_O (y = W~ u, d_model 7168, the
+# DeepSeek-V3-shaped decode batch of 32): its own line, on request only.
+FUSED_WORKLOAD = "dsv3_fused_out"
+FUSED_METRIC = "MLA fused output projection (W~ = W_O W_UV) weight-stream GB/s at 1 GB300; % of HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20  # read (not written) before every timed step
 
@@ -90,10 +94,16 @@ def decode_bytes(w) -> int:
     return rows * w.row_bytes() + q + out
 
 
-def recorded_traffic(kernel_src: str, workload: str):
+def fused_bytes(n_tokens: int, d_model: int, heads: int) -> int:
+    """Algorithmic bytes of one mla_out_proj_fused call (bf16): W~ once, u, y."""
+    K = heads * 512
+    return 2 * (d_model * K + n_tokens * K + n_tokens * d_model)
+
+
+def recorded_traffic(kernel_src: str, workload: str, prefix: str = "decode"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current source of the kernel; else None."""
-    prof = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    prof = os.path.join(ROOT, "profiles", f"{prefix}_{workload}.md")
     try:
         txt = open(prof).read()
         src = open(kernel_src, "rb").read()
@@ -204,7 +214,163 @@ def cpu_oracle_run(w, d, seconds: float):
     return done_bytes / elapsed / 1e9, sample, threads, elapsed
 
 
+def fused_setup(w, d_model: int):
+    """The fused projection's inputs from the seeded generators: W_O, W_UV, u."""
+    import torch
+    from mla_latent_kv_16_gb300 import workloads as W
+    w_o = W.make_out_weight(w, d_model)
+    w_uv = W.make_inputs(w, with_context=False)["w_uv"]
+    g = torch.Generator().manual_seed(w.seed * 7 + 100)
+    u = torch.randn(w.batch, w.q_len, w.heads, 512, generator=g).to(torch.bfloat16)
+    return w_o, w_uv, u
+
+
+def cpu_fused_run(w, d_model: int, seconds: float):
+    """Time the oracle's fused projection on a bounded sample: blocks of 64 rows
+    of W~ (folded by the oracle and rounded to bf16 as set-up, not timed) against
+    the whole batch, until `seconds` of oracle work are done. Returns (GB/s of
+    W~ bytes processed, sample description, threads, seconds)."""
+    import numpy as np
+    from oracle import mla_oracle as O
+    from oracle.harness import f64
+
+    threads = os.cpu_count()
+    w_o, w_uv, u = fused_setup(w, d_model)
+    wo64, wuv64, u64 = f64(w_o), f64(w_uv), f64(u)
+    K = w.heads * 512
+    elapsed, rows = 0.0, 0
+    for r0 in range(0, d_model, 64):
+        wf = O.round_bf16(O.fuse_out_weights(wo64[r0:r0 + 64], wuv64))
+        t0 = time.perf_counter()
+        O.out_proj_fused(u64, wf)
+        elapsed += time.perf_counter() - t0
+        rows += wf.shape[0]
+        if elapsed > seconds:
+            break
+    sample = f"{rows} of {d_model} rows of W~ against all {w.batch * w.q_len} tokens; fp64 oracle product"
+    return rows * K * 2 / elapsed / 1e9, sample, threads, elapsed
+
+
 # ----------------------------------------------------------------------------- GPU arm
+
+def run_fused(args):
+    """One mla_out_proj_fused call per step (W~ already folded and resident)."""
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from mla_latent_kv_16_gb300 import build as B
+    if rank == 0 or world == 1:
+        B.build()
+    if world > 1:
+        dist.barrier()
+    from mla_latent_kv_16_gb300 import capi, workloads as W
+    capi.load()
+    w = W.preset(DEFAULT_WORKLOAD)
+    d_model, H, n = W.D_MODEL, w.heads, w.batch * w.q_len
+    w_o, w_uv, u_h = fused_setup(w, d_model)
+    w_f = capi.mla_fuse_out_weights(w_o.cuda(), w_uv.cuda())
+    del w_o, w_uv
+    u = u_h.cuda()
+    y = torch.empty(w.batch, w.q_len, d_model, dtype=torch.bfloat16, device="cuda")
+    need = capi.mla_out_proj_fused_workspace_size(n, d_model, H)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+    splits = max(1, need // (n * d_model * 4)) if need else 1
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def capture(fn):
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                fn()
+        stream.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    g_call = capture(lambda: capi.mla_out_proj_fused(u, w_f, y, ws))
+
+    def timed(graph, k, clk=None):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        if clk is not None:
+            clk.start()
+            time.sleep(0.3)
+        for i in range(k):
+            flush.sum()
+            evs[i][0].record(stream)
+            graph.replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    for _ in range(args.warmup):
+        flush.sum()
+        g_call.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = ClockSampler(local)
+    call_ms = timed(g_call, args.steps, clk)
+    clocks = clk.stop()
+    tot = max_over_ranks(sum(call_ms), world, "cuda")
+
+    host_u = u_h.pin_memory()
+    host_y = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+
+    def e2e():
+        u.copy_(host_u, non_blocking=True)
+        capi.mla_out_proj_fused(u, w_f, y, ws)
+        host_y.copy_(y, non_blocking=True)
+
+    g_e2e = capture(e2e)
+    for _ in range(args.warmup):
+        flush.sum()
+        g_e2e.replay()
+    e2e_tot = max_over_ranks(sum(timed(g_e2e, args.steps)), world, "cuda")
+
+    nbytes = fused_bytes(n, d_model, H)
+    ms = tot / args.steps
+    gbs = job_rate(world, nbytes, ms) / 1e9
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = nbytes / (statistics.mean(call_ms) * 1e-3) / 1e9
+    traffic = recorded_traffic(os.path.join(ROOT, "mla_latent_kv_16_gb300", "csrc", "out_fused.cu"),
+                               FUSED_WORKLOAD, prefix="out_fused")
+    out = {
+        "metric": FUSED_METRIC, "value": round(gbs, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded W_O ~ N(0,1/sqrt(16384)), W_UV ~ N(0,1/sqrt(512)), u ~ N(0,1))",
+        "config": {"workload": FUSED_WORKLOAD, "tokens": n, "heads": H, "d_model": d_model, "k_splits": splits,
+                   "l2": "flushed before every timed call by reading a 256 MiB buffer; W~ (940 MB) > L2",
+                   "parallelism": f"dp{world} (independent replicas, no collective)"},
+        "tokens_per_s": round(job_rate(world, n, ms), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "mla_out_proj_fused (tcgen05 GEMM + split sum), algorithmic bytes = W~ + u + y",
+                     "peak_source": f"hbm_gbs of {src}"},
+        "e2e": {"value": round(job_rate(world, nbytes, e2e_tot / args.steps) / 1e9, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_tot / args.steps, 5), "h2d_bytes_per_step": host_u.numel() * 2,
+                "d2h_bytes_per_step": host_y.numel() * 2},
+        "gpu_launches": (2 if splits > 1 else 1) * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample, thr, el = cpu_fused_run(w, d_model, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": thr, "kind": "oracle",
+                               "sample": sample, "seconds": round(el, 2)}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
 
 def run_ours(args):
     import torch
@@ -342,10 +508,34 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_reference_fused(args):
+    from mla_latent_kv_16_gb300 import workloads as W
+    w = W.preset(DEFAULT_WORKLOAD)
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_fused_run(w, W.D_MODEL, min(budget, 2.0))
+    vals, secs, sample, thr = [], 0.0, "", 1
+    for _ in range(args.steps):
+        v, sample, thr, el = cpu_fused_run(w, W.D_MODEL, budget)
+        vals.append(v)
+        secs += el
+    value = statistics.mean(vals)
+    out = {"impl": "reference", "metric": FUSED_METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded)", "config": {"workload": FUSED_WORKLOAD, "tokens": w.batch * w.q_len,
+                                                     "heads": w.heads, "d_model": W.D_MODEL},
+           "cpu_baseline": {"kind": "oracle", "cores": thr, "sample": sample, "value": round(value, 4), "unit": UNIT},
+           "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
+    if args.workload == FUSED_WORKLOAD:
+        return run_reference_fused(args)
     from mla_latent_kv_16_gb300 import workloads as W
     w = W.preset(args.workload)
     d = W.make_inputs(w)
@@ -374,6 +564,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == FUSED_WORKLOAD:
+        run_fused(args)
     else:
         run_ours(args)
 

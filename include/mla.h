@@ -10,6 +10,11 @@
  *                       u[t,h,:] = sum_j p_j c_KV[j]  (split-KV + log-sum-exp combine)
  *   mla_out_proj      : o[t,h,:]     = W_UV[h] u[t,h,:]                 (512 -> 128)
  *
+ * or, with W_UV folded into the output projection W_O once at load time
+ * (mla_fuse_out_weights), in place of mla_out_proj:
+ *
+ *   mla_out_proj_fused: y[t,:] = sum_h W~[:,h,:] u[t,h,:]     (H*512 -> d_model)
+ *
  * Sources (page titles):
  *   [P1] "Model Architecture Driving Inference Systems: From MHA/GQA to DeepSeek
  *        MLA Matrix Absorption and Memory Minimalism" (dev.to)
@@ -242,6 +247,55 @@ mla_status_t mla_decode_paged_static_scratch(const void *q_lat, const void *q_ro
  */
 mla_status_t mla_out_proj(const void *u, const void *w_uv, void *o, int32_t n_tokens,
                           mla_dims_t dims, mla_dtype_t act, mla_stream_t stream);
+
+/*
+ * mla_fuse_out_weights -- fold the value up-projection into the output
+ * projection, once, when the weights are loaded:
+ *   W~[m][h][c] = sum_e W_O[m][h][e] W_UV[h][e][c]
+ * [P1] §3.2 (pre-fused W~^O_i = W^O_i W^UV_i in R^{d x d_c}) and §4.2 (the
+ * fusion is done at model load time); [P2] "Value Output Matrix Absorption"
+ * (W_O^i W_UV,i is a static matrix computed at initialisation).
+ *
+ *   w_o     [d_model][H][128] act: W_O in R^{d_model x (H*128)}, row-major,
+ *           whose column block h (128 columns) belongs to head h
+ *   w_uv    [H][128][512] act
+ *   w_fused [d_model][H][512] act, written
+ *   d_model : 1 .. 65536
+ * Each output is a 128-term dot product accumulated in fp32 and rounded once
+ * to act. Not part of the per-step path.
+ */
+mla_status_t mla_fuse_out_weights(const void *w_o, const void *w_uv, void *w_fused, int32_t d_model,
+                                  mla_dims_t dims, mla_dtype_t act, mla_stream_t stream);
+
+/*
+ * Bytes of workspace mla_out_proj_fused needs for these arguments on the
+ * current device: the fp32 partial sums of a K split, [splits][n_tokens][d_model],
+ * 256-byte aligned; 0 when K is not split.
+ */
+size_t mla_out_proj_fused_workspace_size(int32_t n_tokens, int32_t d_model, mla_dims_t dims,
+                                         mla_dtype_t act);
+
+/*
+ * mla_out_proj_fused -- the attention block's output in the model dimension
+ * straight from the latent outputs, through the fused weight:
+ *   y[t][m] = sum_h sum_c W~[m][h][c] u[t][h][c]
+ * [P1] §3.2 (the 512-dimensional latent sum multiplied by the pre-fused
+ * matrix); [P2] "Value Output Matrix Absorption" (the final projection goes
+ * from latent space directly to the hidden dimension).
+ *
+ *   u         [n_tokens][H][512] act (the u_out of mla_decode_paged)
+ *   w_fused   [d_model][H][512] act (from mla_fuse_out_weights)
+ *   y         [n_tokens][d_model] act, written
+ *   workspace : workspace_bytes >= mla_out_proj_fused_workspace_size(...)
+ *               (may be NULL when that is 0); nothing in it has to start at zero
+ * fp32 accumulation. When K = 512 H is split across CTAs, the fp32 partial
+ * sums are added in split order by a second kernel, so results do not depend
+ * on timing. bf16 with d_model % 128 == 0 runs on the tensor cores; other
+ * shapes and fp32 on CUDA cores.
+ */
+mla_status_t mla_out_proj_fused(const void *u, const void *w_fused, void *y, int32_t n_tokens,
+                                int32_t d_model, void *workspace, size_t workspace_bytes,
+                                mla_dims_t dims, mla_dtype_t act, mla_stream_t stream);
 
 /*
  * mla_read_device_error -- synchronise `stream`, copy *dev_error (device) to

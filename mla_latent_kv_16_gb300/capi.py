@@ -28,7 +28,8 @@ MLA_STATIC_SCRATCH_BYTES = 32 << 20  # size of the library's fixed split-KV scra
 
 EXPORTED = ("mla_status_string", "mla_version", "mla_rope_table", "mla_cache_append", "mla_absorb_q",
             "mla_decode_num_splits", "mla_decode_workspace_size", "mla_decode_paged", "mla_out_proj",
-            "mla_read_device_error", "mla_decode_paged_static_scratch")
+            "mla_read_device_error", "mla_decode_paged_static_scratch", "mla_fuse_out_weights",
+            "mla_out_proj_fused_workspace_size", "mla_out_proj_fused")
 
 
 class MlaDims(ctypes.Structure):
@@ -86,6 +87,12 @@ def load(path: Optional[str] = None):
     L.mla_decode_paged_static_scratch.restype = ctypes.c_int
     L.mla_decode_paged_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, f32, i32, vp,
                                                   vp, vp, MlaDims, ctypes.c_int, ctypes.c_int, vp]
+    L.mla_fuse_out_weights.restype = ctypes.c_int
+    L.mla_fuse_out_weights.argtypes = [vp, vp, vp, i32, MlaDims, ctypes.c_int, vp]
+    L.mla_out_proj_fused_workspace_size.restype = sz
+    L.mla_out_proj_fused_workspace_size.argtypes = [i32, i32, MlaDims, ctypes.c_int]
+    L.mla_out_proj_fused.restype = ctypes.c_int
+    L.mla_out_proj_fused.argtypes = [vp, vp, vp, i32, i32, vp, sz, MlaDims, ctypes.c_int, vp]
     L.mla_read_device_error.restype = ctypes.c_int
     L.mla_read_device_error.argtypes = [vp, vp, vp]
     _LIB = L
@@ -182,6 +189,39 @@ def mla_out_proj(u, w_uv, o=None, stream=None):
     _check("mla_out_proj", load().mla_out_proj(_ptr(u), _ptr(w_uv), _ptr(o), n, dims(H), _act_code(u),
                                                 _stream(stream)))
     return o
+
+
+def mla_fuse_out_weights(w_o, w_uv, w_fused=None, stream=None):
+    """w_o [d_model, H, 128], w_uv [H, 128, 512] -> W~ [d_model, H, 512] (load time)."""
+    _contig_cuda(w_o, w_uv, w_fused)
+    d_model, H = w_o.shape[0], w_uv.shape[0]
+    if w_fused is None:
+        w_fused = torch.empty(d_model, H, 512, dtype=w_o.dtype, device=w_o.device)
+    _check("mla_fuse_out_weights", load().mla_fuse_out_weights(_ptr(w_o), _ptr(w_uv), _ptr(w_fused), d_model,
+                                                                dims(H), _act_code(w_o), _stream(stream)))
+    return w_fused
+
+
+def mla_out_proj_fused_workspace_size(n_tokens: int, d_model: int, num_heads: int, act: str = "bf16") -> int:
+    return load().mla_out_proj_fused_workspace_size(n_tokens, d_model, dims(num_heads), DTYPE_CODE[act])
+
+
+def mla_out_proj_fused(u, w_fused, y=None, workspace=None, stream=None):
+    """u [..., H, 512], W~ [d_model, H, 512] -> y [..., d_model]."""
+    _contig_cuda(u, w_fused, y, workspace)
+    d_model, H = w_fused.shape[0], w_fused.shape[1]
+    n = u.numel() // (H * 512)
+    if y is None:
+        y = torch.empty(*u.shape[:-2], d_model, dtype=u.dtype, device=u.device)
+    act = "f32" if u.dtype == torch.float32 else "bf16"
+    need = mla_out_proj_fused_workspace_size(n, d_model, H, act) if n > 0 else 0
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=u.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("mla_out_proj_fused", load().mla_out_proj_fused(_ptr(u), _ptr(w_fused), _ptr(y), n, d_model,
+                                                            _ptr(workspace), ws_bytes, dims(H), _act_code(u),
+                                                            _stream(stream)))
+    return y
 
 
 def mla_decode_paged(q_lat, q_rope, cache, scales, block_table, seq_lens, page_size: int, cache_dtype: str,

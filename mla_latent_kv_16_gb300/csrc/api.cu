@@ -26,6 +26,7 @@ namespace {
 
 constexpr int32_t kMaxTokens = 1 << 20;
 constexpr int32_t kMaxBatchQ = 65535;
+constexpr int32_t kMaxDModel = 1 << 16;
 
 bool dims_ok(const mla_dims_t& d) {
   return d.d_nope == 128 && d.d_c == 512 && d.d_rope == 64 && d.d_v == 128 && d.num_heads >= 1 &&
@@ -165,6 +166,40 @@ mla_status_t mla_out_proj(const void* u, const void* w_uv, void* o, int32_t n_to
     if (e != cudaErrorNotSupported) return from_cuda(e);
   }
   return from_cuda(launch_out_proj_simt(a, s));
+}
+
+mla_status_t mla_fuse_out_weights(const void* w_o, const void* w_uv, void* w_fused, int32_t d_model,
+                                  mla_dims_t dims, mla_dtype_t act, mla_stream_t stream) {
+  if (!dims_ok(dims) || d_model < 1 || d_model > kMaxDModel) return MLA_ERR_INVALID_ARG;
+  if (act != MLA_F32 && act != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (w_o == nullptr || w_uv == nullptr || w_fused == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(w_o) || !aligned16(w_uv) || !aligned16(w_fused)) return MLA_ERR_INVALID_ARG;
+  FuseWeightsArgs a{w_o, w_uv, w_fused, d_model, dims.num_heads, act};
+  return from_cuda(launch_fuse_weights(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t mla_out_proj_fused_workspace_size(int32_t n_tokens, int32_t d_model, mla_dims_t dims, mla_dtype_t act) {
+  if (!dims_ok(dims) || n_tokens < 1 || n_tokens > kMaxTokens || d_model < 1 || d_model > kMaxDModel) return 0;
+  if (act != MLA_F32 && act != MLA_BF16) return 0;
+  return out_fused_workspace_bytes(n_tokens, d_model, dims.num_heads, act);
+}
+
+mla_status_t mla_out_proj_fused(const void* u, const void* w_fused, void* y, int32_t n_tokens, int32_t d_model,
+                                void* workspace, size_t workspace_bytes, mla_dims_t dims, mla_dtype_t act,
+                                mla_stream_t stream) {
+  if (!dims_ok(dims) || n_tokens < 0 || n_tokens > kMaxTokens || d_model < 1 || d_model > kMaxDModel)
+    return MLA_ERR_INVALID_ARG;
+  if (act != MLA_F32 && act != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return MLA_OK;
+  if (u == nullptr || w_fused == nullptr || y == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(w_fused) || !aligned16(y)) return MLA_ERR_INVALID_ARG;
+  const int32_t splits = out_fused_splits(n_tokens, d_model, dims.num_heads, act);
+  const size_t need = out_fused_workspace_bytes(n_tokens, d_model, dims.num_heads, act);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+  FusedOutArgs a{u, w_fused, y, need > 0 ? static_cast<float*>(workspace) : nullptr, n_tokens, d_model,
+                 dims.num_heads, splits, act};
+  return from_cuda(launch_out_fused(a, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t mla_decode_num_splits(int32_t batch, int32_t q_len, int32_t max_pages_per_seq, int32_t page_size,

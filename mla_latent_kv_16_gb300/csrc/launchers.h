@@ -66,6 +66,33 @@ cudaError_t launch_out_proj_simt(const ProjArgs& a, cudaStream_t s);
 cudaError_t launch_absorb_tc(const ProjArgs& a, cudaStream_t s);
 cudaError_t launch_out_proj_tc(const ProjArgs& a, cudaStream_t s);
 
+struct FuseWeightsArgs {
+  const void* w_o;   // [d][H][128]
+  const void* w_uv;  // [H][128][512]
+  void* w_fused;     // [d][H][512]
+  int32_t d_model;
+  int32_t heads;
+  mla_dtype_t act;
+};
+cudaError_t launch_fuse_weights(const FuseWeightsArgs& a, cudaStream_t s);
+
+struct FusedOutArgs {
+  const void* u;     // [n][H][512]
+  const void* w;     // W~ [d][H][512]
+  void* y;           // [n][d]
+  float* part;       // [k_splits][n][d] fp32 partial sums (k_splits > 1)
+  int32_t n_tokens;
+  int32_t d_model;
+  int32_t heads;
+  int32_t k_splits;  // from out_fused_splits
+  mla_dtype_t act;
+};
+// K splits of the fused output projection for these sizes on the current
+// device (1 on the CUDA-core path), and the workspace bytes they need.
+int32_t out_fused_splits(int32_t n_tokens, int32_t d_model, int32_t heads, mla_dtype_t act);
+size_t out_fused_workspace_bytes(int32_t n_tokens, int32_t d_model, int32_t heads, mla_dtype_t act);
+cudaError_t launch_out_fused(const FusedOutArgs& a, cudaStream_t s);
+
 struct DecodeArgs {
   const void* q_lat;
   const void* q_rope;

@@ -1,0 +1,429 @@
+// The attention block's output projection with W_UV folded into W_O
+// ("Model Architecture Driving Inference Systems" §3.2, pre-fused
+// W~^O_i = W^O_i W^UV_i, and §4.2, fused when the model is loaded;
+// "Multi-Head Latent Attention (MLA)" page, "Value Output Matrix Absorption"):
+//
+//   fuse_weights : W~[m][h][c] = sum_e W_O[m][h][e] W_UV[h][e][c]   (once, CUDA cores)
+//   out_fused    : y[t][m]     = sum_k W~[m][k] u[t][k],  k = (h, c), K = 512 H
+//
+// out_fused is a GEMM with K = 65,536 at 128 heads and only the decode batch
+// as N, so W~ (d_model x K bf16: 940 MB at d_model = 7168) is streamed from HBM
+// once and nothing else matters. The tcgen05 kernel takes 128 rows of W~ as
+// the MMA M dimension and up to 256 tokens as N, and splits K across CTAs so
+// that every SM streams: each CTA runs a TMA ring of 64-wide K chunks (a 128 x
+// 64 box of W~ and an n x 64 box of u, both 128-byte swizzled) into one TMEM
+// accumulator. The fp32 partial sums of the splits go to the workspace and a
+// second kernel adds them in split order, so the result does not depend on
+// timing.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "launchers.h"
+#include "tc_ptx.cuh"
+
+namespace mla {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 128;
+constexpr int kMaxTok = 256;       // tokens per CTA (MMA N)
+constexpr int kChunkK = 64;        // K elements per TMA box (128 bytes of bf16)
+constexpr int kABytes = 128 * 128;  // one W~ box: 128 rows x 64 bf16
+constexpr int kMaxStages = 6;
+constexpr int kMaxSplits = 32;
+
+struct FusedCtl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t done;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+// ------------------------------------------------------------------ fold (load time)
+
+// grid (512/64, ceil(d/64), H), block 256: a 64 (m) x 64 (c) tile of W~ for
+// head h, each thread 4 x 4 outputs, the 128-long e dimension in 4 steps of 32.
+template <typename T>
+__global__ void __launch_bounds__(256) fuse_weights_kernel(FuseWeightsArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float as[32][65];  // [e][m]: W_O[m0 + m][h][e0 + e]
+  __shared__ float bs[32][64];  // [e][c]: W_UV[h][e0 + e][c0 + c]
+  const int c0 = blockIdx.x * 64, m0 = blockIdx.y * 64, h = blockIdx.z;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const T* w_o = static_cast<const T*>(a.w_o);
+  const T* w_uv = static_cast<const T*>(a.w_uv);
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  for (int e0 = 0; e0 < kDV; e0 += 32) {
+    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+      const int m = i >> 5, e = i & 31;
+      const int mm = m0 + m;
+      as[e][m] = mm < a.d_model ? ActIO<T>::load(w_o + (static_cast<int64_t>(mm) * a.heads + h) * kDV + e0 + e)
+                                : 0.0f;
+    }
+    for (int i = threadIdx.x; i < 32 * 64; i += 256) {
+      const int e = i >> 6, c = i & 63;
+      bs[e][c] = ActIO<T>::load(w_uv + (static_cast<int64_t>(h) * kDV + e0 + e) * kDC + c0 + c);
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int e = 0; e < 32; ++e) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = as[e][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = bs[e][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  T* out = static_cast<T*>(a.w_fused);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int mm = m0 + ty * 4 + i;
+    if (mm >= a.d_model) continue;
+    T* row = out + (static_cast<int64_t>(mm) * a.heads + h) * kDC + c0 + tx * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ActIO<T>::store(row + j, acc[i][j]);
+  }
+}
+
+// ------------------------------------------------------------------ y = u W~^T, CUDA cores
+
+// grid (ceil(n/8), ceil(d/8)), block 256: warp = one row m of W~ against 8
+// tokens; lanes stride K. Any dtype and d_model.
+template <typename T>
+__global__ void __launch_bounds__(256) out_fused_simt_kernel(FusedOutArgs p) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = blockIdx.y * 8 + warp;
+  const int t0 = blockIdx.x * 8;
+  if (m >= p.d_model) return;
+  const int64_t K = static_cast<int64_t>(p.heads) * kDC;
+  const int nt = min(8, p.n_tokens - t0);
+  const T* w = static_cast<const T*>(p.w) + static_cast<int64_t>(m) * K;
+  const T* u = static_cast<const T*>(p.u) + static_cast<int64_t>(t0) * K;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  for (int64_t k = lane; k < K; k += 32) {
+    const float wv = ActIO<T>::load(w + k);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < nt) acc[j] = fmaf(wv, ActIO<T>::load(u + j * K + k), acc[j]);
+  }
+  T* y = static_cast<T*>(p.y);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float s = warp_sum(acc[j]);
+    if (lane == 0 && j < nt) ActIO<T>::store(y + static_cast<int64_t>(t0 + j) * p.d_model + m, s);
+  }
+}
+
+// ------------------------------------------------------------------ y = u W~^T, tcgen05
+
+// grid (d/128, splits, ceil(n/256)), block 128. Thread 0 issues the TMA loads
+// and the MMAs; all four warps read the accumulator back (thread = row m).
+__global__ void __launch_bounds__(kThreads) out_fused_tc_kernel(const __grid_constant__ CUtensorMap amap,
+                                                                const __grid_constant__ CUtensorMap bmap,
+                                                                FusedOutArgs p, int n_tile, int stages,
+                                                                uint32_t tmem_cols) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int b_bytes = n_tile * 128;
+  const int stage_bytes = kABytes + ((b_bytes + 1023) & ~1023);
+  FusedCtl* ctl = reinterpret_cast<FusedCtl*>(base + stages * stage_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * 128;
+  const int split = blockIdx.y;
+  const int t0 = blockIdx.z * kMaxTok;
+  const int n_tok = min(kMaxTok, p.n_tokens - t0);
+  const int chunks = p.heads * (kDC / kChunkK);
+  const int c_lo = static_cast<int>(static_cast<int64_t>(split) * chunks / p.k_splits);
+  const int c_hi = static_cast<int>(static_cast<int64_t>(split + 1) * chunks / p.k_splits);
+  const int nc = c_hi - c_lo;  // >= 1: the host never splits finer than the chunk count
+  pdl_trigger();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    mbar_init(smem_u32(&ctl->done), 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init_cluster();
+    prefetch_tmap(&amap);
+    prefetch_tmap(&bmap);
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&ctl->tmem_base), tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int32_t* abort_flag = &ctl->abort_flag;
+  // W~ may have been written by the kernel just before this one (the fold), so
+  // nothing is loaded before the wait for the previous kernels.
+  pdl_wait();
+
+  if (threadIdx.x == 0) {
+    // W~ is read once when all tokens fit one tile (then u stays in L2 instead)
+    const bool once = p.n_tokens <= kMaxTok;
+    const uint64_t pol = l2_policy_evict_first();
+    auto load = [&](int k, int s) {
+      const uint32_t dst = smem_u32(base + s * stage_bytes);
+      const uint32_t bar = smem_u32(&ctl->full[s]);
+      const int32_t x = (c_lo + k) * kChunkK;
+      mbar_arrive_expect_tx(bar, kABytes + b_bytes);
+      if (once)
+        tma_load_2d(dst, &amap, bar, x, m0, pol);
+      else
+        tma_load_2d_nohint(dst, &amap, bar, x, m0);
+      tma_load_2d_nohint(dst + kABytes, &bmap, bar, x, t0);  // token rows past n read as zero
+    };
+    const int pre = min(stages, nc);
+    for (int k = 0; k < pre; ++k) load(k, k);
+    int issued = pre, consumed = 0;
+    const uint32_t idesc = idesc_bf16_f32(128, n_tile, false, false);
+    bool ok = true;
+    for (int k = 0; k < nc; ++k) {
+      const int s = k % stages;
+      if (!mbar_wait<2>(smem_u32(&ctl->full[s]), (k / stages) & 1, abort_flag, nullptr)) {
+        ok = false;
+        break;
+      }
+      consumed = k + 1;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(base + s * stage_bytes);
+      const uint64_t db = sdesc_sw128(a0 + kABytes, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kChunkK / 16; ++kk)
+        mma_ss(tmem, sdesc_sw128(a0 + kk * 32, 16, 1024), db + ((kk * 32) >> 4), idesc,
+               (k > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(smem_u32(&ctl->empty[s]));
+      // refill the slot of the previous chunk, whose MMAs have had a chunk's
+      // time to finish, while this chunk's run
+      const int kp = k - 1;
+      if (kp >= 0 && kp + stages < nc) {
+        const int sp = kp % stages;
+        if (!mbar_wait<2>(smem_u32(&ctl->empty[sp]), (kp / stages) & 1, abort_flag, nullptr)) {
+          ok = false;
+          break;
+        }
+        load(kp + stages, sp);
+        issued = kp + stages + 1;
+      }
+    }
+    mma_commit(smem_u32(&ctl->done));
+    if (!ok) {
+      // every copy issued and not yet consumed lands before the CTA exits (one
+      // per slot at most, each one phase ahead of the slot's last wait)
+      volatile int32_t never = 0;
+      for (int k = consumed; k < issued; ++k)
+        mbar_wait<2>(smem_u32(&ctl->full[k % stages]), (k / stages) & 1, &never, nullptr);
+    }
+  }
+  __syncwarp();
+
+  // epilogue: thread = row m0 + 32 warp + lane (TMEM lane), columns = tokens
+  volatile int32_t never = 0;
+  const bool done_ok = __all_sync(0xffffffffu, mbar_wait<0>(smem_u32(&ctl->done), 0, &never, nullptr));
+  tc_fence_after();
+  const bool good = done_ok && *abort_flag == 0;
+  const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+  const int64_t col = m0 + warp * 32 + lane;
+  for (int c = 0; c < n_tile; c += 32) {
+    float v[32];
+    if (done_ok) {
+      tmem_ld32_sync(tmem + lanes + c, v);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int t = c + k;
+      if (t >= n_tok) break;
+      const float val = good ? v[k] : CUDART_NAN_F;  // an aborted tile reads as NaN, never as stale data
+      const int64_t row = t0 + t;
+      if (p.k_splits == 1)
+        static_cast<__nv_bfloat16*>(p.y)[row * p.d_model + col] = __float2bfloat16_rn(val);
+      else
+        p.part[(static_cast<int64_t>(split) * p.n_tokens + row) * p.d_model + col] = val;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+// y = sum over splits s = 0, 1, ... of part[s], four consecutive outputs per thread.
+template <typename T>
+__global__ void __launch_bounds__(256) out_fused_reduce_kernel(FusedOutArgs p) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t n4 = static_cast<int64_t>(p.n_tokens) * p.d_model / 4;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (i >= n4) return;
+  const float4* src = reinterpret_cast<const float4*>(p.part) + i;
+  float4 acc = src[0];
+  for (int s = 1; s < p.k_splits; ++s) {
+    const float4 v = src[s * n4];
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  T* y = static_cast<T*>(p.y) + 4 * i;
+  ActIO<T>::store(y, acc.x);
+  ActIO<T>::store(y + 1, acc.y);
+  ActIO<T>::store(y + 2, acc.z);
+  ActIO<T>::store(y + 3, acc.w);
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2D map over a [rows][cols] bf16 matrix, boxes of 64 columns x box_rows.
+bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool use_tc(int32_t d_model, mla_dtype_t act) { return act == MLA_BF16 && d_model % 128 == 0; }
+
+struct FusedPlan {
+  int n_tile;       // MMA N (tokens per CTA, multiple of 16)
+  int tok_tiles;    // CTAs along the tokens
+  int stages;       // TMA ring depth
+  int splits;       // CTAs along K
+  size_t smem;      // dynamic shared memory per CTA
+  uint32_t tmem_cols;
+};
+
+// Tile shape and K split for the tcgen05 kernel. Two CTAs share an SM when
+// their rings are small (decode batches), so that an SM keeps up to eight
+// chunks in flight. Co-resident CTAs share the SM's bandwidth, so the split
+// count minimises the chunks the busiest SM streams: CTAs per SM (rounded up)
+// x (chunks per CTA + about one chunk's worth of partial-sum traffic).
+FusedPlan plan_tc(int32_t n_tokens, int32_t d_model, int32_t heads) {
+  FusedPlan p{};
+  p.n_tile = n_tokens >= kMaxTok ? kMaxTok : ((n_tokens + 15) / 16) * 16;
+  p.tok_tiles = (n_tokens + kMaxTok - 1) / kMaxTok;
+  const int stage = kABytes + ((p.n_tile * 128 + 1023) & ~1023);
+  if (stage <= 24 * 1024) {
+    p.stages = 4;  // about 83 KB: two CTAs per SM
+  } else {
+    p.stages = (200 * 1024) / stage;
+    if (p.stages > 4) p.stages = 4;
+    if (p.stages < 2) p.stages = 2;
+  }
+  p.smem = 1024 + static_cast<size_t>(p.stages) * stage + sizeof(FusedCtl);
+  p.tmem_cols = 32;
+  while (static_cast<int>(p.tmem_cols) < p.n_tile) p.tmem_cols <<= 1;
+  const int chunks = heads * (kDC / kChunkK);
+  const int64_t tiles = static_cast<int64_t>(d_model / 128) * p.tok_tiles;
+  const int64_t sms = device_sm_count();
+  double best = 1e300;
+  p.splits = 1;
+  for (int s = 1; s <= kMaxSplits && s <= chunks; ++s) {
+    const int per = (chunks + s - 1) / s;
+    if (s > 1 && per < 8) break;
+    const int64_t per_sm_ctas = (tiles * s + sms - 1) / sms;
+    const double cost = static_cast<double>(per_sm_ctas) * (per + (s > 1 ? 1.0 : 0.0));
+    if (cost < best - 1e-9) {
+      best = cost;
+      p.splits = s;
+    }
+  }
+  return p;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+int32_t out_fused_splits(int32_t n_tokens, int32_t d_model, int32_t heads, mla_dtype_t act) {
+  if (n_tokens < 1 || d_model < 1 || heads < 1 || !use_tc(d_model, act)) return 1;
+  return plan_tc(n_tokens, d_model, heads).splits;
+}
+
+size_t out_fused_workspace_bytes(int32_t n_tokens, int32_t d_model, int32_t heads, mla_dtype_t act) {
+  const int32_t s = out_fused_splits(n_tokens, d_model, heads, act);
+  if (s <= 1) return 0;
+  return align256(static_cast<size_t>(s) * n_tokens * d_model * sizeof(float));
+}
+
+cudaError_t launch_fuse_weights(const FuseWeightsArgs& a, cudaStream_t s) {
+  const dim3 grid(kDC / 64, (a.d_model + 63) / 64, a.heads);
+  if (a.act == MLA_F32) return launch_pdl(fuse_weights_kernel<float>, grid, dim3(256), 0, s, a);
+  return launch_pdl(fuse_weights_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, a);
+}
+
+cudaError_t launch_out_fused(const FusedOutArgs& a, cudaStream_t s) {
+  if (a.n_tokens == 0) return cudaSuccess;
+  if (!use_tc(a.d_model, a.act)) {
+    const dim3 grid((a.n_tokens + 7) / 8, (a.d_model + 7) / 8);
+    if (a.act == MLA_F32) return launch_pdl(out_fused_simt_kernel<float>, grid, dim3(256), 0, s, a);
+    return launch_pdl(out_fused_simt_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, a);
+  }
+  if (encoder() == nullptr) return cudaErrorNotSupported;
+  const FusedPlan pl = plan_tc(a.n_tokens, a.d_model, a.heads);
+  if (pl.splits != a.k_splits || (pl.splits > 1 && a.part == nullptr)) return cudaErrorInvalidValue;
+  CUtensorMap am, bm;
+  const uint64_t K = static_cast<uint64_t>(a.heads) * kDC;
+  if (!encode_2d(&am, a.w, static_cast<uint64_t>(a.d_model), K, 128) ||
+      !encode_2d(&bm, a.u, static_cast<uint64_t>(a.n_tokens), K, static_cast<uint32_t>(pl.n_tile)))
+    return cudaErrorInvalidValue;
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (attr_dev != dev) {
+    e = cudaFuncSetAttribute(out_fused_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_dev = dev;
+  }
+  const dim3 grid(a.d_model / 128, pl.splits, pl.tok_tiles);
+  e = launch_pdl(out_fused_tc_kernel, grid, dim3(kThreads), pl.smem, s, am, bm, a, pl.n_tile, pl.stages,
+                 pl.tmem_cols);
+  if (e != cudaSuccess || pl.splits == 1) return e;
+  const int64_t n4 = static_cast<int64_t>(a.n_tokens) * a.d_model / 4;
+  return launch_pdl(out_fused_reduce_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>((n4 + 255) / 256)),
+                    dim3(256), 0, s, a);
+}
+
+}  // namespace mla

@@ -422,20 +422,30 @@ def fuse_out_weights(w_o: np.ndarray, w_uv: np.ndarray) -> np.ndarray:
     [P1] §3.2 (W~^O_i = W^O_i W^UV_i in R^{d x d_c}, fused before decoding);
     [P2] "Value Output Matrix Absorption" (W_O^i W_UV,i is static and computed
     once). w_o [d, H, d_v] is W_O in R^{d x (H d_v)} viewed per head."""
-    return np.einsum("mhe,hec->mhc", np.asarray(w_o, np.float64), np.asarray(w_uv, np.float64))
+    w_o = np.asarray(w_o, np.float64)
+    w_uv = np.asarray(w_uv, np.float64)
+    out = np.empty((w_o.shape[0], w_uv.shape[0], w_uv.shape[2]))
+    for h in range(w_uv.shape[0]):
+        out[:, h, :] = w_o[:, h, :] @ w_uv[h]
+    return out
 
 
 def out_proj_fused(u: np.ndarray, w_fused: np.ndarray) -> np.ndarray:
     """y[..., m] = sum_h sum_c W~[m, h, c] u[..., h, c]: the attention block's
-    output in the model dimension straight from the latent outputs u.
+    output in the model dimension straight from the latent outputs u, as one
+    product with the heads' latent vectors concatenated.
     [P1] §3.2 (the 512-dimensional latent sum times the pre-fused matrix);
     [P2] "Value Output Matrix Absorption" (final projection from latent space)."""
-    return np.einsum("...hc,mhc->...m", np.asarray(u, np.float64), np.asarray(w_fused, np.float64))
+    u = np.asarray(u, np.float64)
+    w = np.asarray(w_fused, np.float64)
+    return u.reshape(*u.shape[:-2], -1) @ w.reshape(w.shape[0], -1).T
 
 
 def out_proj_model(o: np.ndarray, w_o: np.ndarray) -> np.ndarray:
     """y[..., m] = sum_h sum_e W_O[m, h, e] o[..., h, e]: the unfused output
-    projection over the concatenated head outputs o [..., H, d_v].
+    projection, W_O times the concatenated head outputs o [..., H, d_v].
     [P2] "Value Output Matrix Absorption" (W_O = [W_O^1, ..., W_O^nh] in
     R^{d x (nh d_v)})."""
-    return np.einsum("...he,mhe->...m", np.asarray(o, np.float64), np.asarray(w_o, np.float64))
+    o = np.asarray(o, np.float64)
+    w = np.asarray(w_o, np.float64)
+    return o.reshape(*o.shape[:-2], -1) @ w.reshape(w.shape[0], -1).T

@@ -89,3 +89,24 @@ def test_validation_fails_before_device_work(capi):
                               None) == capi.MLA_ERR_INVALID_ARG
     assert L.mla_decode_paged(16, 16, 16, None, 16, 16, 1, 1, 1, 1, 64, float("nan"), 0, None, 0, 16, None, None,
                               capi.dims(128), capi.MLA_BF16, capi.MLA_BF16, None) == capi.MLA_ERR_INVALID_ARG
+
+
+def test_fused_projection_validation(capi):
+    """mla_fuse_out_weights / mla_out_proj_fused reject bad arguments before any
+    device work; the workspace size covers one fp32 partial per K split."""
+    L = capi.load()
+    D = capi.dims(128)
+    assert L.mla_fuse_out_weights(16, 16, 16, 0, D, capi.MLA_BF16, None) == capi.MLA_ERR_INVALID_ARG
+    assert L.mla_fuse_out_weights(16, 16, 16, 7168, D, capi.MLA_E4M3, None) == capi.MLA_ERR_UNSUPPORTED
+    assert L.mla_fuse_out_weights(None, 16, 16, 7168, D, capi.MLA_BF16, None) == capi.MLA_ERR_INVALID_ARG
+    assert L.mla_fuse_out_weights(16, 16, 24, 7168, D, capi.MLA_BF16, None) == capi.MLA_ERR_INVALID_ARG
+    assert L.mla_out_proj_fused(None, None, None, 0, 7168, None, 0, D, capi.MLA_BF16, None) == capi.MLA_OK
+    assert L.mla_out_proj_fused(16, 16, 16, 4, 1 << 17, None, 0, D, capi.MLA_BF16, None) == \
+        capi.MLA_ERR_INVALID_ARG
+    need = capi.mla_out_proj_fused_workspace_size(32, 7168, 128)
+    assert need > 0 and need % 256 == 0 and need % (32 * 7168 * 4) == 0
+    assert L.mla_out_proj_fused(16, 16, 16, 32, 7168, None, 0, D, capi.MLA_BF16, None) == \
+        capi.MLA_ERR_WORKSPACE_TOO_SMALL
+    # the CUDA-core shapes never split K
+    assert capi.mla_out_proj_fused_workspace_size(32, 7000, 128) == 0
+    assert capi.mla_out_proj_fused_workspace_size(32, 7168, 128, "f32") == 0
