@@ -1,8 +1,8 @@
 """Parity of the fused output projection (W~ = W_O W_UV folded per head, then
 y = W~ u over all heads) through the C ABI against the fp64 CPU oracle.
 
-The fold is held to one bf16 ulp of the exact product (it rounds once, after an
-fp32 sum of 128 exact products). The GEMM gets the oracle's own W~ (rounded to
+The fold is held to one bf16 ulp of the exact product plus the fp32 summation
+bound of its 128 exact products (it rounds once, after the fp32 sum). The GEMM gets the oracle's own W~ (rounded to
 the activation type) as input, never the GPU's. Tolerances for y: rel-L2 <=
 5e-3 and max-abs <= 2e-2 (bf16), fp32-level for fp32.
 """
@@ -59,6 +59,15 @@ def _ulp_bf16(x):
     return 2.0 ** (np.floor(np.log2(a)) - 7)
 
 
+def _fold_bound(w_o64, w_uv64, exact):
+    """Error bound of a bf16 fold: one ulp of the result (the final rounding, with
+    room for the fp32 sum pushing it across a rounding boundary) plus the fp32
+    summation bound 128 * 2^-24 * sum_e |W_O W_UV|, which dominates where the 128
+    products cancel."""
+    mag = O.fuse_out_weights(np.abs(w_o64), np.abs(w_uv64))
+    return _ulp_bf16(exact) + 128 * 2.0 ** -24 * mag
+
+
 @pytest.mark.parametrize("act,H,d_model", [("bf16", 4, 200), ("bf16", 2, 128), ("f32", 3, 70)])
 def test_fuse_weights(act, H, d_model):
     w_o, w_uv = _weights(H, d_model, act, seed=11)
@@ -68,7 +77,7 @@ def test_fuse_weights(act, H, d_model):
     assert got.shape == exact.shape
     if act == "bf16":
         # at most one ulp from the exact value, and the oracle's own rounding almost everywhere
-        assert np.all(np.abs(got - exact) <= _ulp_bf16(exact)), "fold more than 1 ulp off"
+        assert np.all(np.abs(got - exact) <= _fold_bound(f64(w_o), f64(w_uv), exact)), "fold off by more than its bound"
         assert np.mean(got != O.round_bf16(exact)) <= 1e-3
     else:
         assert np.max(np.abs(got - exact)) <= 1e-5 * np.max(np.abs(exact))
@@ -143,7 +152,7 @@ def test_out_proj_fused_full_size():
     rows = torch.randperm(d_model, generator=torch.Generator().manual_seed(15))[:48].tolist()
     got = f64(gf[rows])
     exact = O.fuse_out_weights(wo64[rows], wuv64)
-    assert np.all(np.abs(got - exact) <= _ulp_bf16(exact))
+    assert np.all(np.abs(got - exact) <= _fold_bound(wo64[rows], wuv64, exact))
 
 
 def test_decode_then_fused_projection_matches_materialised_attention():
