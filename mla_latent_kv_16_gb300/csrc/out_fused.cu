@@ -9,11 +9,14 @@
 // out_fused is a GEMM with K = 65,536 at 128 heads and only the decode batch
 // as N, so W~ (d_model x K bf16: 940 MB at d_model = 7168) is streamed from HBM
 // once and nothing else matters. The tcgen05 kernel takes 128 rows of W~ as
-// the MMA M dimension and up to 256 tokens as N, and splits K across CTAs so
-// that every SM streams: each CTA runs a TMA ring of 64-wide K chunks (a 128 x
-// 64 box of W~ and an n x 64 box of u, both 128-byte swizzled) into one TMEM
-// accumulator. The fp32 partial sums of the splits go to the workspace and a
-// second kernel adds them in split order, so the result does not depend on
+// the MMA M dimension and up to 256 tokens as N, and splits K so that there
+// are enough work units (row tile x K split x token tile) for every SM. It is
+// persistent, one CTA per SM: a producer warp streams all of the CTA's units
+// through one TMA ring of 64-wide K chunks (a 128 x 64 box of W~ and an n x 64
+// box of u, both 128-byte swizzled) without a break between units, an MMA warp
+// accumulates each unit in one of two TMEM buffers, and four epilogue warps
+// empty the other. The fp32 partial sums of the splits go to the workspace and
+// a second kernel adds them in split order, so the result does not depend on
 // timing.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -28,17 +31,20 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 128;
-constexpr int kMaxTok = 256;       // tokens per CTA (MMA N)
+constexpr int kThreads = 192;      // producer warp, MMA warp, four epilogue warps
+constexpr int kMaxTok = 256;       // tokens per unit (MMA N)
 constexpr int kChunkK = 64;        // K elements per TMA box (128 bytes of bf16)
 constexpr int kABytes = 128 * 128;  // one W~ box: 128 rows x 64 bf16
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 12;
 constexpr int kMaxSplits = 32;
+constexpr int kRingBudget = 200 * 1024;  // shared memory for the TMA ring
 
 struct FusedCtl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t done;
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -134,26 +140,39 @@ __global__ void __launch_bounds__(256) out_fused_simt_kernel(FusedOutArgs p) {
 
 // ------------------------------------------------------------------ y = u W~^T, tcgen05
 
-// grid (d/128, splits, ceil(n/256)), block 128. Thread 0 issues the TMA loads
-// and the MMAs; all four warps read the accumulator back (thread = row m).
-__global__ void __launch_bounds__(kThreads) out_fused_tc_kernel(const __grid_constant__ CUtensorMap amap,
-                                                                const __grid_constant__ CUtensorMap bmap,
-                                                                FusedOutArgs p, int n_tile, int stages,
-                                                                uint32_t tmem_cols) {
+// A work unit is (128 rows of W~, K split, token tile). The unit's coordinates.
+struct Unit {
+  int m0, split, t0, c_lo, nc;
+};
+
+__device__ __forceinline__ Unit unit_at(const FusedOutArgs& p, int u, int m_tiles, int chunks) {
+  Unit r;
+  const int rest = u / m_tiles;
+  r.m0 = (u - rest * m_tiles) * 128;
+  r.split = rest % p.k_splits;
+  r.t0 = (rest / p.k_splits) * kMaxTok;
+  r.c_lo = static_cast<int>(static_cast<int64_t>(r.split) * chunks / p.k_splits);
+  r.nc = static_cast<int>(static_cast<int64_t>(r.split + 1) * chunks / p.k_splits) - r.c_lo;
+  return r;
+}
+
+// Persistent: grid = min(units, SMs), one CTA per SM, CTA c takes units c, c + G,
+// c + 2G, ... Warp 0 (one lane) streams every chunk of those units through the
+// TMA ring without a break between units; warp 1 (one lane) issues the MMAs
+// into one of two TMEM accumulators; warps 2-5 read back the other (warp w owns
+// TMEM lanes 32 (w % 4) .. +32, thread = row of W~) and write the unit's output.
+__global__ void __launch_bounds__(kThreads, 1) out_fused_tc_kernel(const __grid_constant__ CUtensorMap amap,
+                                                                   const __grid_constant__ CUtensorMap bmap,
+                                                                   FusedOutArgs p, int n_tile, int stages,
+                                                                   uint32_t acc_cols, int units) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int b_bytes = n_tile * 128;
   const int stage_bytes = kABytes + ((b_bytes + 1023) & ~1023);
   FusedCtl* ctl = reinterpret_cast<FusedCtl*>(base + stages * stage_bytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * 128;
-  const int split = blockIdx.y;
-  const int t0 = blockIdx.z * kMaxTok;
-  const int n_tok = min(kMaxTok, p.n_tokens - t0);
+  const int m_tiles = p.d_model / 128;
   const int chunks = p.heads * (kDC / kChunkK);
-  const int c_lo = static_cast<int>(static_cast<int64_t>(split) * chunks / p.k_splits);
-  const int c_hi = static_cast<int>(static_cast<int64_t>(split + 1) * chunks / p.k_splits);
-  const int nc = c_hi - c_lo;  // >= 1: the host never splits finer than the chunk count
   pdl_trigger();
 
   if (threadIdx.x == 0) {
@@ -161,13 +180,17 @@ __global__ void __launch_bounds__(kThreads) out_fused_tc_kernel(const __grid_con
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
-    mbar_init(smem_u32(&ctl->done), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl->acc_full[b]), 1);
+      mbar_init(smem_u32(&ctl->acc_empty[b]), 4);  // the four epilogue warps
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort_flag = 0;
     fence_mbar_init_cluster();
     prefetch_tmap(&amap);
     prefetch_tmap(&bmap);
   }
-  if (warp == 0) tmem_alloc(smem_u32(&ctl->tmem_base), tmem_cols);
+  if (warp == 0) tmem_alloc(smem_u32(&ctl->tmem_base), 2 * acc_cols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -177,97 +200,125 @@ __global__ void __launch_bounds__(kThreads) out_fused_tc_kernel(const __grid_con
   // nothing is loaded before the wait for the previous kernels.
   pdl_wait();
 
-  if (threadIdx.x == 0) {
-    // W~ is read once when all tokens fit one tile (then u stays in L2 instead)
-    const bool once = p.n_tokens <= kMaxTok;
-    const uint64_t pol = l2_policy_evict_first();
-    auto load = [&](int k, int s) {
-      const uint32_t dst = smem_u32(base + s * stage_bytes);
-      const uint32_t bar = smem_u32(&ctl->full[s]);
-      const int32_t x = (c_lo + k) * kChunkK;
-      mbar_arrive_expect_tx(bar, kABytes + b_bytes);
-      if (once)
-        tma_load_2d(dst, &amap, bar, x, m0, pol);
-      else
-        tma_load_2d_nohint(dst, &amap, bar, x, m0);
-      tma_load_2d_nohint(dst + kABytes, &bmap, bar, x, t0);  // token rows past n read as zero
-    };
-    const int pre = min(stages, nc);
-    for (int k = 0; k < pre; ++k) load(k, k);
-    int issued = pre, consumed = 0;
-    const uint32_t idesc = idesc_bf16_f32(128, n_tile, false, false);
-    bool ok = true;
-    for (int k = 0; k < nc; ++k) {
-      const int s = k % stages;
-      if (!mbar_wait<2>(smem_u32(&ctl->full[s]), (k / stages) & 1, abort_flag, nullptr)) {
-        ok = false;
-        break;
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer. W~ is read once when all tokens fit one tile (u then stays in L2).
+      const bool once = p.n_tokens <= kMaxTok;
+      const uint64_t pol = l2_policy_evict_first();
+      uint32_t g = 0;  // chunks issued so far, over all of this CTA's units
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = unit_at(p, u, m_tiles, chunks);
+        for (int k = 0; k < w.nc; ++k, ++g) {
+          const int s = static_cast<int>(g % stages);
+          if (g >= static_cast<uint32_t>(stages) &&
+              !mbar_wait<2>(smem_u32(&ctl->empty[s]), ((g / stages) & 1) ^ 1, abort_flag, nullptr)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = smem_u32(base + s * stage_bytes);
+          const uint32_t bar = smem_u32(&ctl->full[s]);
+          const int32_t x = (w.c_lo + k) * kChunkK;
+          mbar_arrive_expect_tx(bar, kABytes + b_bytes);
+          if (once)
+            tma_load_2d(dst, &amap, bar, x, w.m0, pol);
+          else
+            tma_load_2d_nohint(dst, &amap, bar, x, w.m0);
+          tma_load_2d_nohint(dst + kABytes, &bmap, bar, x, w.t0);  // token rows past n read as zero
+        }
       }
-      consumed = k + 1;
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(base + s * stage_bytes);
-      const uint64_t db = sdesc_sw128(a0 + kABytes, 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < kChunkK / 16; ++kk)
-        mma_ss(tmem, sdesc_sw128(a0 + kk * 32, 16, 1024), db + ((kk * 32) >> 4), idesc,
-               (k > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(smem_u32(&ctl->empty[s]));
-      // refill the slot of the previous chunk, whose MMAs have had a chunk's
-      // time to finish, while this chunk's run
-      const int kp = k - 1;
-      if (kp >= 0 && kp + stages < nc) {
-        const int sp = kp % stages;
-        if (!mbar_wait<2>(smem_u32(&ctl->empty[sp]), (kp / stages) & 1, abort_flag, nullptr)) {
+      if (!ok) {
+        // after an abort nobody consumes: let the last copy issued into each slot land
+        volatile int32_t never = 0;
+        const uint32_t first = g > static_cast<uint32_t>(stages) ? g - stages : 0;
+        for (uint32_t q = first; q < g; ++q)
+          mbar_wait<2>(smem_u32(&ctl->full[q % stages]), (q / stages) & 1, &never, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(128, n_tile, false, false);
+      uint32_t g = 0;
+      bool ok = true;
+      int i = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
+        const Unit w = unit_at(p, u, m_tiles, chunks);
+        const int b = i & 1;
+        if (i >= 2 && !mbar_wait<2>(smem_u32(&ctl->acc_empty[b]), ((i >> 1) - 1) & 1, abort_flag, nullptr)) {
           ok = false;
           break;
         }
-        load(kp + stages, sp);
-        issued = kp + stages + 1;
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(b) * acc_cols;
+        for (int k = 0; k < w.nc; ++k, ++g) {
+          const int s = static_cast<int>(g % stages);
+          if (!mbar_wait<2>(smem_u32(&ctl->full[s]), (g / stages) & 1, abort_flag, nullptr)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(base + s * stage_bytes);
+          const uint64_t db = sdesc_sw128(a0 + kABytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kChunkK / 16; ++kk)
+            mma_ss(d, sdesc_sw128(a0 + kk * 32, 16, 1024), db + ((kk * 32) >> 4), idesc,
+                   (k > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&ctl->empty[s]));
+        }
+        if (ok) mma_commit(smem_u32(&ctl->acc_full[b]));
       }
-    }
-    mma_commit(smem_u32(&ctl->done));
-    if (!ok) {
-      // every copy issued and not yet consumed lands before the CTA exits (one
-      // per slot at most, each one phase ahead of the slot's last wait)
+      // every MMA this thread issued completes before the TMEM is freed
+      mma_commit(smem_u32(&ctl->drain));
       volatile int32_t never = 0;
-      for (int k = consumed; k < issued; ++k)
-        mbar_wait<2>(smem_u32(&ctl->full[k % stages]), (k / stages) & 1, &never, nullptr);
+      mbar_wait<2>(smem_u32(&ctl->drain), 0, &never, nullptr);
+    }
+  } else {
+    // ---- epilogue (warps 2-5)
+    const int q = warp & 3;
+    const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+    bool ok = true;
+    int i = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+      const Unit w = unit_at(p, u, m_tiles, chunks);
+      const int b = i & 1;
+      const bool got =
+          __all_sync(0xffffffffu, ok && mbar_wait<0>(smem_u32(&ctl->acc_full[b]), (i >> 1) & 1, abort_flag, nullptr));
+      ok = got;
+      tc_fence_after();
+      const int n_tok = min(kMaxTok, p.n_tokens - w.t0);
+      const int64_t col = w.m0 + q * 32 + lane;
+      for (int c = 0; c < n_tile; c += 32) {
+        float v[32];
+        if (got) {
+          tmem_ld32_sync(tmem + static_cast<uint32_t>(b) * acc_cols + lanes + c, v);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int t = c + k;
+          if (t >= n_tok) break;
+          const float val = got ? v[k] : CUDART_NAN_F;  // an aborted unit reads as NaN, never as stale data
+          const int64_t row = w.t0 + t;
+          if (p.k_splits == 1)
+            static_cast<__nv_bfloat16*>(p.y)[row * p.d_model + col] = __float2bfloat16_rn(val);
+          else
+            p.part[(static_cast<int64_t>(w.split) * p.n_tokens + row) * p.d_model + col] = val;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (got && lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[b]));
     }
   }
   __syncwarp();
-
-  // epilogue: thread = row m0 + 32 warp + lane (TMEM lane), columns = tokens
-  volatile int32_t never = 0;
-  const bool done_ok = __all_sync(0xffffffffu, mbar_wait<0>(smem_u32(&ctl->done), 0, &never, nullptr));
-  tc_fence_after();
-  const bool good = done_ok && *abort_flag == 0;
-  const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
-  const int64_t col = m0 + warp * 32 + lane;
-  for (int c = 0; c < n_tile; c += 32) {
-    float v[32];
-    if (done_ok) {
-      tmem_ld32_sync(tmem + lanes + c, v);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 32; ++k) v[k] = 0.0f;
-    }
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const int t = c + k;
-      if (t >= n_tok) break;
-      const float val = good ? v[k] : CUDART_NAN_F;  // an aborted tile reads as NaN, never as stale data
-      const int64_t row = t0 + t;
-      if (p.k_splits == 1)
-        static_cast<__nv_bfloat16*>(p.y)[row * p.d_model + col] = __float2bfloat16_rn(val);
-      else
-        p.part[(static_cast<int64_t>(split) * p.n_tokens + row) * p.d_model + col] = val;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, tmem_cols);
+    tmem_dealloc(tmem, 2 * acc_cols);
   }
 }
 
@@ -326,34 +377,30 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, ui
 bool use_tc(int32_t d_model, mla_dtype_t act) { return act == MLA_BF16 && d_model % 128 == 0; }
 
 struct FusedPlan {
-  int n_tile;       // MMA N (tokens per CTA, multiple of 16)
-  int tok_tiles;    // CTAs along the tokens
-  int stages;       // TMA ring depth
-  int splits;       // CTAs along K
-  size_t smem;      // dynamic shared memory per CTA
-  uint32_t tmem_cols;
+  int n_tile;         // MMA N (tokens per unit, multiple of 16)
+  int tok_tiles;      // units along the tokens
+  int stages;         // TMA ring depth
+  int splits;         // units along K
+  int units;          // M tiles x splits x token tiles
+  int grid;           // persistent CTAs: min(units, SMs)
+  size_t smem;        // dynamic shared memory per CTA
+  uint32_t acc_cols;  // TMEM columns of one of the two accumulators
 };
 
-// Tile shape and K split for the tcgen05 kernel. Two CTAs share an SM when
-// their rings are small (decode batches), so that an SM keeps up to eight
-// chunks in flight. Co-resident CTAs share the SM's bandwidth, so the split
-// count minimises the chunks the busiest SM streams: CTAs per SM (rounded up)
-// x (chunks per CTA + about one chunk's worth of partial-sum traffic).
+// Tile shape, ring depth and K split of the persistent tcgen05 kernel. One CTA
+// per SM streams its units back to back, so the split count minimises the
+// chunks the busiest CTA streams: units per CTA (rounded up) x (chunks per unit
+// + about one chunk's worth of partial-sum traffic).
 FusedPlan plan_tc(int32_t n_tokens, int32_t d_model, int32_t heads) {
   FusedPlan p{};
   p.n_tile = n_tokens >= kMaxTok ? kMaxTok : ((n_tokens + 15) / 16) * 16;
   p.tok_tiles = (n_tokens + kMaxTok - 1) / kMaxTok;
   const int stage = kABytes + ((p.n_tile * 128 + 1023) & ~1023);
-  if (stage <= 24 * 1024) {
-    p.stages = 4;  // about 83 KB: two CTAs per SM
-  } else {
-    p.stages = (200 * 1024) / stage;
-    if (p.stages > 4) p.stages = 4;
-    if (p.stages < 2) p.stages = 2;
-  }
+  p.stages = kRingBudget / stage;
+  if (p.stages > kMaxStages) p.stages = kMaxStages;
   p.smem = 1024 + static_cast<size_t>(p.stages) * stage + sizeof(FusedCtl);
-  p.tmem_cols = 32;
-  while (static_cast<int>(p.tmem_cols) < p.n_tile) p.tmem_cols <<= 1;
+  p.acc_cols = 32;
+  while (static_cast<int>(p.acc_cols) < p.n_tile) p.acc_cols <<= 1;
   const int chunks = heads * (kDC / kChunkK);
   const int64_t tiles = static_cast<int64_t>(d_model / 128) * p.tok_tiles;
   const int64_t sms = device_sm_count();
@@ -362,13 +409,16 @@ FusedPlan plan_tc(int32_t n_tokens, int32_t d_model, int32_t heads) {
   for (int s = 1; s <= kMaxSplits && s <= chunks; ++s) {
     const int per = (chunks + s - 1) / s;
     if (s > 1 && per < 8) break;
-    const int64_t per_sm_ctas = (tiles * s + sms - 1) / sms;
-    const double cost = static_cast<double>(per_sm_ctas) * (per + (s > 1 ? 1.0 : 0.0));
+    const int64_t per_cta = (tiles * s + sms - 1) / sms;
+    const double cost = static_cast<double>(per_cta) * (per + (s > 1 ? 1.0 : 0.0));
     if (cost < best - 1e-9) {
       best = cost;
       p.splits = s;
     }
   }
+  const int64_t units = tiles * p.splits;
+  p.units = static_cast<int>(units);
+  p.grid = static_cast<int>(units < sms ? units : sms);
   return p;
 }
 
@@ -413,13 +463,12 @@ cudaError_t launch_out_fused(const FusedOutArgs& a, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (attr_dev != dev) {
-    e = cudaFuncSetAttribute(out_fused_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
+    e = cudaFuncSetAttribute(out_fused_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e != cudaSuccess) return e;
     attr_dev = dev;
   }
-  const dim3 grid(a.d_model / 128, pl.splits, pl.tok_tiles);
-  e = launch_pdl(out_fused_tc_kernel, grid, dim3(kThreads), pl.smem, s, am, bm, a, pl.n_tile, pl.stages,
-                 pl.tmem_cols);
+  e = launch_pdl(out_fused_tc_kernel, dim3(pl.grid), dim3(kThreads), pl.smem, s, am, bm, a, pl.n_tile, pl.stages,
+                 pl.acc_cols, pl.units);
   if (e != cudaSuccess || pl.splits == 1) return e;
   const int64_t n4 = static_cast<int64_t>(a.n_tokens) * a.d_model / 4;
   return launch_pdl(out_fused_reduce_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>((n4 + 255) / 256)),
