@@ -18,7 +18,11 @@ Recipe (every workload):
     subset of tokens by 4.0 (a power of two, exact in every dtype used here);
   * the output projection W_O [d_model, H, 128] (d_model = 7168 for the
     DeepSeek-V3 shape) ~ N(0,1) * (1/sqrt(H*128)), from a generator of its own
-    so that drawing it leaves every other input unchanged.
+    so that drawing it leaves every other input unchanged;
+  * the front end's hidden states h [B*Lq, d_model] ~ N(0,1) and its weights
+    W_DQ [1536, d], W_UQ [H*128, 1536], W_QR [H*64, 1536], W_DKV [512, d],
+    W_KR [64, d] ~ N(0,1) * (1/sqrt(fan_in)), RMSNorm gains 1 + 0.1 N(0,1),
+    also from a generator of its own.
 
 The named presets are the five decode workloads the method is measured on:
 a tiny fp32 case, the DeepSeek-V3-shaped bf16 decode, a ragged bf16 batch, a
@@ -38,6 +42,8 @@ D_C = 512
 D_V = 128
 ROW = D_C + D_ROPE  # 576 values per cached token
 D_MODEL = 7168      # hidden size of the DeepSeek-V3 shape
+D_CQ = 1536         # query latent width
+RMS_EPS = 2.0 ** -23  # nn.RMSNorm's default eps (float32 machine epsilon)
 
 # dtype names shared with the C ABI (mla_dtype_t)
 F32, BF16, E4M3 = "f32", "bf16", "e4m3"
@@ -206,6 +212,24 @@ def make_out_weight(w: Workload, d_model: int = D_MODEL) -> torch.Tensor:
     g = torch.Generator().manual_seed(w.seed * 1000003 + 29)
     std = 1.0 / math.sqrt(w.heads * D_V)
     return (torch.randn(d_model, w.heads, D_V, generator=g) * std).to(TORCH_DTYPE[w.act_dtype])
+
+
+def make_front_inputs(w: Workload, d_model: int = D_MODEL, d_cq: int = D_CQ) -> dict:
+    """Hidden states of the step's B*Lq new tokens and the front end's weights
+    (nn.Linear layouts [out, in], act dtype), seeded independently of make_inputs."""
+    g = torch.Generator().manual_seed(w.seed * 1000033 + 41)
+    dt = TORCH_DTYPE[w.act_dtype]
+    H = w.heads
+
+    def lin(n_out, n_in):
+        return (torch.randn(n_out, n_in, generator=g) / math.sqrt(n_in)).to(dt)
+
+    d = {"h": torch.randn(w.batch * w.q_len, d_model, generator=g).to(dt),
+         "w_dq": lin(d_cq, d_model), "w_uq": lin(H * D_NOPE, d_cq), "w_qr": lin(H * D_ROPE, d_cq),
+         "w_dkv": lin(D_C, d_model), "w_kr": lin(D_ROPE, d_model)}
+    d["g_q"] = (1.0 + 0.1 * torch.randn(d_cq, generator=g)).to(dt)
+    d["g_kv"] = (1.0 + 0.1 * torch.randn(D_C, generator=g)).to(dt)
+    return d
 
 
 def sample_sequences(w: Workload, k: int, seed: int = 12345):

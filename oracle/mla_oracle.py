@@ -449,3 +449,38 @@ def out_proj_model(o: np.ndarray, w_o: np.ndarray) -> np.ndarray:
     o = np.asarray(o, np.float64)
     w = np.asarray(w_o, np.float64)
     return o.reshape(*o.shape[:-2], -1) @ w.reshape(w.shape[0], -1).T
+
+
+# ---------------------------------------------------------------------------
+# Decode-layer front end: hidden state -> q_nope, q_rope, c_KV, k_R
+# ---------------------------------------------------------------------------
+
+def rms_norm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * gamma over the last axis. [P2] "PyTorch
+    Reference Implementation" (q_norm and kv_norm are RMS norms over d_c_q and
+    d_c_kv)."""
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(gamma, np.float64)
+
+
+def decode_front(h, w_dq, g_q, w_uq, w_qr, w_dkv, g_kv, w_kr, positions, eps: float,
+                 base: float = 10000.0):
+    """The step's projections from the hidden states h [n, d] of its new tokens,
+    [P2] "PyTorch Reference Implementation" (forward_decode_absorbed, steps 1
+    and 2; [P1] §2.1 c^KV = W^DKV h, §2.3 decoupled RoPE keys and queries):
+      c_q    = RMSNorm(W_DQ h)                 (d_c_q)
+      q_nope = W_UQ c_q, per head 128          ([n, H, 128])
+      q_rope = RoPE_pos(W_QR c_q), per head 64 ([n, H, 64], rotated)
+      c_kv   = RMSNorm(W_DKV h)                ([n, 512])
+      k_r    = W_KR h                          ([n, 64], before its rotation, which append applies)
+    Weights are nn.Linear layouts [out, in]: w_dq [d_c_q, d], w_uq [H*128, d_c_q],
+    w_qr [H*64, d_c_q], w_dkv [512, d], w_kr [64, d]. Exact fp64 throughout."""
+    h = np.asarray(h, np.float64)
+    n = h.shape[0]
+    c_q = rms_norm(h @ np.asarray(w_dq, np.float64).T, g_q, eps)
+    q_nope = (c_q @ np.asarray(w_uq, np.float64).T).reshape(n, -1, D_NOPE)
+    q_r = (c_q @ np.asarray(w_qr, np.float64).T).reshape(n, -1, D_ROPE)
+    q_rope = np.stack([rope_rotate_f64(q_r[t], float(positions[t]), base) for t in range(n)]) if n else q_r
+    c_kv = rms_norm(h @ np.asarray(w_dkv, np.float64).T, g_kv, eps)
+    k_r = h @ np.asarray(w_kr, np.float64).T
+    return q_nope, q_rope, c_kv, k_r
