@@ -35,6 +35,10 @@ DEFAULT_WORKLOAD = "dsv3_bf16"
 # DeepSeek-V3-shaped decode batch of 32): its own line, on request only.
 FUSED_WORKLOAD = "dsv3_fused_out"
 FUSED_METRIC = "MLA fused output projection (W~ = W_O W_UV) weight-stream GB/s at 1 GB300; % of HBM roofline"
+# A whole decode layer from the hidden states (front end, append, absorb,
+# paged decode, fused output projection) at the DeepSeek-V3 shape: its own line.
+LAYER_WORKLOAD = "dsv3_layer"
+LAYER_METRIC = "MLA decode layer (front end + latent attention + fused output projection) tokens/s at 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20  # read (not written) before every timed step
 
@@ -341,8 +345,8 @@ def run_fused(args):
     peaks, src = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     achieved = nbytes / (statistics.mean(call_ms) * 1e-3) / 1e9
-    traffic = recorded_traffic(os.path.join(ROOT, "mla_latent_kv_16_gb300", "csrc", "out_fused.cu"),
-                               FUSED_WORKLOAD, prefix="out_fused")
+    traffic = recorded_traffic(os.path.join(ROOT, "mla_latent_kv_16_gb300", "csrc", "linear.cu"),
+                               FUSED_WORKLOAD, prefix="linear")
     out = {
         "metric": FUSED_METRIC, "value": round(gbs, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -508,6 +512,184 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def layer_bytes(w, d_model: int, d_cq: int) -> int:
+    """Algorithmic HBM bytes of one layer step (bf16): every weight once (W_DQKV,
+    W_UQR, W_UK, W~), the visible cache rows, and the step's activations."""
+    H, n = w.heads, w.batch * w.q_len
+    weights = 2 * ((d_cq + 512 + 64) * d_model + H * 192 * d_cq + H * 128 * 512 + d_model * H * 512)
+    cache = sum(int(L) for L in w.seq_lens) * w.row_bytes()
+    acts = 2 * n * (d_model + H * (128 + 64 + 512 + 512) + 576 + d_model)
+    return weights + cache + acts
+
+
+def cpu_layer_run(w, d, fr, w_o, seconds: float):
+    """Time the oracle's whole layer on a bounded sample: the front end for every
+    token of the step, then, sequence by sequence, the materialised attention
+    (all heads) and W_O over the heads, until `seconds` of oracle work are done.
+    The oracle's cache is built as untimed set-up. Returns (tokens/s, sample,
+    threads, seconds)."""
+    import numpy as np
+    from oracle import mla_oracle as O
+    from oracle.harness import f64, oracle_pool, seq_token_mask
+    from mla_latent_kv_16_gb300 import workloads as W
+
+    pos = d["ctx_positions"][d["new_index"]].numpy()
+    t0 = time.perf_counter()
+    q_nope, q_rope, c_kv, k_r = O.decode_front(f64(fr["h"]), f64(fr["w_dq"]), f64(fr["g_q"]), f64(fr["w_uq"]),
+                                               f64(fr["w_qr"]), f64(fr["w_dkv"]), f64(fr["g_kv"]),
+                                               f64(fr["w_kr"]), pos, W.RMS_EPS)
+    elapsed = time.perf_counter() - t0
+    wo64, wuk, wuv = f64(w_o), f64(d["w_uk"]), f64(d["w_uv"])
+    bt = d["block_table"].numpy()
+    H, Lq = w.heads, w.q_len
+    done = 0
+    for b in range(w.batch):
+        pool, sc = oracle_pool(w, d, token_mask=seq_token_mask(w, [b]))
+        t1 = time.perf_counter()
+        full = O.decode_full(q_nope.reshape(w.batch, Lq, H, 128), q_rope.reshape(w.batch, Lq, H, 64), wuk, wuv,
+                             pool, sc, bt, d["seq_lens"].numpy(), Lq, w.page_size, w.cache_dtype,
+                             O.default_scale(), batch_index=[b])
+        O.out_proj_model(full[b][0], wo64)
+        elapsed += time.perf_counter() - t1
+        done += Lq
+        if elapsed > seconds:
+            break
+    sample = (f"front end for all {w.batch * Lq} tokens, then {done} token(s) of {w.name} through the "
+              f"materialised fp64 attention and W_O")
+    return done / elapsed, sample, os.cpu_count(), elapsed
+
+
+def run_layer(args):
+    """One whole decode layer step per timed iteration, replayed as a graph."""
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    from mla_latent_kv_16_gb300 import build as B
+    B.build()
+    from mla_latent_kv_16_gb300 import capi, workloads as W
+    from mla_latent_kv_16_gb300.engine import build_layer
+    capi.load()
+    w = W.preset(DEFAULT_WORKLOAD)
+    d = W.make_inputs(w)
+    d_model, d_cq, H, n = W.D_MODEL, W.D_CQ, w.heads, w.batch * w.q_len
+    fr = W.make_front_inputs(w, d_model, d_cq)
+    w_o = W.make_out_weight(w, d_model)
+    layer = build_layer(w, d)
+    ni = d["new_index"]
+    pos = d["ctx_positions"][ni].cuda()
+    slots = d["ctx_slots"][ni].cuda()
+    h = fr["h"].cuda()
+    w_dqkv = torch.cat([fr["w_dq"], fr["w_dkv"], fr["w_kr"]], 0).cuda()
+    w_uqr = torch.cat([fr["w_uq"], fr["w_qr"]], 0).cuda()
+    g_q, g_kv = fr["g_q"].cuda(), fr["g_kv"].cuda()
+    w_o_dev = w_o.cuda()
+    w_f = capi.mla_fuse_out_weights(w_o_dev, layer.w_uv)
+    w_o2 = w_o_dev.view(d_model, H * 128)
+    ws_front = torch.empty(capi.mla_decode_front_workspace_size(n, d_model, d_cq, H), dtype=torch.uint8,
+                           device="cuda")
+    ws_f = torch.empty(max(16, capi.mla_out_proj_fused_workspace_size(n, d_model, H)), dtype=torch.uint8,
+                       device="cuda")
+    ws_o = torch.empty(max(16, capi.mla_linear_workspace_size(n, d_model, H * 128)), dtype=torch.uint8,
+                       device="cuda")
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    q_nope, q_rope = torch.empty(n, H, 128, **bf), torch.empty(n, H, 64, **bf)
+    c_kv, k_r = torch.empty(n, 512, **bf), torch.empty(n, 64, **bf)
+    y = torch.empty(n, d_model, **bf)
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+
+    def attend():
+        capi.mla_decode_front(h, w_dqkv, g_q, g_kv, w_uqr, pos, layer.rope_cos, layer.rope_sin, W.RMS_EPS, H,
+                              q_nope, q_rope, c_kv, k_r, ws_front, layer.dev_error)
+        layer.append(c_kv, k_r, pos, slots)
+        q_lat = layer.absorb(q_nope.view(w.batch, w.q_len, H, 128))
+        return layer.decode(q_lat, q_rope.view(w.batch, w.q_len, H, 64))[0]
+
+    def step_fused():
+        capi.mla_out_proj_fused(attend(), w_f, y.view(w.batch, w.q_len, d_model), ws_f)
+
+    def step_unfused():
+        o = layer.out_proj(attend())
+        capi.mla_linear(o.view(n, H * 128), w_o2, y, ws_o)
+
+    g_fused = layer.capture(step_fused)
+    g_unfused = layer.capture(step_unfused)
+
+    def timed(graph, k, clk=None):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        if clk is not None:
+            clk.start()
+            time.sleep(0.3)
+        for i in range(k):
+            flush.sum()
+            evs[i][0].record(stream)
+            graph.replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    for g_ in (g_fused, g_unfused):
+        for _ in range(args.warmup):
+            flush.sum()
+            g_.replay()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    fused_ms = timed(g_fused, args.steps, clk)
+    clocks = clk.stop()
+    unfused_ms = timed(g_unfused, args.steps)
+    assert layer.device_error() == 0
+
+    host_h = fr["h"].pin_memory()
+    host_y = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+
+    def e2e():
+        h.copy_(host_h, non_blocking=True)
+        step_fused()
+        host_y.copy_(y, non_blocking=True)
+
+    g_e2e = layer.capture(e2e)
+    for _ in range(args.warmup):
+        flush.sum()
+        g_e2e.replay()
+    e2e_ms = statistics.mean(timed(g_e2e, args.steps))
+
+    ms = statistics.mean(fused_ms)
+    nbytes = layer_bytes(w, d_model, d_cq)
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    launches = 4 + 1 + 1 + 1 + (1 if layer.splits > 1 else 0) + (2 if capi.mla_out_proj_fused_workspace_size(
+        n, d_model, H) else 1)
+    out = {
+        "metric": LAYER_METRIC, "value": round(n / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded hidden states, N(0,1/sqrt(fan_in)) weights, RMSNorm gains 1 + 0.1 N(0,1))",
+        "config": {"workload": LAYER_WORKLOAD, "batch": w.batch, "q_len": w.q_len, "heads": H, "d_model": d_model,
+                   "d_cq": d_cq, "seq_len": int(max(w.seq_lens)), "page_size": w.page_size,
+                   "num_splits": layer.splits,
+                   "l2": "flushed before every timed step by reading a 256 MiB buffer; weights + cache > L2",
+                   "parallelism": "dp1 (one replica)"},
+        "unfused_output_ms_per_step": round(statistics.mean(unfused_ms), 5),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "whole layer step; algorithmic bytes = W_DQKV + W_UQR + W_UK + W~ + cache rows + activations",
+                     "bytes_per_step": nbytes, "peak_source": f"hbm_gbs of {src}"},
+        "e2e": {"value": round(n / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": host_h.numel() * 2, "d2h_bytes_per_step": host_y.numel() * 2},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        v, sample, thr, el = cpu_layer_run(w, d, fr, w_o, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(v, 4), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                               "sample": sample, "seconds": round(el, 2)}
+    print(json.dumps(out), flush=True)
+
+
 def run_reference_fused(args):
     from mla_latent_kv_16_gb300 import workloads as W
     w = W.preset(DEFAULT_WORKLOAD)
@@ -530,12 +712,40 @@ def run_reference_fused(args):
     print(json.dumps(out), flush=True)
 
 
+def run_reference_layer(args):
+    from mla_latent_kv_16_gb300 import workloads as W
+    w = W.preset(DEFAULT_WORKLOAD)
+    d = W.make_inputs(w)
+    fr = W.make_front_inputs(w, W.D_MODEL, W.D_CQ)
+    w_o = W.make_out_weight(w, W.D_MODEL)
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_layer_run(w, d, fr, w_o, min(budget, 2.0))
+    vals, secs, sample, thr = [], 0.0, "", 1
+    for _ in range(args.steps):
+        v, sample, thr, el = cpu_layer_run(w, d, fr, w_o, budget)
+        vals.append(v)
+        secs += el
+    value = statistics.mean(vals)
+    out = {"impl": "reference", "metric": LAYER_METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded)", "config": {"workload": LAYER_WORKLOAD, "batch": w.batch, "q_len": w.q_len,
+                                                     "heads": w.heads, "d_model": W.D_MODEL, "d_cq": W.D_CQ},
+           "cpu_baseline": {"kind": "oracle", "cores": thr, "sample": sample, "value": round(value, 4),
+                            "unit": "tokens/s"},
+           "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
     if args.workload == FUSED_WORKLOAD:
         return run_reference_fused(args)
+    if args.workload == LAYER_WORKLOAD:
+        return run_reference_layer(args)
     from mla_latent_kv_16_gb300 import workloads as W
     w = W.preset(args.workload)
     d = W.make_inputs(w)
@@ -566,6 +776,8 @@ def main():
         run_reference(args)
     elif args.workload == FUSED_WORKLOAD:
         run_fused(args)
+    elif args.workload == LAYER_WORKLOAD:
+        run_layer(args)
     else:
         run_ours(args)
 

@@ -15,6 +15,12 @@
  *
  *   mla_out_proj_fused: y[t,:] = sum_h W~[:,h,:] u[t,h,:]     (H*512 -> d_model)
  *
+ * and before the step, from the layer's hidden states (mla_decode_front):
+ *
+ *   h -> q_nope, q_rope (rotated), c_kv, k_r   (RMSNorm'ed low-rank projections)
+ *
+ * mla_linear is the generic y = x W^T these projections run on.
+ *
  * Sources (page titles):
  *   [P1] "Model Architecture Driving Inference Systems: From MHA/GQA to DeepSeek
  *        MLA Matrix Absorption and Memory Minimalism" (dev.to)
@@ -288,14 +294,77 @@ size_t mla_out_proj_fused_workspace_size(int32_t n_tokens, int32_t d_model, mla_
  *   y         [n_tokens][d_model] act, written
  *   workspace : workspace_bytes >= mla_out_proj_fused_workspace_size(...)
  *               (may be NULL when that is 0); nothing in it has to start at zero
- * fp32 accumulation. When K = 512 H is split across CTAs, the fp32 partial
- * sums are added in split order by a second kernel, so results do not depend
- * on timing. bf16 with d_model % 128 == 0 runs on the tensor cores; other
- * shapes and fp32 on CUDA cores.
+ * This is mla_linear with n_out = d_model and n_in = 512 H (W~ viewed as
+ * [d_model][512 H]); its accumulation, determinism and workspace are those of
+ * mla_linear.
  */
 mla_status_t mla_out_proj_fused(const void *u, const void *w_fused, void *y, int32_t n_tokens,
                                 int32_t d_model, void *workspace, size_t workspace_bytes,
                                 mla_dims_t dims, mla_dtype_t act, mla_stream_t stream);
+
+/*
+ * mla_linear -- y[t][o] = sum_i W[o][i] x[t][i], the linear layer of a decode
+ * step (nn.Linear layout, no bias): the fused output projection and the
+ * front end's projections are instances of it; so is an unfused W_O applied to
+ * the concatenated per-head outputs ([P2] "Value Output Matrix Absorption",
+ * W_O in R^{d x (H d_v)}).
+ *
+ *   x [n_tokens][n_in] act, w [n_out][n_in] act, y [n_tokens][n_out] act (written)
+ *   n_out, n_in: 1 .. 2^20; n_tokens: 0 .. 2^20
+ *   workspace : workspace_bytes >= mla_linear_workspace_size(...) (may be NULL
+ *               when that is 0); nothing in it has to start at zero
+ * fp32 accumulation. bf16 with n_in % 64 == 0 runs on the tensor cores, with K
+ * split across CTAs when there are too few rows of W to occupy every SM; the
+ * fp32 partial sums are then added in split order by a second kernel, so the
+ * result does not depend on timing. Other shapes and fp32 run on CUDA cores.
+ */
+size_t mla_linear_workspace_size(int32_t n_tokens, int32_t n_out, int32_t n_in, mla_dtype_t act);
+mla_status_t mla_linear(const void *x, const void *w, void *y, int32_t n_tokens, int32_t n_out,
+                        int32_t n_in, void *workspace, size_t workspace_bytes, mla_dtype_t act,
+                        mla_stream_t stream);
+
+/*
+ * mla_decode_front -- the decode layer's front end: from the hidden states of
+ * the step's new tokens to the inputs of mla_cache_append and mla_absorb_q /
+ * mla_decode_paged. [P2] "PyTorch Reference Implementation"
+ * (forward_decode_absorbed, steps 1 and 2); [P1] §2.1 (c^KV = W^DKV h), §2.3
+ * (decoupled RoPE queries and keys).
+ *
+ *   c_q    = RMSNorm(W_DQ h) * g_q            RMSNorm(v) = v / sqrt(mean(v^2) + eps)
+ *   q_nope = W_UQ c_q   per head 128
+ *   q_rope = RoPE_pos(W_QR c_q)   per head 64, adjacent pairs, the angle and
+ *            rounding conventions of mla_cache_append (cos/sin tables)
+ *   c_kv   = RMSNorm(W_DKV h) * g_kv
+ *   k_r    = W_KR h   (not rotated: mla_cache_append rotates it)
+ *
+ *   h         [n_tokens][d_model] act
+ *   w_dqkv    [d_cq + 512 + 64][d_model] act: rows [0, d_cq) W_DQ, then 512
+ *             rows of W_DKV, then 64 rows of W_KR (nn.Linear layouts, stacked)
+ *   g_q [d_cq], g_kv [512] act: the RMSNorm gains
+ *   w_uqr     [H*128 + H*64][d_cq] act: rows [0, H*128) W_UQ (row 128 h + d is
+ *             head h, feature d), then H*64 rows of W_QR (row 64 h + r)
+ *   positions [n_tokens] int32: each token's position (that of its cache row)
+ *   rope_cos, rope_sin [max_pos][32] fp32 (mla_rope_table)
+ *   eps       >= 0 (torch's nn.RMSNorm default in fp32 is 2^-23)
+ *   q_nope [n_tokens][H][128], q_rope [n_tokens][H][64], c_kv [n_tokens][512],
+ *   k_r [n_tokens][64] act, written
+ *   workspace : workspace_bytes >= mla_decode_front_workspace_size(...); holds
+ *             the fp32 sums of both products and c_q; nothing in it has to
+ *             start at zero
+ * The products accumulate in fp32; the norms and the rotation are computed in
+ * fp32 from the fp32 sums; c_q is rounded to act once, before W_UQ and W_QR.
+ * A position outside [0, max_pos) writes a zero q_rope for that token and ORs
+ * MLA_DEVERR_BAD_POSITION into *dev_error.
+ */
+size_t mla_decode_front_workspace_size(int32_t n_tokens, int32_t d_model, int32_t d_cq,
+                                       mla_dims_t dims, mla_dtype_t act);
+mla_status_t mla_decode_front(const void *h, const void *w_dqkv, const void *g_q, const void *g_kv,
+                              const void *w_uqr, const int32_t *positions, const float *rope_cos,
+                              const float *rope_sin, int32_t max_pos, float eps, int32_t n_tokens,
+                              int32_t d_model, int32_t d_cq, void *q_nope, void *q_rope, void *c_kv,
+                              void *k_r, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_error, mla_dims_t dims, mla_dtype_t act,
+                              mla_stream_t stream);
 
 /*
  * mla_read_device_error -- synchronise `stream`, copy *dev_error (device) to

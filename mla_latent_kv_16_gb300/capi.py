@@ -29,7 +29,8 @@ MLA_STATIC_SCRATCH_BYTES = 32 << 20  # size of the library's fixed split-KV scra
 EXPORTED = ("mla_status_string", "mla_version", "mla_rope_table", "mla_cache_append", "mla_absorb_q",
             "mla_decode_num_splits", "mla_decode_workspace_size", "mla_decode_paged", "mla_out_proj",
             "mla_read_device_error", "mla_decode_paged_static_scratch", "mla_fuse_out_weights",
-            "mla_out_proj_fused_workspace_size", "mla_out_proj_fused")
+            "mla_out_proj_fused_workspace_size", "mla_out_proj_fused", "mla_linear_workspace_size", "mla_linear",
+            "mla_decode_front_workspace_size", "mla_decode_front")
 
 
 class MlaDims(ctypes.Structure):
@@ -93,6 +94,15 @@ def load(path: Optional[str] = None):
     L.mla_out_proj_fused_workspace_size.argtypes = [i32, i32, MlaDims, ctypes.c_int]
     L.mla_out_proj_fused.restype = ctypes.c_int
     L.mla_out_proj_fused.argtypes = [vp, vp, vp, i32, i32, vp, sz, MlaDims, ctypes.c_int, vp]
+    L.mla_linear_workspace_size.restype = sz
+    L.mla_linear_workspace_size.argtypes = [i32, i32, i32, ctypes.c_int]
+    L.mla_linear.restype = ctypes.c_int
+    L.mla_linear.argtypes = [vp, vp, vp, i32, i32, i32, vp, sz, ctypes.c_int, vp]
+    L.mla_decode_front_workspace_size.restype = sz
+    L.mla_decode_front_workspace_size.argtypes = [i32, i32, i32, MlaDims, ctypes.c_int]
+    L.mla_decode_front.restype = ctypes.c_int
+    L.mla_decode_front.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, f32, i32, i32, i32, vp, vp, vp, vp, vp, sz,
+                                   vp, MlaDims, ctypes.c_int, vp]
     L.mla_read_device_error.restype = ctypes.c_int
     L.mla_read_device_error.argtypes = [vp, vp, vp]
     _LIB = L
@@ -222,6 +232,57 @@ def mla_out_proj_fused(u, w_fused, y=None, workspace=None, stream=None):
                                                             _ptr(workspace), ws_bytes, dims(H), _act_code(u),
                                                             _stream(stream)))
     return y
+
+
+def mla_linear_workspace_size(n_tokens: int, n_out: int, n_in: int, act: str = "bf16") -> int:
+    return load().mla_linear_workspace_size(n_tokens, n_out, n_in, DTYPE_CODE[act])
+
+
+def mla_linear(x, w, y=None, workspace=None, stream=None):
+    """x [..., n_in], w [n_out, n_in] -> y [..., n_out] = x w^T."""
+    _contig_cuda(x, w, y, workspace)
+    n_out, n_in = w.shape
+    n = x.numel() // n_in
+    if y is None:
+        y = torch.empty(*x.shape[:-1], n_out, dtype=x.dtype, device=x.device)
+    act = "f32" if x.dtype == torch.float32 else "bf16"
+    need = mla_linear_workspace_size(n, n_out, n_in, act) if n > 0 else 0
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("mla_linear", load().mla_linear(_ptr(x), _ptr(w), _ptr(y), n, n_out, n_in, _ptr(workspace), ws_bytes,
+                                            _act_code(x), _stream(stream)))
+    return y
+
+
+def mla_decode_front_workspace_size(n_tokens: int, d_model: int, d_cq: int, num_heads: int, act: str = "bf16") -> int:
+    return load().mla_decode_front_workspace_size(n_tokens, d_model, d_cq, dims(num_heads), DTYPE_CODE[act])
+
+
+def mla_decode_front(h, w_dqkv, g_q, g_kv, w_uqr, positions, rope_cos, rope_sin, eps: float, num_heads: int,
+                     q_nope=None, q_rope=None, c_kv=None, k_r=None, workspace=None, dev_error=None, stream=None):
+    """h [n, d_model] -> (q_nope [n, H, 128], q_rope [n, H, 64] rotated, c_kv [n, 512], k_r [n, 64])."""
+    _contig_cuda(h, w_dqkv, g_q, g_kv, w_uqr, positions, rope_cos, rope_sin, q_nope, q_rope, c_kv, k_r, workspace,
+                 dev_error)
+    n, d_model = h.shape
+    d_cq = g_q.shape[0]
+    H = num_heads
+    mk = lambda *shape: torch.empty(*shape, dtype=h.dtype, device=h.device)
+    q_nope = mk(n, H, 128) if q_nope is None else q_nope
+    q_rope = mk(n, H, 64) if q_rope is None else q_rope
+    c_kv = mk(n, 512) if c_kv is None else c_kv
+    k_r = mk(n, 64) if k_r is None else k_r
+    act = "f32" if h.dtype == torch.float32 else "bf16"
+    need = mla_decode_front_workspace_size(n, d_model, d_cq, H, act) if n > 0 else 0
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=h.device)
+    st = load().mla_decode_front(_ptr(h), _ptr(w_dqkv), _ptr(g_q), _ptr(g_kv), _ptr(w_uqr), _ptr(positions),
+                                 _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0], eps, n, d_model, d_cq,
+                                 _ptr(q_nope), _ptr(q_rope), _ptr(c_kv), _ptr(k_r), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _ptr(dev_error), dims(H),
+                                 _act_code(h), _stream(stream))
+    _check("mla_decode_front", st)
+    return q_nope, q_rope, c_kv, k_r
 
 
 def mla_decode_paged(q_lat, q_rope, cache, scales, block_table, seq_lens, page_size: int, cache_dtype: str,

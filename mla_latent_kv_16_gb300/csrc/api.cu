@@ -27,6 +27,7 @@ namespace {
 constexpr int32_t kMaxTokens = 1 << 20;
 constexpr int32_t kMaxBatchQ = 65535;
 constexpr int32_t kMaxDModel = 1 << 16;
+constexpr int32_t kMaxLinearDim = 1 << 20;
 
 bool dims_ok(const mla_dims_t& d) {
   return d.d_nope == 128 && d.d_c == 512 && d.d_rope == 64 && d.d_v == 128 && d.num_heads >= 1 &&
@@ -178,28 +179,77 @@ mla_status_t mla_fuse_out_weights(const void* w_o, const void* w_uv, void* w_fus
   return from_cuda(launch_fuse_weights(a, static_cast<cudaStream_t>(stream)));
 }
 
-size_t mla_out_proj_fused_workspace_size(int32_t n_tokens, int32_t d_model, mla_dims_t dims, mla_dtype_t act) {
-  if (!dims_ok(dims) || n_tokens < 1 || n_tokens > kMaxTokens || d_model < 1 || d_model > kMaxDModel) return 0;
+size_t mla_linear_workspace_size(int32_t n_tokens, int32_t n_out, int32_t n_in, mla_dtype_t act) {
+  if (n_tokens < 1 || n_tokens > kMaxTokens || n_out < 1 || n_out > kMaxLinearDim || n_in < 1 ||
+      n_in > kMaxLinearDim)
+    return 0;
   if (act != MLA_F32 && act != MLA_BF16) return 0;
-  return out_fused_workspace_bytes(n_tokens, d_model, dims.num_heads, act);
+  if (linear_splits(n_tokens, n_out, n_in, act) <= 1) return 0;
+  return linear_partial_bytes(n_tokens, n_out, n_in, act);
+}
+
+mla_status_t mla_linear(const void* x, const void* w, void* y, int32_t n_tokens, int32_t n_out, int32_t n_in,
+                        void* workspace, size_t workspace_bytes, mla_dtype_t act, mla_stream_t stream) {
+  if (n_tokens < 0 || n_tokens > kMaxTokens || n_out < 1 || n_out > kMaxLinearDim || n_in < 1 ||
+      n_in > kMaxLinearDim)
+    return MLA_ERR_INVALID_ARG;
+  if (act != MLA_F32 && act != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return MLA_OK;
+  if (x == nullptr || w == nullptr || y == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return MLA_ERR_INVALID_ARG;
+  const int32_t splits = linear_splits(n_tokens, n_out, n_in, act);
+  const size_t need = splits > 1 ? linear_partial_bytes(n_tokens, n_out, n_in, act) : 0;
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+  LinearArgs a{x, w, y, need > 0 ? static_cast<float*>(workspace) : nullptr, n_tokens, n_out, n_in, splits, act};
+  return from_cuda(launch_linear(a, static_cast<cudaStream_t>(stream), true));
+}
+
+size_t mla_out_proj_fused_workspace_size(int32_t n_tokens, int32_t d_model, mla_dims_t dims, mla_dtype_t act) {
+  if (!dims_ok(dims) || d_model > kMaxDModel) return 0;
+  return mla_linear_workspace_size(n_tokens, d_model, dims.num_heads * dims.d_c, act);
 }
 
 mla_status_t mla_out_proj_fused(const void* u, const void* w_fused, void* y, int32_t n_tokens, int32_t d_model,
                                 void* workspace, size_t workspace_bytes, mla_dims_t dims, mla_dtype_t act,
                                 mla_stream_t stream) {
-  if (!dims_ok(dims) || n_tokens < 0 || n_tokens > kMaxTokens || d_model < 1 || d_model > kMaxDModel)
+  if (!dims_ok(dims) || d_model < 1 || d_model > kMaxDModel) return MLA_ERR_INVALID_ARG;
+  return mla_linear(u, w_fused, y, n_tokens, d_model, dims.num_heads * dims.d_c, workspace, workspace_bytes, act,
+                    stream);
+}
+
+size_t mla_decode_front_workspace_size(int32_t n_tokens, int32_t d_model, int32_t d_cq, mla_dims_t dims,
+                                       mla_dtype_t act) {
+  if (!dims_ok(dims) || n_tokens < 1 || n_tokens > kMaxTokens || d_model < 1 || d_model > kMaxDModel ||
+      d_cq < 1 || d_cq > kMaxDModel)
+    return 0;
+  if (act != MLA_F32 && act != MLA_BF16) return 0;
+  return front_workspace_bytes(n_tokens, d_model, d_cq, dims.num_heads, act);
+}
+
+mla_status_t mla_decode_front(const void* h, const void* w_dqkv, const void* g_q, const void* g_kv,
+                              const void* w_uqr, const int32_t* positions, const float* rope_cos,
+                              const float* rope_sin, int32_t max_pos, float eps, int32_t n_tokens, int32_t d_model,
+                              int32_t d_cq, void* q_nope, void* q_rope, void* c_kv, void* k_r, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_error, mla_dims_t dims, mla_dtype_t act,
+                              mla_stream_t stream) {
+  if (!dims_ok(dims) || n_tokens < 0 || n_tokens > kMaxTokens || d_model < 1 || d_model > kMaxDModel || d_cq < 1 ||
+      d_cq > kMaxDModel || max_pos < 1 || !std::isfinite(eps) || eps < 0.0f)
     return MLA_ERR_INVALID_ARG;
   if (act != MLA_F32 && act != MLA_BF16) return MLA_ERR_UNSUPPORTED;
   if (n_tokens == 0) return MLA_OK;
-  if (u == nullptr || w_fused == nullptr || y == nullptr) return MLA_ERR_INVALID_ARG;
-  if (!aligned16(u) || !aligned16(w_fused) || !aligned16(y)) return MLA_ERR_INVALID_ARG;
-  const int32_t splits = out_fused_splits(n_tokens, d_model, dims.num_heads, act);
-  const size_t need = out_fused_workspace_bytes(n_tokens, d_model, dims.num_heads, act);
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MLA_ERR_WORKSPACE_TOO_SMALL;
-  if (need > 0 && !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
-  FusedOutArgs a{u, w_fused, y, need > 0 ? static_cast<float*>(workspace) : nullptr, n_tokens, d_model,
-                 dims.num_heads, splits, act};
-  return from_cuda(launch_out_fused(a, static_cast<cudaStream_t>(stream)));
+  const void* ptrs[] = {h, w_dqkv, g_q, g_kv, w_uqr, positions, rope_cos, rope_sin, q_nope, q_rope, c_kv, k_r};
+  for (const void* p : ptrs)
+    if (p == nullptr) return MLA_ERR_INVALID_ARG;
+  const void* aligned[] = {h, w_dqkv, w_uqr, q_nope, q_rope, c_kv, k_r};
+  for (const void* p : aligned)
+    if (!aligned16(p)) return MLA_ERR_INVALID_ARG;
+  const size_t need = front_workspace_bytes(n_tokens, d_model, d_cq, dims.num_heads, act);
+  if (workspace == nullptr || workspace_bytes < need) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+  FrontArgs f{h, w_dqkv, g_q, g_kv, w_uqr, positions, rope_cos, rope_sin, max_pos, eps, n_tokens, d_model, d_cq,
+              dims.num_heads, q_nope, q_rope, c_kv, k_r, workspace, dev_error, act};
+  return from_cuda(launch_front(f, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t mla_decode_num_splits(int32_t batch, int32_t q_len, int32_t max_pages_per_seq, int32_t page_size,

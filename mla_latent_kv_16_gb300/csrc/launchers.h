@@ -76,22 +76,52 @@ struct FuseWeightsArgs {
 };
 cudaError_t launch_fuse_weights(const FuseWeightsArgs& a, cudaStream_t s);
 
-struct FusedOutArgs {
-  const void* u;     // [n][H][512]
-  const void* w;     // W~ [d][H][512]
-  void* y;           // [n][d]
-  float* part;       // [k_splits][n][d] fp32 partial sums (k_splits > 1)
+// Generic linear layer y[t][o] = sum_i W[o][i] x[t][i] (linear.cu).
+struct LinearArgs {
+  const void* x;     // [n][n_in]
+  const void* w;     // [n_out][n_in]
+  void* y;           // [n][n_out] act (written when part is null, or by the split sum)
+  float* part;       // [k_splits][n][n_out] fp32 sums, or null (then k_splits == 1, y written directly)
   int32_t n_tokens;
-  int32_t d_model;
-  int32_t heads;
-  int32_t k_splits;  // from out_fused_splits
+  int32_t n_out;
+  int32_t n_in;
+  int32_t k_splits;  // from linear_splits
   mla_dtype_t act;
 };
-// K splits of the fused output projection for these sizes on the current
-// device (1 on the CUDA-core path), and the workspace bytes they need.
-int32_t out_fused_splits(int32_t n_tokens, int32_t d_model, int32_t heads, mla_dtype_t act);
-size_t out_fused_workspace_bytes(int32_t n_tokens, int32_t d_model, int32_t heads, mla_dtype_t act);
-cudaError_t launch_out_fused(const FusedOutArgs& a, cudaStream_t s);
+// K splits for these sizes on the current device (1 on the CUDA-core path),
+// and the bytes of their fp32 sums [splits][n][n_out], 256-byte aligned.
+int32_t linear_splits(int32_t n_tokens, int32_t n_out, int32_t n_in, mla_dtype_t act);
+size_t linear_partial_bytes(int32_t n_tokens, int32_t n_out, int32_t n_in, mla_dtype_t act);
+// reduce: with part set, also add the splits into y (otherwise the caller
+// consumes the fp32 sums itself).
+cudaError_t launch_linear(const LinearArgs& a, cudaStream_t s, bool reduce);
+
+// Decode-layer front end (front.cu).
+struct FrontArgs {
+  const void* h;       // [n][d_model]
+  const void* w_dqkv;  // [d_cq + 512 + 64][d_model]
+  const void* g_q;     // [d_cq]
+  const void* g_kv;    // [512]
+  const void* w_uqr;   // [H*128 + H*64][d_cq]
+  const int32_t* positions;
+  const float* cos_t;
+  const float* sin_t;
+  int32_t max_pos;
+  float eps;
+  int32_t n_tokens;
+  int32_t d_model;
+  int32_t d_cq;
+  int32_t heads;
+  void* q_nope;  // [n][H][128]
+  void* q_rope;  // [n][H][64]
+  void* c_kv;    // [n][512]
+  void* k_r;     // [n][64]
+  void* workspace;
+  int32_t* dev_error;
+  mla_dtype_t act;
+};
+size_t front_workspace_bytes(int32_t n_tokens, int32_t d_model, int32_t d_cq, int32_t heads, mla_dtype_t act);
+cudaError_t launch_front(const FrontArgs& f, cudaStream_t s);
 
 struct DecodeArgs {
   const void* q_lat;

@@ -1,0 +1,412 @@
+// Generic linear layer y[t][o] = sum_i W[o][i] x[t][i] for the few tokens of
+// a decode step (nn.Linear layout: W is [n_out][n_in], row-major). At decode
+// batch sizes this is a stream of W from HBM and nothing else matters.
+//
+// The tcgen05 kernel (bf16, n_in % 64 == 0) takes 128 rows of W as the MMA M
+// dimension and up to 256 tokens as N, and splits the n_in (K) dimension so
+// that there are enough work units (row tile x K split x token tile) for every
+// SM. It is persistent, one CTA per SM: a producer warp streams all of the
+// CTA's units through one TMA ring of 64-wide K chunks (a 128 x 64 box of W
+// and an n x 64 box of x, both 128-byte swizzled) without a break between
+// units, an MMA warp accumulates each unit in one of two TMEM buffers, and four
+// epilogue warps empty the other. Rows of W past n_out read as zero and are
+// not written. With a K split (or when the caller asks for fp32 sums) the
+// partial sums go to an fp32 workspace and a second kernel adds them in split
+// order, so results do not depend on timing. Other types and shapes run on
+// CUDA cores.
+//
+// Users: the fused output projection ("Model Architecture Driving Inference
+// Systems" §3.2, y = W~^O u over all heads) and the decode-layer front end's
+// projections ("Multi-Head Latent Attention (MLA)" page, "PyTorch Reference
+// Implementation": W_DQ, W_DKV, W_KR on h; W_UQ, W_QR on c_q).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "launchers.h"
+#include "tc_ptx.cuh"
+
+namespace mla {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 192;      // producer warp, MMA warp, four epilogue warps
+constexpr int kMaxTok = 256;       // tokens per unit (MMA N)
+constexpr int kChunkK = 64;        // K elements per TMA box (128 bytes of bf16)
+constexpr int kABytes = 128 * 128;  // one W box: 128 rows x 64 bf16
+constexpr int kMaxStages = 12;
+constexpr int kMaxSplits = 32;
+constexpr int kRingBudget = 200 * 1024;  // shared memory for the TMA ring
+
+struct LinearCtl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+// ------------------------------------------------------------------ CUDA cores
+
+// grid (ceil(n/8), ceil(n_out/8)), block 256: warp = one row o of W against 8
+// tokens; lanes stride K. Writes y, or fp32 sums to part[0] when part is set.
+template <typename T>
+__global__ void __launch_bounds__(256) linear_simt_kernel(LinearArgs p) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int o = blockIdx.y * 8 + warp;
+  const int t0 = blockIdx.x * 8;
+  if (o >= p.n_out) return;
+  const int64_t K = p.n_in;
+  const int nt = min(8, p.n_tokens - t0);
+  const T* w = static_cast<const T*>(p.w) + static_cast<int64_t>(o) * K;
+  const T* x = static_cast<const T*>(p.x) + static_cast<int64_t>(t0) * K;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  for (int64_t k = lane; k < K; k += 32) {
+    const float wv = ActIO<T>::load(w + k);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < nt) acc[j] = fmaf(wv, ActIO<T>::load(x + j * K + k), acc[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float s = warp_sum(acc[j]);
+    if (lane == 0 && j < nt) {
+      const int64_t idx = static_cast<int64_t>(t0 + j) * p.n_out + o;
+      if (p.part != nullptr)
+        p.part[idx] = s;
+      else
+        ActIO<T>::store(static_cast<T*>(p.y) + idx, s);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ tcgen05
+
+// A work unit is (128 rows of W, K split, token tile). The unit's coordinates.
+struct Unit {
+  int o0, split, t0, c_lo, nc;
+};
+
+__device__ __forceinline__ Unit unit_at(const LinearArgs& p, int u, int o_tiles, int chunks) {
+  Unit r;
+  const int rest = u / o_tiles;
+  r.o0 = (u - rest * o_tiles) * 128;
+  r.split = rest % p.k_splits;
+  r.t0 = (rest / p.k_splits) * kMaxTok;
+  r.c_lo = static_cast<int>(static_cast<int64_t>(r.split) * chunks / p.k_splits);
+  r.nc = static_cast<int>(static_cast<int64_t>(r.split + 1) * chunks / p.k_splits) - r.c_lo;
+  return r;
+}
+
+// Persistent: grid = min(units, SMs), one CTA per SM, CTA c takes units c, c + G,
+// c + 2G, ... Warp 0 (one lane) streams every chunk of those units through the
+// TMA ring without a break between units; warp 1 (one lane) issues the MMAs
+// into one of two TMEM accumulators; warps 2-5 read back the other (warp w owns
+// TMEM lanes 32 (w % 4) .. +32, thread = row of W) and write the unit's output.
+__global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const __grid_constant__ CUtensorMap amap,
+                                                                const __grid_constant__ CUtensorMap bmap,
+                                                                LinearArgs p, int n_tile, int stages,
+                                                                uint32_t acc_cols, int units) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int b_bytes = n_tile * 128;
+  const int stage_bytes = kABytes + ((b_bytes + 1023) & ~1023);
+  LinearCtl* ctl = reinterpret_cast<LinearCtl*>(base + stages * stage_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int o_tiles = (p.n_out + 127) / 128;
+  const int chunks = p.n_in / kChunkK;
+  pdl_trigger();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl->acc_full[b]), 1);
+      mbar_init(smem_u32(&ctl->acc_empty[b]), 4);  // the four epilogue warps
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init_cluster();
+    prefetch_tmap(&amap);
+    prefetch_tmap(&bmap);
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&ctl->tmem_base), 2 * acc_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int32_t* abort_flag = &ctl->abort_flag;
+  // W may have been written by the kernel just before this one (the fold), so
+  // nothing is loaded before the wait for the previous kernels.
+  pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer. W is read once when all tokens fit one tile (x then stays in L2).
+      const bool once = p.n_tokens <= kMaxTok;
+      const uint64_t pol = l2_policy_evict_first();
+      uint32_t g = 0;  // chunks issued so far, over all of this CTA's units
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = unit_at(p, u, o_tiles, chunks);
+        for (int k = 0; k < w.nc; ++k, ++g) {
+          const int s = static_cast<int>(g % stages);
+          if (g >= static_cast<uint32_t>(stages) &&
+              !mbar_wait<2>(smem_u32(&ctl->empty[s]), ((g / stages) & 1) ^ 1, abort_flag, nullptr)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = smem_u32(base + s * stage_bytes);
+          const uint32_t bar = smem_u32(&ctl->full[s]);
+          const int32_t xk = (w.c_lo + k) * kChunkK;
+          mbar_arrive_expect_tx(bar, kABytes + b_bytes);
+          if (once)
+            tma_load_2d(dst, &amap, bar, xk, w.o0, pol);  // rows past n_out read as zero
+          else
+            tma_load_2d_nohint(dst, &amap, bar, xk, w.o0);
+          tma_load_2d_nohint(dst + kABytes, &bmap, bar, xk, w.t0);  // token rows past n read as zero
+        }
+      }
+      if (!ok) {
+        // after an abort nobody consumes: let the last copy issued into each slot land
+        volatile int32_t never = 0;
+        const uint32_t first = g > static_cast<uint32_t>(stages) ? g - stages : 0;
+        for (uint32_t q = first; q < g; ++q)
+          mbar_wait<2>(smem_u32(&ctl->full[q % stages]), (q / stages) & 1, &never, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(128, n_tile, false, false);
+      uint32_t g = 0;
+      bool ok = true;
+      int i = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
+        const Unit w = unit_at(p, u, o_tiles, chunks);
+        const int b = i & 1;
+        if (i >= 2 && !mbar_wait<2>(smem_u32(&ctl->acc_empty[b]), ((i >> 1) - 1) & 1, abort_flag, nullptr)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(b) * acc_cols;
+        for (int k = 0; k < w.nc; ++k, ++g) {
+          const int s = static_cast<int>(g % stages);
+          if (!mbar_wait<2>(smem_u32(&ctl->full[s]), (g / stages) & 1, abort_flag, nullptr)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(base + s * stage_bytes);
+          const uint64_t db = sdesc_sw128(a0 + kABytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kChunkK / 16; ++kk)
+            mma_ss(d, sdesc_sw128(a0 + kk * 32, 16, 1024), db + ((kk * 32) >> 4), idesc,
+                   (k > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&ctl->empty[s]));
+        }
+        if (ok) mma_commit(smem_u32(&ctl->acc_full[b]));
+      }
+      // every MMA this thread issued completes before the TMEM is freed
+      mma_commit(smem_u32(&ctl->drain));
+      volatile int32_t never = 0;
+      mbar_wait<2>(smem_u32(&ctl->drain), 0, &never, nullptr);
+    }
+  } else {
+    // ---- epilogue (warps 2-5)
+    const int q = warp & 3;
+    const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+    bool ok = true;
+    int i = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+      const Unit w = unit_at(p, u, o_tiles, chunks);
+      const int b = i & 1;
+      const bool got =
+          __all_sync(0xffffffffu, ok && mbar_wait<0>(smem_u32(&ctl->acc_full[b]), (i >> 1) & 1, abort_flag, nullptr));
+      ok = got;
+      tc_fence_after();
+      const int n_tok = min(kMaxTok, p.n_tokens - w.t0);
+      const int o = w.o0 + q * 32 + lane;
+      for (int c = 0; c < n_tile; c += 32) {
+        float v[32];
+        if (got) {
+          tmem_ld32_sync(tmem + static_cast<uint32_t>(b) * acc_cols + lanes + c, v);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = 0.0f;
+        }
+        if (o >= p.n_out) continue;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int t = c + k;
+          if (t >= n_tok) break;
+          const float val = got ? v[k] : CUDART_NAN_F;  // an aborted unit reads as NaN, never as stale data
+          const int64_t row = w.t0 + t;
+          if (p.part == nullptr)
+            static_cast<__nv_bfloat16*>(p.y)[row * p.n_out + o] = __float2bfloat16_rn(val);
+          else
+            p.part[(static_cast<int64_t>(w.split) * p.n_tokens + row) * p.n_out + o] = val;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (got && lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[b]));
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * acc_cols);
+  }
+}
+
+// y = sum over splits s = 0, 1, ... of part[s], one output per thread.
+template <typename T>
+__global__ void __launch_bounds__(256) linear_reduce_kernel(LinearArgs p) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t n = static_cast<int64_t>(p.n_tokens) * p.n_out;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (i >= n) return;
+  float acc = p.part[i];
+  for (int s = 1; s < p.k_splits; ++s) acc += p.part[s * n + i];
+  ActIO<T>::store(static_cast<T*>(p.y) + i, acc);
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2D map over a [rows][cols] bf16 matrix, boxes of 64 columns x box_rows.
+bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool use_tc(int32_t n_in, mla_dtype_t act) { return act == MLA_BF16 && n_in % kChunkK == 0; }
+
+struct LinearPlan {
+  int n_tile;         // MMA N (tokens per unit, multiple of 16)
+  int tok_tiles;      // units along the tokens
+  int stages;         // TMA ring depth
+  int splits;         // units along K
+  int units;          // row tiles x splits x token tiles
+  int grid;           // persistent CTAs: min(units, SMs)
+  size_t smem;        // dynamic shared memory per CTA
+  uint32_t acc_cols;  // TMEM columns of one of the two accumulators
+};
+
+// Tile shape, ring depth and K split of the persistent tcgen05 kernel. One CTA
+// per SM streams its units back to back, so the split count minimises the
+// chunks the busiest CTA streams: units per CTA (rounded up) x (chunks per unit
+// + about one chunk's worth of partial-sum traffic).
+LinearPlan plan_tc(int32_t n_tokens, int32_t n_out, int32_t n_in) {
+  LinearPlan p{};
+  p.n_tile = n_tokens >= kMaxTok ? kMaxTok : ((n_tokens + 15) / 16) * 16;
+  p.tok_tiles = (n_tokens + kMaxTok - 1) / kMaxTok;
+  const int stage = kABytes + ((p.n_tile * 128 + 1023) & ~1023);
+  p.stages = kRingBudget / stage;
+  if (p.stages > kMaxStages) p.stages = kMaxStages;
+  p.smem = 1024 + static_cast<size_t>(p.stages) * stage + sizeof(LinearCtl);
+  p.acc_cols = 32;
+  while (static_cast<int>(p.acc_cols) < p.n_tile) p.acc_cols <<= 1;
+  const int chunks = n_in / kChunkK;
+  const int64_t tiles = static_cast<int64_t>((n_out + 127) / 128) * p.tok_tiles;
+  const int64_t sms = device_sm_count();
+  double best = 1e300;
+  p.splits = 1;
+  for (int s = 1; s <= kMaxSplits && s <= chunks; ++s) {
+    const int per = (chunks + s - 1) / s;
+    if (s > 1 && per < 8) break;
+    const int64_t per_cta = (tiles * s + sms - 1) / sms;
+    const double cost = static_cast<double>(per_cta) * (per + (s > 1 ? 1.0 : 0.0));
+    if (cost < best - 1e-9) {
+      best = cost;
+      p.splits = s;
+    }
+  }
+  const int64_t units = tiles * p.splits;
+  p.units = static_cast<int>(units);
+  p.grid = static_cast<int>(units < sms ? units : sms);
+  return p;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+int32_t linear_splits(int32_t n_tokens, int32_t n_out, int32_t n_in, mla_dtype_t act) {
+  if (n_tokens < 1 || n_out < 1 || n_in < 1 || !use_tc(n_in, act)) return 1;
+  return plan_tc(n_tokens, n_out, n_in).splits;
+}
+
+size_t linear_partial_bytes(int32_t n_tokens, int32_t n_out, int32_t n_in, mla_dtype_t act) {
+  return align256(static_cast<size_t>(linear_splits(n_tokens, n_out, n_in, act)) * n_tokens * n_out *
+                  sizeof(float));
+}
+
+cudaError_t launch_linear(const LinearArgs& a, cudaStream_t s, bool reduce) {
+  if (a.n_tokens == 0) return cudaSuccess;
+  if (!use_tc(a.n_in, a.act)) {
+    if (a.k_splits != 1) return cudaErrorInvalidValue;
+    const dim3 grid((a.n_tokens + 7) / 8, (a.n_out + 7) / 8);
+    if (a.act == MLA_F32) return launch_pdl(linear_simt_kernel<float>, grid, dim3(256), 0, s, a);
+    return launch_pdl(linear_simt_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, a);
+  }
+  if (encoder() == nullptr) return cudaErrorNotSupported;
+  const LinearPlan pl = plan_tc(a.n_tokens, a.n_out, a.n_in);
+  if (pl.splits != a.k_splits || (pl.splits > 1 && a.part == nullptr)) return cudaErrorInvalidValue;
+  CUtensorMap am, bm;
+  if (!encode_2d(&am, a.w, static_cast<uint64_t>(a.n_out), static_cast<uint64_t>(a.n_in), 128) ||
+      !encode_2d(&bm, a.x, static_cast<uint64_t>(a.n_tokens), static_cast<uint64_t>(a.n_in),
+                 static_cast<uint32_t>(pl.n_tile)))
+    return cudaErrorInvalidValue;
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (attr_dev != dev) {
+    e = cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_dev = dev;
+  }
+  e = launch_pdl(linear_tc_kernel, dim3(pl.grid), dim3(kThreads), pl.smem, s, am, bm, a, pl.n_tile, pl.stages,
+                 pl.acc_cols, pl.units);
+  if (e != cudaSuccess || a.part == nullptr || !reduce) return e;
+  const int64_t n = static_cast<int64_t>(a.n_tokens) * a.n_out;
+  return launch_pdl(linear_reduce_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256),
+                    0, s, a);
+}
+
+}  // namespace mla

@@ -1,53 +1,17 @@
-// The attention block's output projection with W_UV folded into W_O
+// Load-time fold of the value up-projection into the output projection
 // ("Model Architecture Driving Inference Systems" §3.2, pre-fused
 // W~^O_i = W^O_i W^UV_i, and §4.2, fused when the model is loaded;
 // "Multi-Head Latent Attention (MLA)" page, "Value Output Matrix Absorption"):
 //
-//   fuse_weights : W~[m][h][c] = sum_e W_O[m][h][e] W_UV[h][e][c]   (once, CUDA cores)
-//   out_fused    : y[t][m]     = sum_k W~[m][k] u[t][k],  k = (h, c), K = 512 H
+//   W~[m][h][c] = sum_e W_O[m][h][e] W_UV[h][e][c]
 //
-// out_fused is a GEMM with K = 65,536 at 128 heads and only the decode batch
-// as N, so W~ (d_model x K bf16: 940 MB at d_model = 7168) is streamed from HBM
-// once and nothing else matters. The tcgen05 kernel takes 128 rows of W~ as
-// the MMA M dimension and up to 256 tokens as N, and splits K so that there
-// are enough work units (row tile x K split x token tile) for every SM. It is
-// persistent, one CTA per SM: a producer warp streams all of the CTA's units
-// through one TMA ring of 64-wide K chunks (a 128 x 64 box of W~ and an n x 64
-// box of u, both 128-byte swizzled) without a break between units, an MMA warp
-// accumulates each unit in one of two TMEM buffers, and four epilogue warps
-// empty the other. The fp32 partial sums of the splits go to the workspace and
-// a second kernel adds them in split order, so the result does not depend on
-// timing.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <math_constants.h>
-
+// Run once, on CUDA cores; the per-step product y = W~ u is the generic linear
+// layer of linear.cu.
 #include "common.cuh"
 #include "launchers.h"
-#include "tc_ptx.cuh"
 
 namespace mla {
 namespace {
-
-using namespace tc;
-
-constexpr int kThreads = 192;      // producer warp, MMA warp, four epilogue warps
-constexpr int kMaxTok = 256;       // tokens per unit (MMA N)
-constexpr int kChunkK = 64;        // K elements per TMA box (128 bytes of bf16)
-constexpr int kABytes = 128 * 128;  // one W~ box: 128 rows x 64 bf16
-constexpr int kMaxStages = 12;
-constexpr int kMaxSplits = 32;
-constexpr int kRingBudget = 200 * 1024;  // shared memory for the TMA ring
-
-struct FusedCtl {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
-  uint64_t drain;
-  uint32_t tmem_base;
-  int32_t abort_flag;
-};
 
 // ------------------------------------------------------------------ fold (load time)
 
@@ -105,374 +69,12 @@ __global__ void __launch_bounds__(256) fuse_weights_kernel(FuseWeightsArgs a) {
   }
 }
 
-// ------------------------------------------------------------------ y = u W~^T, CUDA cores
-
-// grid (ceil(n/8), ceil(d/8)), block 256: warp = one row m of W~ against 8
-// tokens; lanes stride K. Any dtype and d_model.
-template <typename T>
-__global__ void __launch_bounds__(256) out_fused_simt_kernel(FusedOutArgs p) {
-  pdl_trigger();
-  pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m = blockIdx.y * 8 + warp;
-  const int t0 = blockIdx.x * 8;
-  if (m >= p.d_model) return;
-  const int64_t K = static_cast<int64_t>(p.heads) * kDC;
-  const int nt = min(8, p.n_tokens - t0);
-  const T* w = static_cast<const T*>(p.w) + static_cast<int64_t>(m) * K;
-  const T* u = static_cast<const T*>(p.u) + static_cast<int64_t>(t0) * K;
-  float acc[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-  for (int64_t k = lane; k < K; k += 32) {
-    const float wv = ActIO<T>::load(w + k);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < nt) acc[j] = fmaf(wv, ActIO<T>::load(u + j * K + k), acc[j]);
-  }
-  T* y = static_cast<T*>(p.y);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float s = warp_sum(acc[j]);
-    if (lane == 0 && j < nt) ActIO<T>::store(y + static_cast<int64_t>(t0 + j) * p.d_model + m, s);
-  }
-}
-
-// ------------------------------------------------------------------ y = u W~^T, tcgen05
-
-// A work unit is (128 rows of W~, K split, token tile). The unit's coordinates.
-struct Unit {
-  int m0, split, t0, c_lo, nc;
-};
-
-__device__ __forceinline__ Unit unit_at(const FusedOutArgs& p, int u, int m_tiles, int chunks) {
-  Unit r;
-  const int rest = u / m_tiles;
-  r.m0 = (u - rest * m_tiles) * 128;
-  r.split = rest % p.k_splits;
-  r.t0 = (rest / p.k_splits) * kMaxTok;
-  r.c_lo = static_cast<int>(static_cast<int64_t>(r.split) * chunks / p.k_splits);
-  r.nc = static_cast<int>(static_cast<int64_t>(r.split + 1) * chunks / p.k_splits) - r.c_lo;
-  return r;
-}
-
-// Persistent: grid = min(units, SMs), one CTA per SM, CTA c takes units c, c + G,
-// c + 2G, ... Warp 0 (one lane) streams every chunk of those units through the
-// TMA ring without a break between units; warp 1 (one lane) issues the MMAs
-// into one of two TMEM accumulators; warps 2-5 read back the other (warp w owns
-// TMEM lanes 32 (w % 4) .. +32, thread = row of W~) and write the unit's output.
-__global__ void __launch_bounds__(kThreads, 1) out_fused_tc_kernel(const __grid_constant__ CUtensorMap amap,
-                                                                   const __grid_constant__ CUtensorMap bmap,
-                                                                   FusedOutArgs p, int n_tile, int stages,
-                                                                   uint32_t acc_cols, int units) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int b_bytes = n_tile * 128;
-  const int stage_bytes = kABytes + ((b_bytes + 1023) & ~1023);
-  FusedCtl* ctl = reinterpret_cast<FusedCtl*>(base + stages * stage_bytes);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tiles = p.d_model / 128;
-  const int chunks = p.heads * (kDC / kChunkK);
-  pdl_trigger();
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&ctl->acc_full[b]), 1);
-      mbar_init(smem_u32(&ctl->acc_empty[b]), 4);  // the four epilogue warps
-    }
-    mbar_init(smem_u32(&ctl->drain), 1);
-    ctl->abort_flag = 0;
-    fence_mbar_init_cluster();
-    prefetch_tmap(&amap);
-    prefetch_tmap(&bmap);
-  }
-  if (warp == 0) tmem_alloc(smem_u32(&ctl->tmem_base), 2 * acc_cols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = ctl->tmem_base;
-  volatile int32_t* abort_flag = &ctl->abort_flag;
-  // W~ may have been written by the kernel just before this one (the fold), so
-  // nothing is loaded before the wait for the previous kernels.
-  pdl_wait();
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---- TMA producer. W~ is read once when all tokens fit one tile (u then stays in L2).
-      const bool once = p.n_tokens <= kMaxTok;
-      const uint64_t pol = l2_policy_evict_first();
-      uint32_t g = 0;  // chunks issued so far, over all of this CTA's units
-      bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = unit_at(p, u, m_tiles, chunks);
-        for (int k = 0; k < w.nc; ++k, ++g) {
-          const int s = static_cast<int>(g % stages);
-          if (g >= static_cast<uint32_t>(stages) &&
-              !mbar_wait<2>(smem_u32(&ctl->empty[s]), ((g / stages) & 1) ^ 1, abort_flag, nullptr)) {
-            ok = false;
-            break;
-          }
-          const uint32_t dst = smem_u32(base + s * stage_bytes);
-          const uint32_t bar = smem_u32(&ctl->full[s]);
-          const int32_t x = (w.c_lo + k) * kChunkK;
-          mbar_arrive_expect_tx(bar, kABytes + b_bytes);
-          if (once)
-            tma_load_2d(dst, &amap, bar, x, w.m0, pol);
-          else
-            tma_load_2d_nohint(dst, &amap, bar, x, w.m0);
-          tma_load_2d_nohint(dst + kABytes, &bmap, bar, x, w.t0);  // token rows past n read as zero
-        }
-      }
-      if (!ok) {
-        // after an abort nobody consumes: let the last copy issued into each slot land
-        volatile int32_t never = 0;
-        const uint32_t first = g > static_cast<uint32_t>(stages) ? g - stages : 0;
-        for (uint32_t q = first; q < g; ++q)
-          mbar_wait<2>(smem_u32(&ctl->full[q % stages]), (q / stages) & 1, &never, nullptr);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---- MMA issuer
-      const uint32_t idesc = idesc_bf16_f32(128, n_tile, false, false);
-      uint32_t g = 0;
-      bool ok = true;
-      int i = 0;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
-        const Unit w = unit_at(p, u, m_tiles, chunks);
-        const int b = i & 1;
-        if (i >= 2 && !mbar_wait<2>(smem_u32(&ctl->acc_empty[b]), ((i >> 1) - 1) & 1, abort_flag, nullptr)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(b) * acc_cols;
-        for (int k = 0; k < w.nc; ++k, ++g) {
-          const int s = static_cast<int>(g % stages);
-          if (!mbar_wait<2>(smem_u32(&ctl->full[s]), (g / stages) & 1, abort_flag, nullptr)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(base + s * stage_bytes);
-          const uint64_t db = sdesc_sw128(a0 + kABytes, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < kChunkK / 16; ++kk)
-            mma_ss(d, sdesc_sw128(a0 + kk * 32, 16, 1024), db + ((kk * 32) >> 4), idesc,
-                   (k > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&ctl->empty[s]));
-        }
-        if (ok) mma_commit(smem_u32(&ctl->acc_full[b]));
-      }
-      // every MMA this thread issued completes before the TMEM is freed
-      mma_commit(smem_u32(&ctl->drain));
-      volatile int32_t never = 0;
-      mbar_wait<2>(smem_u32(&ctl->drain), 0, &never, nullptr);
-    }
-  } else {
-    // ---- epilogue (warps 2-5)
-    const int q = warp & 3;
-    const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
-    bool ok = true;
-    int i = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
-      const Unit w = unit_at(p, u, m_tiles, chunks);
-      const int b = i & 1;
-      const bool got =
-          __all_sync(0xffffffffu, ok && mbar_wait<0>(smem_u32(&ctl->acc_full[b]), (i >> 1) & 1, abort_flag, nullptr));
-      ok = got;
-      tc_fence_after();
-      const int n_tok = min(kMaxTok, p.n_tokens - w.t0);
-      const int64_t col = w.m0 + q * 32 + lane;
-      for (int c = 0; c < n_tile; c += 32) {
-        float v[32];
-        if (got) {
-          tmem_ld32_sync(tmem + static_cast<uint32_t>(b) * acc_cols + lanes + c, v);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = 0.0f;
-        }
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int t = c + k;
-          if (t >= n_tok) break;
-          const float val = got ? v[k] : CUDART_NAN_F;  // an aborted unit reads as NaN, never as stale data
-          const int64_t row = w.t0 + t;
-          if (p.k_splits == 1)
-            static_cast<__nv_bfloat16*>(p.y)[row * p.d_model + col] = __float2bfloat16_rn(val);
-          else
-            p.part[(static_cast<int64_t>(w.split) * p.n_tokens + row) * p.d_model + col] = val;
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (got && lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[b]));
-    }
-  }
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 2 * acc_cols);
-  }
-}
-
-// y = sum over splits s = 0, 1, ... of part[s], four consecutive outputs per thread.
-template <typename T>
-__global__ void __launch_bounds__(256) out_fused_reduce_kernel(FusedOutArgs p) {
-  pdl_trigger();
-  pdl_wait();
-  const int64_t n4 = static_cast<int64_t>(p.n_tokens) * p.d_model / 4;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
-  if (i >= n4) return;
-  const float4* src = reinterpret_cast<const float4*>(p.part) + i;
-  float4 acc = src[0];
-  for (int s = 1; s < p.k_splits; ++s) {
-    const float4 v = src[s * n4];
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
-  }
-  T* y = static_cast<T*>(p.y) + 4 * i;
-  ActIO<T>::store(y, acc.x);
-  ActIO<T>::store(y + 1, acc.y);
-  ActIO<T>::store(y + 2, acc.z);
-  ActIO<T>::store(y + 3, acc.w);
-}
-
-// ------------------------------------------------------------------ host side
-
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// 2D map over a [rows][cols] bf16 matrix, boxes of 64 columns x box_rows.
-bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool use_tc(int32_t d_model, mla_dtype_t act) { return act == MLA_BF16 && d_model % 128 == 0; }
-
-struct FusedPlan {
-  int n_tile;         // MMA N (tokens per unit, multiple of 16)
-  int tok_tiles;      // units along the tokens
-  int stages;         // TMA ring depth
-  int splits;         // units along K
-  int units;          // M tiles x splits x token tiles
-  int grid;           // persistent CTAs: min(units, SMs)
-  size_t smem;        // dynamic shared memory per CTA
-  uint32_t acc_cols;  // TMEM columns of one of the two accumulators
-};
-
-// Tile shape, ring depth and K split of the persistent tcgen05 kernel. One CTA
-// per SM streams its units back to back, so the split count minimises the
-// chunks the busiest CTA streams: units per CTA (rounded up) x (chunks per unit
-// + about one chunk's worth of partial-sum traffic).
-FusedPlan plan_tc(int32_t n_tokens, int32_t d_model, int32_t heads) {
-  FusedPlan p{};
-  p.n_tile = n_tokens >= kMaxTok ? kMaxTok : ((n_tokens + 15) / 16) * 16;
-  p.tok_tiles = (n_tokens + kMaxTok - 1) / kMaxTok;
-  const int stage = kABytes + ((p.n_tile * 128 + 1023) & ~1023);
-  p.stages = kRingBudget / stage;
-  if (p.stages > kMaxStages) p.stages = kMaxStages;
-  p.smem = 1024 + static_cast<size_t>(p.stages) * stage + sizeof(FusedCtl);
-  p.acc_cols = 32;
-  while (static_cast<int>(p.acc_cols) < p.n_tile) p.acc_cols <<= 1;
-  const int chunks = heads * (kDC / kChunkK);
-  const int64_t tiles = static_cast<int64_t>(d_model / 128) * p.tok_tiles;
-  const int64_t sms = device_sm_count();
-  double best = 1e300;
-  p.splits = 1;
-  for (int s = 1; s <= kMaxSplits && s <= chunks; ++s) {
-    const int per = (chunks + s - 1) / s;
-    if (s > 1 && per < 8) break;
-    const int64_t per_cta = (tiles * s + sms - 1) / sms;
-    const double cost = static_cast<double>(per_cta) * (per + (s > 1 ? 1.0 : 0.0));
-    if (cost < best - 1e-9) {
-      best = cost;
-      p.splits = s;
-    }
-  }
-  const int64_t units = tiles * p.splits;
-  p.units = static_cast<int>(units);
-  p.grid = static_cast<int>(units < sms ? units : sms);
-  return p;
-}
-
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
 }  // namespace
-
-int32_t out_fused_splits(int32_t n_tokens, int32_t d_model, int32_t heads, mla_dtype_t act) {
-  if (n_tokens < 1 || d_model < 1 || heads < 1 || !use_tc(d_model, act)) return 1;
-  return plan_tc(n_tokens, d_model, heads).splits;
-}
-
-size_t out_fused_workspace_bytes(int32_t n_tokens, int32_t d_model, int32_t heads, mla_dtype_t act) {
-  const int32_t s = out_fused_splits(n_tokens, d_model, heads, act);
-  if (s <= 1) return 0;
-  return align256(static_cast<size_t>(s) * n_tokens * d_model * sizeof(float));
-}
 
 cudaError_t launch_fuse_weights(const FuseWeightsArgs& a, cudaStream_t s) {
   const dim3 grid(kDC / 64, (a.d_model + 63) / 64, a.heads);
   if (a.act == MLA_F32) return launch_pdl(fuse_weights_kernel<float>, grid, dim3(256), 0, s, a);
   return launch_pdl(fuse_weights_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, a);
-}
-
-cudaError_t launch_out_fused(const FusedOutArgs& a, cudaStream_t s) {
-  if (a.n_tokens == 0) return cudaSuccess;
-  if (!use_tc(a.d_model, a.act)) {
-    const dim3 grid((a.n_tokens + 7) / 8, (a.d_model + 7) / 8);
-    if (a.act == MLA_F32) return launch_pdl(out_fused_simt_kernel<float>, grid, dim3(256), 0, s, a);
-    return launch_pdl(out_fused_simt_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, a);
-  }
-  if (encoder() == nullptr) return cudaErrorNotSupported;
-  const FusedPlan pl = plan_tc(a.n_tokens, a.d_model, a.heads);
-  if (pl.splits != a.k_splits || (pl.splits > 1 && a.part == nullptr)) return cudaErrorInvalidValue;
-  CUtensorMap am, bm;
-  const uint64_t K = static_cast<uint64_t>(a.heads) * kDC;
-  if (!encode_2d(&am, a.w, static_cast<uint64_t>(a.d_model), K, 128) ||
-      !encode_2d(&bm, a.u, static_cast<uint64_t>(a.n_tokens), K, static_cast<uint32_t>(pl.n_tile)))
-    return cudaErrorInvalidValue;
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (attr_dev != dev) {
-    e = cudaFuncSetAttribute(out_fused_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
-  e = launch_pdl(out_fused_tc_kernel, dim3(pl.grid), dim3(kThreads), pl.smem, s, am, bm, a, pl.n_tile, pl.stages,
-                 pl.acc_cols, pl.units);
-  if (e != cudaSuccess || pl.splits == 1) return e;
-  const int64_t n4 = static_cast<int64_t>(a.n_tokens) * a.d_model / 4;
-  return launch_pdl(out_fused_reduce_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>((n4 + 255) / 256)),
-                    dim3(256), 0, s, a);
 }
 
 }  // namespace mla

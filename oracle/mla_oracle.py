@@ -484,3 +484,10 @@ def decode_front(h, w_dq, g_q, w_uq, w_qr, w_dkv, g_kv, w_kr, positions, eps: fl
     c_kv = rms_norm(h @ np.asarray(w_dkv, np.float64).T, g_kv, eps)
     k_r = h @ np.asarray(w_kr, np.float64).T
     return q_nope, q_rope, c_kv, k_r
+
+
+def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """y[..., o] = sum_i w[o, i] x[..., i]: a bias-free nn.Linear with weight
+    w [out, in] ([P2] "PyTorch Reference Implementation" declares every
+    projection so)."""
+    return np.asarray(x, np.float64) @ np.asarray(w, np.float64).T

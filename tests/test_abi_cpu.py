@@ -107,6 +107,35 @@ def test_fused_projection_validation(capi):
     assert need > 0 and need % 256 == 0 and need % (32 * 7168 * 4) == 0
     assert L.mla_out_proj_fused(16, 16, 16, 32, 7168, None, 0, D, capi.MLA_BF16, None) == \
         capi.MLA_ERR_WORKSPACE_TOO_SMALL
-    # the CUDA-core shapes never split K
-    assert capi.mla_out_proj_fused_workspace_size(32, 7000, 128) == 0
+    # the CUDA-core shapes (fp32, or n_in not a multiple of 64) never split K
     assert capi.mla_out_proj_fused_workspace_size(32, 7168, 128, "f32") == 0
+    assert capi.mla_linear_workspace_size(32, 7000, 100) == 0
+    assert capi.mla_linear_workspace_size(32, 7000, 7168) % (32 * 7000 * 4) == 0
+
+
+def test_linear_and_front_validation(capi):
+    L = capi.load()
+    D = capi.dims(128)
+    assert L.mla_linear(16, 16, 16, 4, 0, 64, None, 0, capi.MLA_BF16, None) == capi.MLA_ERR_INVALID_ARG
+    assert L.mla_linear(16, 16, 16, 4, 64, 64, None, 0, capi.MLA_E4M3, None) == capi.MLA_ERR_UNSUPPORTED
+    assert L.mla_linear(16, 16, 24, 4, 64, 64, None, 0, capi.MLA_BF16, None) == capi.MLA_ERR_INVALID_ARG
+    assert L.mla_linear(None, None, None, 0, 64, 64, None, 0, capi.MLA_BF16, None) == capi.MLA_OK
+    assert L.mla_linear(16, 16, 16, 32, 2112, 7168, None, 0, capi.MLA_BF16, None) == capi.MLA_ERR_WORKSPACE_TOO_SMALL
+    args = [16] * 8
+    ok = dict(max_pos=100, eps=1e-6, n=4, d=7168, dcq=1536)
+
+    def front(max_pos=100, eps=1e-6, n=4, d=7168, dcq=1536, ws=16, ws_bytes=1 << 30, act=capi.MLA_BF16, outs=16):
+        return L.mla_decode_front(*args, max_pos, eps, n, d, dcq, outs, 16, 16, 16, ws, ws_bytes, None, D, act, None)
+
+    assert front(max_pos=0) == capi.MLA_ERR_INVALID_ARG
+    assert front(eps=-1.0) == capi.MLA_ERR_INVALID_ARG
+    assert front(eps=float("nan")) == capi.MLA_ERR_INVALID_ARG
+    assert front(dcq=0) == capi.MLA_ERR_INVALID_ARG
+    assert front(act=capi.MLA_E4M3) == capi.MLA_ERR_UNSUPPORTED
+    assert front(outs=None) == capi.MLA_ERR_INVALID_ARG
+    assert front(outs=24) == capi.MLA_ERR_INVALID_ARG
+    assert front(ws_bytes=16) == capi.MLA_ERR_WORKSPACE_TOO_SMALL
+    assert front(n=0) == capi.MLA_OK
+    # workspace: the fp32 sums of both products plus c_q
+    need = capi.mla_decode_front_workspace_size(32, 7168, 1536, 128)
+    assert need >= 32 * (2112 + 24576) * 4 + 32 * 1536 * 2

@@ -99,3 +99,12 @@ def test_front_pins_catch_planted_mistakes():
     x = a["h"] @ a["w_dkv"].T
     bad_n = x / np.mean(np.abs(x), -1, keepdims=True) * a["g_kv"]
     assert not np.allclose(bad_n, good[2])
+
+
+def test_linear_by_loops():
+    rng = np.random.default_rng(5)
+    x, w = rng.standard_normal((3, 7)), rng.standard_normal((4, 7))
+    y = O.linear(x, w)
+    for t in range(3):
+        for o in range(4):
+            assert abs(y[t, o] - math.fsum(w[o, i] * x[t, i] for i in range(7))) <= 1e-14
