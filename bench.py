@@ -580,40 +580,23 @@ def run_layer(args):
     pos = d["ctx_positions"][ni].cuda()
     slots = d["ctx_slots"][ni].cuda()
     h = fr["h"].cuda()
-    w_dqkv = torch.cat([fr["w_dq"], fr["w_dkv"], fr["w_kr"]], 0).cuda()
-    w_uqr = torch.cat([fr["w_uq"], fr["w_qr"]], 0).cuda()
-    g_q, g_kv = fr["g_q"].cuda(), fr["g_kv"].cuda()
-    w_o_dev = w_o.cuda()
-    w_f = capi.mla_fuse_out_weights(w_o_dev, layer.w_uv)
-    w_o2 = w_o_dev.view(d_model, H * 128)
-    ws_front = torch.empty(capi.mla_decode_front_workspace_size(n, d_model, d_cq, H), dtype=torch.uint8,
-                           device="cuda")
-    ws_f = torch.empty(max(16, capi.mla_out_proj_fused_workspace_size(n, d_model, H)), dtype=torch.uint8,
-                       device="cuda")
-    ws_o = torch.empty(max(16, capi.mla_linear_workspace_size(n, d_model, H * 128)), dtype=torch.uint8,
-                       device="cuda")
-    bf = dict(dtype=torch.bfloat16, device="cuda")
-    q_nope, q_rope = torch.empty(n, H, 128, **bf), torch.empty(n, H, 64, **bf)
-    c_kv, k_r = torch.empty(n, 512, **bf), torch.empty(n, 64, **bf)
-    y = torch.empty(n, d_model, **bf)
+    layer.attach_front(fr["w_dq"], fr["w_dkv"], fr["w_kr"], fr["g_q"], fr["g_kv"], fr["w_uq"], fr["w_qr"], W.RMS_EPS)
+    # the same layer twice over one cache: the output projection fused, and unfused
+    import copy
+    unf = copy.copy(layer)
+    unf.attach_output(w_o, fused=False)
+    layer.attach_output(w_o, fused=True)
+    y = layer.y
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     assert layer.device_error() == 0
 
-    def attend():
-        capi.mla_decode_front(h, w_dqkv, g_q, g_kv, w_uqr, pos, layer.rope_cos, layer.rope_sin, W.RMS_EPS, H,
-                              q_nope, q_rope, c_kv, k_r, ws_front, layer.dev_error)
-        layer.append(c_kv, k_r, pos, slots)
-        q_lat = layer.absorb(q_nope.view(w.batch, w.q_len, H, 128))
-        return layer.decode(q_lat, q_rope.view(w.batch, w.q_len, H, 64))[0]
-
     def step_fused():
-        capi.mla_out_proj_fused(attend(), w_f, y.view(w.batch, w.q_len, d_model), ws_f)
+        layer.step_from_hidden(h, pos, slots)
 
     def step_unfused():
-        o = layer.out_proj(attend())
-        capi.mla_linear(o.view(n, H * 128), w_o2, y, ws_o)
+        unf.step_from_hidden(h, pos, slots)
 
     g_fused = layer.capture(step_fused)
     g_unfused = layer.capture(step_unfused)

@@ -9,6 +9,11 @@ decode step is
 
 exactly the four calls of the library, on one stream, with no allocation in
 the step once the buffers exist.
+
+With the model-level weights attached (attach_front, attach_output), a step can
+start from the hidden states of the new tokens and end in the model dimension:
+
+    decode_front(h) -> append -> absorb_q -> decode_paged -> out_proj_fused (or out_proj, W_O)
 """
 from __future__ import annotations
 
@@ -100,6 +105,74 @@ class MLADecodeLayer:
         q_lat = self.absorb(q_nope, stream)
         u, _ = self.decode(q_lat, q_rope, stream)
         return self.out_proj(u, stream)
+
+    # ------------------------------------------------------------------ model-level weights
+
+    def attach_front(self, w_dq, w_dkv, w_kr, g_q, g_kv, w_uq, w_qr, eps: float):
+        """Front-end weights (nn.Linear layouts [out, in]) and RMSNorm gains. The
+        three down-projections and the two query up-projections are stacked once
+        here, as mla_decode_front takes them; its workspace and outputs are
+        allocated for the layer's B*Lq tokens."""
+        dev = self.device
+        self.w_dqkv = torch.cat([w_dq, w_dkv, w_kr], 0).to(dev).contiguous()
+        self.w_uqr = torch.cat([w_uq, w_qr], 0).to(dev).contiguous()
+        self.g_q = g_q.to(dev).contiguous()
+        self.g_kv = g_kv.to(dev).contiguous()
+        self.rms_eps = float(eps)
+        n = self.w.batch * self.w.q_len
+        d_model, d_cq = w_dq.shape[1], w_dq.shape[0]
+        act = self.w.act_dtype
+        self.front_ws = torch.empty(max(16, capi.mla_decode_front_workspace_size(n, d_model, d_cq, self.H, act)),
+                                    dtype=torch.uint8, device=dev)
+        mk = lambda *shape: torch.empty(*shape, dtype=self.act, device=dev)
+        self.q_nope_buf, self.q_rope_buf = mk(n, self.H, 128), mk(n, self.H, 64)
+        self.c_kv_buf, self.k_r_buf = mk(n, 512), mk(n, 64)
+
+    def attach_output(self, w_o, fused: bool = True):
+        """The output projection W_O [d_model, H, 128]. fused=True folds W_UV
+        into it once (mla_fuse_out_weights) and a step ends with one product over
+        all heads; fused=False keeps W_UV per head and applies W_O to the
+        concatenated head outputs."""
+        dev = self.device
+        n = self.w.batch * self.w.q_len
+        d_model = w_o.shape[0]
+        act = self.w.act_dtype
+        self.out_fused = fused
+        w_o = w_o.to(dev).contiguous()
+        if fused:
+            self.w_out = capi.mla_fuse_out_weights(w_o, self.w_uv)
+            need = capi.mla_out_proj_fused_workspace_size(n, d_model, self.H, act)
+        else:
+            self.w_out = w_o.view(d_model, self.H * 128)
+            need = capi.mla_linear_workspace_size(n, d_model, self.H * 128, act)
+        self.out_ws = torch.empty(max(16, need), dtype=torch.uint8, device=dev)
+        self.y = torch.empty(self.w.batch, self.w.q_len, d_model, dtype=self.act, device=dev)
+
+    def front(self, h, positions, stream=None):
+        """decode_front: h [B*Lq, d_model] -> (q_nope, q_rope, c_kv, k_r) in the layer's buffers."""
+        return capi.mla_decode_front(h, self.w_dqkv, self.g_q, self.g_kv, self.w_uqr, positions, self.rope_cos,
+                                     self.rope_sin, self.rms_eps, self.H, self.q_nope_buf, self.q_rope_buf,
+                                     self.c_kv_buf, self.k_r_buf, self.front_ws, self.dev_error, stream)
+
+    def output(self, u, stream=None):
+        """u [B, Lq, H, 512] -> y [B, Lq, d_model] through the attached output projection."""
+        if self.out_fused:
+            return capi.mla_out_proj_fused(u, self.w_out, self.y, self.out_ws, stream)
+        o = self.out_proj(u, stream)
+        capi.mla_linear(o.view(-1, self.H * 128), self.w_out, self.y.view(-1, self.y.shape[-1]), self.out_ws,
+                        stream)
+        return self.y
+
+    def step_from_hidden(self, h, positions, slots, stream=None):
+        """One whole layer step: front end on the new tokens' hidden states, their
+        rows appended at `slots`, absorbed paged decode, output projection.
+        Returns y [B, Lq, d_model]."""
+        B, Lq = self.w.batch, self.w.q_len
+        q_nope, q_rope, c_kv, k_r = self.front(h, positions, stream)
+        self.append(c_kv, k_r, positions, slots, stream)
+        q_lat = self.absorb(q_nope.view(B, Lq, self.H, 128), stream)
+        u, _ = self.decode(q_lat, q_rope.view(B, Lq, self.H, 64), stream)
+        return self.output(u, stream)
 
     def device_error(self) -> int:
         return capi.mla_read_device_error(self.dev_error)

@@ -117,13 +117,14 @@ def test_front_bad_position_flags_and_zeroes():
     assert_close(f64(q_nope), ref[0], what="q_nope")
 
 
-def test_decode_layer_end_to_end():
-    """One decode step of a whole layer from the hidden states. GPU: front end
-    -> append of the new tokens -> absorb -> paged decode -> fused output
-    projection. Oracle: its own front end, the new tokens' rows appended to its
-    cache, K and V materialised per head, softmax, W_O over the heads."""
+@pytest.mark.parametrize("fused", [True, False], ids=["fused_output", "unfused_output"])
+def test_decode_layer_end_to_end(fused):
+    """One decode step of a whole layer from the hidden states, through the
+    layer API. GPU: front end -> append of the new tokens -> absorb -> paged
+    decode -> output projection (W_UV folded into W_O, or W_UV per head then
+    W_O). Oracle: its own front end, the new tokens' rows appended to its cache,
+    K and V materialised per head, softmax, W_O over the concatenated heads."""
     W = _W()
-    C = _C()
     from mla_latent_kv_16_gb300.engine import build_layer
     w = W.preset("dsv3_bf16", batch=3, seq_lens=[4096, 700, 129])
     d = W.make_inputs(w)
@@ -131,14 +132,11 @@ def test_decode_layer_end_to_end():
     fr = W.make_front_inputs(w, d_model, d_cq)
     w_o = W.make_out_weight(w, d_model)
     layer = build_layer(w, d)  # context without the step's new tokens
+    layer.attach_front(fr["w_dq"], fr["w_dkv"], fr["w_kr"], fr["g_q"], fr["g_kv"], fr["w_uq"], fr["w_qr"], W.RMS_EPS)
+    layer.attach_output(w_o, fused=fused)
     ni = d["new_index"]
     pos = d["ctx_positions"][ni].contiguous()
-    q_nope, q_rope, c_kv, k_r = _run_front(fr, pos, w.max_pos, w.heads)
-    layer.append(c_kv, k_r, pos.cuda(), d["ctx_slots"][ni].cuda())
-    q_lat = layer.absorb(q_nope.view(w.batch, w.q_len, w.heads, 128))
-    u, _ = layer.decode(q_lat, q_rope.view(w.batch, w.q_len, w.heads, 64))
-    w_f = C.mla_fuse_out_weights(w_o.cuda(), layer.w_uv)
-    y = f64(C.mla_out_proj_fused(u, w_f))
+    y = f64(layer.step_from_hidden(fr["h"].cuda(), pos.cuda(), d["ctx_slots"][ni].cuda()))
     torch.cuda.synchronize()
     assert layer.device_error() == 0
     # oracle: front end in fp64; the new rows enter its cache in the activation type
