@@ -74,6 +74,20 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// sum over s = 0 .. splits-1 of part[s * stride + i], added left to right in
+// split order; the loads are issued four at a time so that they overlap.
+__device__ __forceinline__ float split_sum(const float* part, int64_t i, int64_t stride, int splits) {
+  float a = part[i];
+  int s = 1;
+  for (; s + 3 < splits; s += 4) {
+    const float b0 = part[s * stride + i], b1 = part[(s + 1) * stride + i];
+    const float b2 = part[(s + 2) * stride + i], b3 = part[(s + 3) * stride + i];
+    a = (((a + b0) + b1) + b2) + b3;
+  }
+  for (; s < splits; ++s) a += part[s * stride + i];
+  return a;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -41,26 +41,22 @@ FrontLayout front_layout(int32_t n, int32_t d_model, int32_t d_cq, int32_t heads
   return l;
 }
 
-// Sum over splits s of part[s][i] (stride = one split's n x rows), in split order.
-__device__ __forceinline__ float split_sum(const float* part, int64_t i, int64_t stride, int splits) {
-  float a = part[i];
-  for (int s = 1; s < splits; ++s) a += part[s * stride + i];
-  return a;
-}
+constexpr int kFinishThreads = 1024;
 
-// grid (n), block 256: token t's 1536 + 512 + 64 sums; the two mean squares in
+// grid (n), block 1024: token t's 1536 + 512 + 64 sums; the two mean squares in
 // a first pass over the (L2-resident) partials, the outputs in a second.
 template <typename T>
-__global__ void __launch_bounds__(256) front_finish_a_kernel(FrontArgs f, const float* part, int splits, T* c_q) {
+__global__ void __launch_bounds__(kFinishThreads) front_finish_a_kernel(FrontArgs f, const float* part, int splits,
+                                                                        T* c_q) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float red[2][8];
+  __shared__ float red[2][kFinishThreads / 32];
   const int t = blockIdx.x;
   const int ma = f.d_cq + kDC + kDRope;
   const int64_t stride = static_cast<int64_t>(f.n_tokens) * ma;
   const int64_t row = static_cast<int64_t>(t) * ma;
   float sq_q = 0.0f, sq_kv = 0.0f;
-  for (int i = threadIdx.x; i < f.d_cq + kDC; i += 256) {
+  for (int i = threadIdx.x; i < f.d_cq + kDC; i += kFinishThreads) {
     const float v = split_sum(part, row + i, stride, splits);
     if (i < f.d_cq)
       sq_q = fmaf(v, v, sq_q);
@@ -77,7 +73,7 @@ __global__ void __launch_bounds__(256) front_finish_a_kernel(FrontArgs f, const 
   __syncthreads();
   float tq = 0.0f, tkv = 0.0f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
+  for (int w = 0; w < kFinishThreads / 32; ++w) {
     tq += red[0][w];
     tkv += red[1][w];
   }
@@ -85,7 +81,7 @@ __global__ void __launch_bounds__(256) front_finish_a_kernel(FrontArgs f, const 
   const float inv_kv = 1.0f / sqrtf(tkv / static_cast<float>(kDC) + f.eps);
   const T* g_q = static_cast<const T*>(f.g_q);
   const T* g_kv = static_cast<const T*>(f.g_kv);
-  for (int i = threadIdx.x; i < ma; i += 256) {
+  for (int i = threadIdx.x; i < ma; i += kFinishThreads) {
     const float v = split_sum(part, row + i, stride, splits);
     if (i < f.d_cq) {
       ActIO<T>::store(c_q + static_cast<int64_t>(t) * f.d_cq + i, v * inv_q * ActIO<T>::load(g_q + i));
@@ -147,7 +143,8 @@ cudaError_t launch_front_t(const FrontArgs& f, cudaStream_t s) {
   LinearArgs a{f.h, f.w_dqkv, nullptr, part_a, f.n_tokens, l.ma, f.d_model, l.splits_a, f.act};
   cudaError_t e = launch_linear(a, s, false);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(front_finish_a_kernel<T>, dim3(f.n_tokens), dim3(256), 0, s, f, static_cast<const float*>(part_a),
+  e = launch_pdl(front_finish_a_kernel<T>, dim3(f.n_tokens), dim3(kFinishThreads), 0, s, f,
+                 static_cast<const float*>(part_a),
                  l.splits_a, c_q);
   if (e != cudaSuccess) return e;
   LinearArgs b{c_q, f.w_uqr, nullptr, part_b, f.n_tokens, l.mb, f.d_cq, l.splits_b, f.act};

@@ -281,9 +281,7 @@ __global__ void __launch_bounds__(256) linear_reduce_kernel(LinearArgs p) {
   const int64_t n = static_cast<int64_t>(p.n_tokens) * p.n_out;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
   if (i >= n) return;
-  float acc = p.part[i];
-  for (int s = 1; s < p.k_splits; ++s) acc += p.part[s * n + i];
-  ActIO<T>::store(static_cast<T*>(p.y) + i, acc);
+  ActIO<T>::store(static_cast<T*>(p.y) + i, split_sum(p.part, i, n, p.k_splits));
 }
 
 // ------------------------------------------------------------------ host side
