@@ -201,7 +201,8 @@ mla_status_t mla_linear(const void* x, const void* w, void* y, int32_t n_tokens,
   const size_t need = splits > 1 ? linear_partial_bytes(n_tokens, n_out, n_in, act) : 0;
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MLA_ERR_WORKSPACE_TOO_SMALL;
   if (need > 0 && !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
-  LinearArgs a{x, w, y, need > 0 ? static_cast<float*>(workspace) : nullptr, n_tokens, n_out, n_in, splits, act};
+  // W may be the output of mla_fuse_out_weights just before: nothing is read before the wait
+  LinearArgs a{x, w, y, need > 0 ? static_cast<float*>(workspace) : nullptr, n_tokens, n_out, n_in, splits, act, 0};
   return from_cuda(launch_linear(a, static_cast<cudaStream_t>(stream), true));
 }
 

@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kFinishThreads) front_finish_a_kernel(FrontArg
   }
 }
 
-// grid (ceil(mb / 512), n), block 256: one adjacent pair of outputs per thread.
+// grid (n, ceil(mb / 512)), block 256: one adjacent pair of outputs per thread.
 // Pairs in the first H*128 rows are q_nope; the rest are q_r, rotated by the
 // token's position in fp32 with every product and sum rounded separately, as
 // the cache append rotates k_R.
@@ -102,9 +102,9 @@ template <typename T>
 __global__ void __launch_bounds__(256) front_finish_b_kernel(FrontArgs f, const float* part, int splits) {
   pdl_trigger();
   pdl_wait();
-  const int t = blockIdx.y;
+  const int t = blockIdx.x;
   const int mb = f.heads * (kDNope + kDRope);
-  const int o = 2 * (blockIdx.x * 256 + threadIdx.x);
+  const int o = 2 * (blockIdx.y * 256 + threadIdx.x);
   if (o >= mb) return;
   const int64_t stride = static_cast<int64_t>(f.n_tokens) * mb;
   const int64_t row = static_cast<int64_t>(t) * mb;
@@ -140,17 +140,18 @@ cudaError_t launch_front_t(const FrontArgs& f, cudaStream_t s) {
   float* part_a = reinterpret_cast<float*>(ws);
   T* c_q = reinterpret_cast<T*>(ws + l.off_cq);
   float* part_b = reinterpret_cast<float*>(ws + l.off_b);
-  LinearArgs a{f.h, f.w_dqkv, nullptr, part_a, f.n_tokens, l.ma, f.d_model, l.splits_a, f.act};
+  // the weights are the caller's, written by no kernel of this library
+  LinearArgs a{f.h, f.w_dqkv, nullptr, part_a, f.n_tokens, l.ma, f.d_model, l.splits_a, f.act, 1};
   cudaError_t e = launch_linear(a, s, false);
   if (e != cudaSuccess) return e;
   e = launch_pdl(front_finish_a_kernel<T>, dim3(f.n_tokens), dim3(kFinishThreads), 0, s, f,
                  static_cast<const float*>(part_a),
                  l.splits_a, c_q);
   if (e != cudaSuccess) return e;
-  LinearArgs b{c_q, f.w_uqr, nullptr, part_b, f.n_tokens, l.mb, f.d_cq, l.splits_b, f.act};
+  LinearArgs b{c_q, f.w_uqr, nullptr, part_b, f.n_tokens, l.mb, f.d_cq, l.splits_b, f.act, 1};
   e = launch_linear(b, s, false);
   if (e != cudaSuccess) return e;
-  const dim3 grid((l.mb / 2 + 255) / 256, f.n_tokens);
+  const dim3 grid(f.n_tokens, (l.mb / 2 + 255) / 256);
   return launch_pdl(front_finish_b_kernel<T>, grid, dim3(256), 0, s, f, static_cast<const float*>(part_b),
                     l.splits_b);
 }

@@ -87,6 +87,8 @@ struct LinearArgs {
   int32_t n_in;
   int32_t k_splits;  // from linear_splits
   mla_dtype_t act;
+  int32_t w_static;  // 1: no kernel still running before this one writes W (its
+                     // first ring may be requested before griddepcontrol.wait)
 };
 // K splits for these sizes on the current device (1 on the CUDA-core path),
 // and the bytes of their fp32 sums [splits][n][n_out], 256-byte aligned.

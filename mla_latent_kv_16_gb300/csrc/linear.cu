@@ -52,38 +52,40 @@ struct LinearCtl {
 
 // ------------------------------------------------------------------ CUDA cores
 
-// grid (ceil(n/8), ceil(n_out/8)), block 256: warp = one row o of W against 8
-// tokens; lanes stride K. Writes y, or fp32 sums to part[0] when part is set.
+// grid (ceil(n_out/8), min(ceil(n/8), 65535)), block 256: warp = one row o of W
+// against 8 tokens at a time (token tiles strided by the grid's y extent);
+// lanes stride K. Writes y, or fp32 sums to part[0] when part is set.
 template <typename T>
 __global__ void __launch_bounds__(256) linear_simt_kernel(LinearArgs p) {
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int o = blockIdx.y * 8 + warp;
-  const int t0 = blockIdx.x * 8;
+  const int o = blockIdx.x * 8 + warp;
   if (o >= p.n_out) return;
   const int64_t K = p.n_in;
-  const int nt = min(8, p.n_tokens - t0);
   const T* w = static_cast<const T*>(p.w) + static_cast<int64_t>(o) * K;
-  const T* x = static_cast<const T*>(p.x) + static_cast<int64_t>(t0) * K;
-  float acc[8];
+  for (int t0 = blockIdx.y * 8; t0 < p.n_tokens; t0 += gridDim.y * 8) {
+    const int nt = min(8, p.n_tokens - t0);
+    const T* x = static_cast<const T*>(p.x) + static_cast<int64_t>(t0) * K;
+    float acc[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-  for (int64_t k = lane; k < K; k += 32) {
-    const float wv = ActIO<T>::load(w + k);
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int64_t k = lane; k < K; k += 32) {
+      const float wv = ActIO<T>::load(w + k);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < nt) acc[j] = fmaf(wv, ActIO<T>::load(x + j * K + k), acc[j]);
-  }
+      for (int j = 0; j < 8; ++j)
+        if (j < nt) acc[j] = fmaf(wv, ActIO<T>::load(x + j * K + k), acc[j]);
+    }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float s = warp_sum(acc[j]);
-    if (lane == 0 && j < nt) {
-      const int64_t idx = static_cast<int64_t>(t0 + j) * p.n_out + o;
-      if (p.part != nullptr)
-        p.part[idx] = s;
-      else
-        ActIO<T>::store(static_cast<T*>(p.y) + idx, s);
+    for (int j = 0; j < 8; ++j) {
+      const float s = warp_sum(acc[j]);
+      if (lane == 0 && j < nt) {
+        const int64_t idx = static_cast<int64_t>(t0 + j) * p.n_out + o;
+        if (p.part != nullptr)
+          p.part[idx] = s;
+        else
+          ActIO<T>::store(static_cast<T*>(p.y) + idx, s);
+      }
     }
   }
 }
@@ -146,34 +148,53 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   volatile int32_t* abort_flag = &ctl->abort_flag;
-  // W may have been written by the kernel just before this one (the fold), so
-  // nothing is loaded before the wait for the previous kernels.
-  pdl_wait();
+  // Everything below reads or writes data of earlier kernels, except W when the
+  // caller vouches that no kernel still running writes it (w_static): then the
+  // producer requests the first ring of W before its wait.
+  const bool producer = warp == 0 && lane == 0;
+  if (!producer) pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA producer. W is read once when all tokens fit one tile (x then stays in L2).
       const bool once = p.n_tokens <= kMaxTok;
       const uint64_t pol = l2_policy_evict_first();
+      auto load_w = [&](uint32_t dst, uint32_t bar, int32_t xk, int32_t o0) {
+        if (once)
+          tma_load_2d(dst, &amap, bar, xk, o0, pol);  // rows past n_out read as zero
+        else
+          tma_load_2d_nohint(dst, &amap, bar, xk, o0);
+      };
+      uint32_t pre = 0;  // chunks whose W box was requested before the wait
+      if (p.w_static) {
+        for (int u = blockIdx.x; u < units && pre < static_cast<uint32_t>(stages); u += gridDim.x) {
+          const Unit w = unit_at(p, u, o_tiles, chunks);
+          for (int k = 0; k < w.nc && pre < static_cast<uint32_t>(stages); ++k, ++pre) {
+            const uint32_t bar = smem_u32(&ctl->full[pre]);
+            mbar_arrive_expect_tx(bar, kABytes + b_bytes);
+            load_w(smem_u32(base + pre * stage_bytes), bar, (w.c_lo + k) * kChunkK, w.o0);
+          }
+        }
+      }
+      pdl_wait();
       uint32_t g = 0;  // chunks issued so far, over all of this CTA's units
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit w = unit_at(p, u, o_tiles, chunks);
         for (int k = 0; k < w.nc; ++k, ++g) {
           const int s = static_cast<int>(g % stages);
-          if (g >= static_cast<uint32_t>(stages) &&
-              !mbar_wait<2>(smem_u32(&ctl->empty[s]), ((g / stages) & 1) ^ 1, abort_flag, nullptr)) {
-            ok = false;
-            break;
-          }
           const uint32_t dst = smem_u32(base + s * stage_bytes);
           const uint32_t bar = smem_u32(&ctl->full[s]);
           const int32_t xk = (w.c_lo + k) * kChunkK;
-          mbar_arrive_expect_tx(bar, kABytes + b_bytes);
-          if (once)
-            tma_load_2d(dst, &amap, bar, xk, w.o0, pol);  // rows past n_out read as zero
-          else
-            tma_load_2d_nohint(dst, &amap, bar, xk, w.o0);
+          if (g >= pre) {
+            if (g >= static_cast<uint32_t>(stages) &&
+                !mbar_wait<2>(smem_u32(&ctl->empty[s]), ((g / stages) & 1) ^ 1, abort_flag, nullptr)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar, kABytes + b_bytes);
+            load_w(dst, bar, xk, w.o0);
+          }
           tma_load_2d_nohint(dst + kABytes, &bmap, bar, xk, w.t0);  // token rows past n read as zero
         }
       }
@@ -378,7 +399,8 @@ cudaError_t launch_linear(const LinearArgs& a, cudaStream_t s, bool reduce) {
   if (a.n_tokens == 0) return cudaSuccess;
   if (!use_tc(a.n_in, a.act)) {
     if (a.k_splits != 1) return cudaErrorInvalidValue;
-    const dim3 grid((a.n_tokens + 7) / 8, (a.n_out + 7) / 8);
+    const int tok_tiles = (a.n_tokens + 7) / 8;
+    const dim3 grid((a.n_out + 7) / 8, tok_tiles < 65535 ? tok_tiles : 65535);
     if (a.act == MLA_F32) return launch_pdl(linear_simt_kernel<float>, grid, dim3(256), 0, s, a);
     return launch_pdl(linear_simt_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, a);
   }
@@ -403,6 +425,7 @@ cudaError_t launch_linear(const LinearArgs& a, cudaStream_t s, bool reduce) {
                  pl.acc_cols, pl.units);
   if (e != cudaSuccess || a.part == nullptr || !reduce) return e;
   const int64_t n = static_cast<int64_t>(a.n_tokens) * a.n_out;
+  if ((n + 255) / 256 > 0x7fffffff) return cudaErrorInvalidConfiguration;
   return launch_pdl(linear_reduce_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256),
                     0, s, a);
 }

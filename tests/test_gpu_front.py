@@ -105,6 +105,23 @@ def test_front(act, n, d_model, d_cq, H):
         assert_close(f64(g_), r_, what=f"front {name} {act} n={n} d={d_model}", **tol)
 
 
+def test_linear_and_front_past_grid_y_limit():
+    """Token counts whose tiles exceed a grid's y extent (65,535): the CUDA-core
+    linear layer at 600,000 tokens (75,000 tiles of 8) and the front end at
+    70,000 tokens (its per-token finishing kernels)."""
+    g = torch.Generator().manual_seed(24)
+    x = torch.randn(600_000, 64, generator=g)
+    w = torch.randn(8, 64, generator=g) / 8.0
+    y = _C().mla_linear(x.cuda(), w.cuda())
+    torch.cuda.synchronize()
+    assert_close(f64(y), O.linear(f64(x), f64(w)), what="linear, 600k tokens", **F32_TOL)
+    d, pos, max_pos = _front_case("bf16", 70_000, 64, 64, 1, seed=25, max_pos=4096)
+    got = _run_front(d, pos, max_pos, 1)
+    ref = _oracle_front(d, pos)
+    for name, g_, r_ in zip(("q_nope", "q_rope", "c_kv", "k_r"), got, ref):
+        assert_close(f64(g_), r_, what=f"front {name}, 70k tokens")
+
+
 def test_front_bad_position_flags_and_zeroes():
     d, pos, max_pos = _front_case("bf16", 3, 256, 128, 2, seed=23, max_pos=100)
     pos[1] = 100  # one past the table
