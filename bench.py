@@ -450,16 +450,27 @@ def run_ours(args):
     assert layer.device_error() == 0
 
     # end to end through the public API: the step's inputs copied in from pinned
-    # host memory and o copied back, inside the timed region (also a graph)
-    host_in = {k: v.cpu().pin_memory() for k, v in s.items()}
+    # host memory and o copied back, inside the timed region (also a graph). The
+    # inputs sit packed in one pinned buffer (256-byte aligned pieces), so the
+    # step pays for one copy in rather than one per tensor.
+    offs, total = {}, 0
+    for k, v in s.items():
+        offs[k] = total
+        total += (v.numel() * v.element_size() + 255) // 256 * 256
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    dev_in = torch.empty(total, dtype=torch.uint8, device="cuda")
+    s_e2e = {}
+    for k, v in s.items():
+        nb = v.numel() * v.element_size()
+        host_in[offs[k]:offs[k] + nb].copy_(v.cpu().contiguous().view(-1).view(torch.uint8))
+        s_e2e[k] = dev_in[offs[k]:offs[k] + nb].view(v.dtype).view(v.shape)
     host_out = torch.empty(layer.o.shape, dtype=layer.o.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    h2d = total
     d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step():
-        for k in host_in:
-            s[k].copy_(host_in[k], non_blocking=True)
-        layer.step(**s)
+        dev_in.copy_(host_in, non_blocking=True)
+        layer.step(**s_e2e)
         host_out.copy_(layer.o, non_blocking=True)
 
     g_e2e = layer.capture(e2e_step)
