@@ -74,7 +74,6 @@ constexpr int kCvtWarp0 = 2 + kSmxWarps;  // first of the two E4M3 converter war
 __host__ __device__ constexpr int threads_for(bool fp8) { return kThreads + (fp8 ? 64 : 0); }
 constexpr int kFp8BoxBytes = 64 * 64;  // 64 rows x 64 bytes of E4M3
 constexpr int kTileTok = 64;
-constexpr uint32_t kScaleTileBytes = kTileTok * MLA_E4M3_GROUPS * 4;  // a tile's E4M3 scale rows
 constexpr int kStages = 4;                  // ring of page halves
 constexpr int kBoxBytes = kTileTok * 128;   // 64 rows x 64 bf16, 128-byte swizzled
 constexpr int kHalfBytes = 4 * kBoxBytes;   // one page, one latent half
@@ -227,8 +226,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
     const int64_t yl = static_cast<int64_t>(my_entry) * P;
     const int32_t y0 = (yl < 0 || yl >= a.num_pages * static_cast<int64_t>(P)) ? -kTileTok : static_cast<int32_t>(yl);
     if constexpr (kFp8) {
-      if ((reinterpret_cast<uintptr_t>(a.scales) & 15u) == 0 && y0 >= 0)
-        bulk_prefetch_l2(a.scales + static_cast<int64_t>(y0) * MLA_E4M3_GROUPS, kScaleTileBytes);
       mbar_arrive_expect_tx(smem_u32(&sm->raw_full[0]), 4 * kFp8BoxBytes);
       for (int k = 0; k < 4; ++k)
         tma_load_2d_nohint(smem_u32(sm->kv[0]) + kHalfBytes / 2 + k * kFp8BoxBytes, &tmap, smem_u32(&sm->raw_full[0]),
@@ -301,7 +298,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
     // ================= TMA producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      const bool scales_pf = kFp8 && (reinterpret_cast<uintptr_t>(a.scales) & 15u) == 0;
       auto y_of = [&](int t) {  // pool row of tile t
         const int tok = tok_begin + t * kTileTok;
         return bt[tok / P] * P + (tok % P);
@@ -310,10 +306,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
         const int32_t yp = y_of(t);
         for (int k = 0; k < 4; ++k) tma_prefetch_l2_2d(&tmap, col_half + 64 * k, yp);
         if ((t & 1) == static_cast<int>(r)) tma_prefetch_l2_2d(&tmap, 512, yp);
-        // E4M3: the tile's scale rows too (64 rows x 5 fp32, contiguous; a tile
-        // starts at a multiple of 64 rows, so at a multiple of 1280 bytes), which
-        // the converter warps would otherwise fetch from DRAM page by page
-        if (scales_pf) bulk_prefetch_l2(a.scales + static_cast<int64_t>(yp) * MLA_E4M3_GROUPS, kScaleTileBytes);
       };
       constexpr int kPrefetch = 3;
       // Two independent streams: the KV half of page i into ring slot i % 4 once
