@@ -479,28 +479,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
     const int row_base = c >> 2, chunk = c & 3;
     const float* scales = a.scales;
     bool ok = true;
-    // 16 E4M3 values (one uint4) x scale -> 16 bf16 (two 16-byte chunks). A code's
-    // sign moved to bit 31 and its 7 exponent and mantissa bits to bits 20-26 read
-    // as fp32 the code's value times 2^-120: a normal code's exponent field e
-    // (bias 7) becomes fp32's (bias 127), and a subnormal code m 2^-9 becomes the
-    // fp32 denormal m 2^-129. Times 2^120 (exact) is the code's value; times the
-    // scale rounds once, to fl32(code * scale). Integer and fp32-pipe work only;
-    // the final bf16 packing is the one conversion. (NaN codes never occur in
-    // encoded rows: the encoder saturates.)
+    // 16 E4M3 values (one uint4) x scale -> 16 bf16 (two 16-byte chunks)
     auto convert16 = [&](const uint4& x, float sc, uint4& lo, uint4& hi) {
       const uint32_t wds[4] = {x.x, x.y, x.z, x.w};
       uint32_t outw[8];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        float f[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t t = wds[q] << (24 - 8 * k);  // byte k at bits 24..31
-          const uint32_t bits = (t & 0x80000000u) | ((t >> 4) & 0x07F00000u);
-          f[k] = __uint_as_float(bits) * 0x1p120f * sc;
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint16_t pair = static_cast<uint16_t>(wds[q] >> (16 * hh));
+          uint32_t h2;
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+          outw[2 * q + hh] = pack_bf16x2(f.x * sc, f.y * sc);
         }
-        outw[2 * q] = pack_bf16x2(f[0], f[1]);
-        outw[2 * q + 1] = pack_bf16x2(f[2], f[3]);
       }
       lo = make_uint4(outw[0], outw[1], outw[2], outw[3]);
       hi = make_uint4(outw[4], outw[5], outw[6], outw[7]);
