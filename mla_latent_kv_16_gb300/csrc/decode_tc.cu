@@ -479,6 +479,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
     const int row_base = c >> 2, chunk = c & 3;
     const float* scales = a.scales;
     bool ok = true;
+    // (x, y) * sc with one packed fp32 multiply (each product rounded once, as two
+    // separate multiplies would), packed to bf16x2
+    auto pack_bf16x2_scaled = [](float2 v, float sc) -> uint32_t {
+      uint64_t p;
+      asm("{\n\t.reg .b64 a, b;\n\tmov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %3};\n\t"
+          "mul.rn.f32x2 %0, a, b;\n\t}"
+          : "=l"(p)
+          : "f"(v.x), "f"(v.y), "f"(sc));
+      return pack_bf16x2(__uint_as_float(static_cast<uint32_t>(p)), __uint_as_float(static_cast<uint32_t>(p >> 32)));
+    };
     // 16 E4M3 values (one uint4) x scale -> 16 bf16 (two 16-byte chunks)
     auto convert16 = [&](const uint4& x, float sc, uint4& lo, uint4& hi) {
       const uint32_t wds[4] = {x.x, x.y, x.z, x.w};
@@ -491,7 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           uint32_t h2;
           asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-          outw[2 * q + hh] = pack_bf16x2(f.x * sc, f.y * sc);
+          outw[2 * q + hh] = pack_bf16x2_scaled(f, sc);
         }
       }
       lo = make_uint4(outw[0], outw[1], outw[2], outw[3]);
