@@ -491,3 +491,38 @@ def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
     w [out, in] ([P2] "PyTorch Reference Implementation" declares every
     projection so)."""
     return np.asarray(x, np.float64) @ np.asarray(w, np.float64).T
+
+
+# ---------------------------------------------------------------------------
+# Prefill in the MHA form: per-head K and V expanded from the latent rows
+# ---------------------------------------------------------------------------
+
+def expand_kv(rows: np.ndarray, w_uk: np.ndarray, w_uv: np.ndarray):
+    """Per-head keys and values of cached rows [T, 576] (c_KV, rotated k_R):
+    K[t, h] = [W_UK[h] c_t ; k_R,t] (192) and V[t, h] = W_UV[h] c_t (128).
+    [P4] §2.5 (the MHA form expands the shared latent into per-head K/V);
+    [P1] §2.3 (k = [k^C ; k^R], the RoPE key shared by all heads)."""
+    rows = np.asarray(rows, np.float64)
+    C, KR = rows[:, :D_C], rows[:, D_C:]
+    kc = np.einsum("tc,hec->the", C, np.asarray(w_uk, np.float64))
+    v = np.einsum("tc,hec->the", C, np.asarray(w_uv, np.float64))
+    k = np.concatenate([kc, np.broadcast_to(KR[:, None, :], (rows.shape[0], kc.shape[1], D_ROPE))], axis=-1)
+    return k, v
+
+
+def prefill_mha(q_nope: np.ndarray, q_rope: np.ndarray, rows: np.ndarray, w_uk: np.ndarray,
+                w_uv: np.ndarray, scale: float):
+    """Causal attention of the last Tq tokens of a sequence over all its rows,
+    in the MHA form: K and V expanded once, S = Q K^T * scale per head with
+    query j (of Tq) seeing rows 0 .. T - Tq + j, softmax, O = P V.
+    [P1] Q2 (prefill runs uncompressed, absorption is for decode); [P4] §2.5.
+    q_nope [Tq, H, 128], q_rope [Tq, H, 64] (rotated), rows [T, 576].
+    Returns o [Tq, H, 128] and lse [Tq, H]."""
+    k, v = expand_kv(rows, w_uk, w_uv)
+    q = np.concatenate([np.asarray(q_nope, np.float64), np.asarray(q_rope, np.float64)], axis=-1)
+    Tq, T = q.shape[0], rows.shape[0]
+    s = np.einsum("jhd,thd->hjt", q, k) * scale
+    visible = np.arange(T)[None, :] <= (T - Tq + np.arange(Tq))[:, None]
+    s = np.where(visible[None], s, -np.inf)
+    p, lse = softmax_stats(s)
+    return np.einsum("hjt,the->jhe", p, v), lse.T
