@@ -87,7 +87,9 @@ typedef void *mla_stream_t; /* cudaStream_t */
 #define MLA_DEVERR_BAD_SLOT 4     /* slot_mapping entry outside the pool        */
 #define MLA_DEVERR_BAD_POSITION 8 /* position outside [0, max_pos)              */
 #define MLA_DEVERR_TIMEOUT 16     /* a kernel-internal wait ran out of time; the
-                                     affected outputs are unspecified           */
+                                     affected work item's outputs are written as
+                                     for an empty one (zeros, lse -inf) where
+                                     the kernel can, else left unspecified      */
 
 /* E4M3 cache: one fp32 scale per token per group; groups of the 576-value row
  * are [0,128) [128,256) [256,384) [384,512) [512,576). */
@@ -197,9 +199,14 @@ size_t mla_decode_workspace_size(int32_t batch, int32_t q_len, int32_t max_pages
  *
  * Rows past seq_len in a sequence's last page are never read into the result
  * (they may hold anything, NaN included). act is MLA_F32 or MLA_BF16;
- * cache_dtype is act, or MLA_E4M3 with act == MLA_BF16. An E4M3 value enters
- * the scores and the latent sum as bf16: fl32(code * scale) rounded to
- * nearest-even, the operand type of the bf16 activations it pairs with.
+ * cache_dtype is act, or MLA_E4M3 with act == MLA_BF16. An E4M3 value is
+ * defined as decode(byte) * scale; the tensor-core kernel multiplies it as
+ * fl32(code * scale) rounded to bf16 (within 2^-8 relative), the operand type
+ * of the bf16 activations it pairs with.
+ * Which kernel runs: the tensor-core kernel for bf16 activations, 128 heads,
+ * page sizes that are multiples of 64 and pools of fewer than 2^31 rows (when
+ * the driver's tensor-map encoder is available); else the CUDA-core kernel.
+ * mla_decode_kernel_path reports which one a call with these arguments takes.
  */
 mla_status_t mla_decode_paged(const void *q_lat, const void *q_rope, const void *cache,
                               const float *scales, const int32_t *block_table,
@@ -209,6 +216,20 @@ mla_status_t mla_decode_paged(const void *q_lat, const void *q_rope, const void 
                               size_t workspace_bytes, void *u_out, float *lse_out,
                               int32_t *dev_error, mla_dims_t dims, mla_dtype_t act,
                               mla_dtype_t cache_dtype, mla_stream_t stream);
+
+/*
+ * mla_decode_kernel_path -- which decode kernel mla_decode_paged runs for a
+ * cache at `cache` of num_pages pages of page_size tokens with these dims and
+ * types: *path_out = MLA_DECODE_PATH_TENSOR_CORE (tcgen05, TMA) or
+ * MLA_DECODE_PATH_CUDA_CORE. Host only; reads no device memory. The pages
+ * describe no such call: it makes the kernel choice visible to a caller.
+ * Errors: MLA_ERR_INVALID_ARG for a NULL path_out or invalid dims / sizes.
+ */
+#define MLA_DECODE_PATH_TENSOR_CORE 1
+#define MLA_DECODE_PATH_CUDA_CORE 2
+mla_status_t mla_decode_kernel_path(const void *cache, const float *scales, int64_t num_pages,
+                                    int32_t page_size, mla_dims_t dims, mla_dtype_t act,
+                                    mla_dtype_t cache_dtype, int32_t *path_out);
 
 /*
  * mla_decode_paged_static_scratch -- mla_decode_paged without a caller
@@ -226,12 +247,17 @@ mla_status_t mla_decode_paged(const void *q_lat, const void *q_rope, const void 
  * MLA_STATIC_SCRATCH_BYTES (nothing is enqueued; use fewer splits, a smaller
  * batch, or mla_decode_paged with a workspace), and MLA_ERR_CUDA if the
  * array's address cannot be obtained.
- * Set-up: the first call on a device (that device current) looks up and caches
- * the array's address; make it before any stream capture on that device.
+ * Errors are checked in mla_decode_paged's order (the argument errors first),
+ * then the scratch size.
+ * Set-up: every call looks up the array's address on the current device
+ * (cudaGetSymbolAddress); the first call on a device may load the module, so
+ * make it before any stream capture on that device.
  * Sharing: all calls on a device share the array. Calls that may run
  * concurrently on the device (unordered streams, several host threads) race on
  * it and corrupt each other's results; order them. Nothing in the array has to
- * start at zero.
+ * start at zero: every partial the combine reads was written by the same call
+ * (a work item that gave up on a wait writes -inf log-sum-exps, so its
+ * partials are skipped; the timeout bit in dev_error reports it).
  */
 #define MLA_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 mla_status_t mla_decode_paged_static_scratch(const void *q_lat, const void *q_rope, const void *cache,

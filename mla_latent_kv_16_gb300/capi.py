@@ -25,12 +25,13 @@ DTYPE_CODE = {"f32": MLA_F32, "bf16": MLA_BF16, "e4m3": MLA_E4M3}
 MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_SEQLEN, MLA_DEVERR_BAD_SLOT, MLA_DEVERR_BAD_POSITION = 1, 2, 4, 8
 MLA_DEVERR_TIMEOUT = 16
 MLA_STATIC_SCRATCH_BYTES = 32 << 20  # size of the library's fixed split-KV scratch array
+MLA_DECODE_PATH_TENSOR_CORE, MLA_DECODE_PATH_CUDA_CORE = 1, 2
 
 EXPORTED = ("mla_status_string", "mla_version", "mla_rope_table", "mla_cache_append", "mla_absorb_q",
             "mla_decode_num_splits", "mla_decode_workspace_size", "mla_decode_paged", "mla_out_proj",
             "mla_read_device_error", "mla_decode_paged_static_scratch", "mla_fuse_out_weights",
             "mla_out_proj_fused_workspace_size", "mla_out_proj_fused", "mla_linear_workspace_size", "mla_linear",
-            "mla_decode_front_workspace_size", "mla_decode_front")
+            "mla_decode_front_workspace_size", "mla_decode_front", "mla_decode_kernel_path")
 
 
 class MlaDims(ctypes.Structure):
@@ -104,6 +105,8 @@ def load(path: Optional[str] = None):
     L.mla_decode_front.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, f32, i32, i32, i32, vp, vp, vp, vp, vp, sz,
                                    vp, MlaDims, ctypes.c_int, vp]
     L.mla_read_device_error.restype = ctypes.c_int
+    L.mla_decode_kernel_path.restype = ctypes.c_int
+    L.mla_decode_kernel_path.argtypes = [vp, vp, i64, i32, MlaDims, ctypes.c_int, ctypes.c_int, vp]
     L.mla_read_device_error.argtypes = [vp, vp, vp]
     _LIB = L
     return L
@@ -330,6 +333,17 @@ def mla_decode_paged_static_scratch(q_lat, q_rope, cache, scales, block_table, s
         _ptr(dev_error), dims(H), _act_code(q_lat), DTYPE_CODE[cache_dtype], _stream(stream))
     _check("mla_decode_paged_static_scratch", st)
     return u_out, lse_out
+
+
+def mla_decode_kernel_path(cache, scales, page_size: int, heads: int, act: str, cache_dtype: str) -> int:
+    """Which decode kernel mla_decode_paged runs on this cache: MLA_DECODE_PATH_TENSOR_CORE
+    or MLA_DECODE_PATH_CUDA_CORE."""
+    rows = cache.shape[0] * cache.shape[1] if cache.dim() == 3 else cache.shape[0]
+    out = ctypes.c_int32(0)
+    st = load().mla_decode_kernel_path(_ptr(cache), _ptr(scales), rows // page_size, page_size, dims(heads),
+                                       DTYPE_CODE[act], DTYPE_CODE[cache_dtype], ctypes.byref(out))
+    _check("mla_decode_kernel_path", st)
+    return out.value
 
 
 def mla_read_device_error(dev_error, stream=None) -> int:

@@ -82,6 +82,69 @@ size_t workspace_bytes_for(int32_t batch, int32_t q_len, int32_t splits, int32_t
 }
 
 }  // namespace
+
+mla_status_t decode_prepare(const void* q_lat, const void* q_rope, const void* cache, const float* scales,
+                            const int32_t* block_table, const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                            int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size, float softmax_scale,
+                            int32_t num_splits, void* u_out, float* lse_out, int32_t* dev_error, mla_dims_t dims,
+                            mla_dtype_t act, mla_dtype_t cache_dtype, DecodeArgs* out, size_t* workspace_need) {
+  if (!dims_ok(dims) || batch < 0 || q_len < 1 || static_cast<int64_t>(batch) * q_len > kMaxBatchQ ||
+      max_pages_per_seq < 1 || num_pages < 1 || page_size < 1 || num_splits < 0 || !std::isfinite(softmax_scale))
+    return MLA_ERR_INVALID_ARG;
+  if (act != MLA_F32 && act != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (!(cache_dtype == act || (cache_dtype == MLA_E4M3 && act == MLA_BF16))) return MLA_ERR_UNSUPPORTED;
+  if ((cache_dtype == MLA_E4M3) != (scales != nullptr)) return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_pages_per_seq) * page_size > (int64_t(1) << 30)) return MLA_ERR_INVALID_ARG;
+  *workspace_need = 0;
+  if (batch == 0) return MLA_OK;
+  if (q_lat == nullptr || q_rope == nullptr || cache == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      u_out == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_lat) || !aligned16(q_rope) || !aligned16(cache) || !aligned16(u_out))
+    return MLA_ERR_INVALID_ARG;
+  const int32_t S = resolve_splits(batch, q_len, max_pages_per_seq, page_size, num_splits, dims, cache_dtype);
+  if (S < 1) return MLA_ERR_INVALID_ARG;
+  DecodeArgs& a = *out;
+  a = DecodeArgs{};
+  a.q_lat = q_lat;
+  a.q_rope = q_rope;
+  a.cache = cache;
+  a.scales = scales;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.q_len = q_len;
+  a.max_pages = max_pages_per_seq;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.softmax_scale = softmax_scale;
+  a.num_splits = S;
+  a.pages_per_split = (max_pages_per_seq + S - 1) / S;
+  a.u_out = u_out;
+  a.lse_out = lse_out;
+  a.dev_error = dev_error;
+  a.heads = dims.num_heads;
+  a.act = act;
+  a.cache_dtype = cache_dtype;
+  *workspace_need = workspace_bytes_for(batch, q_len, S, dims.num_heads);
+  return MLA_OK;
+}
+
+mla_status_t decode_run(DecodeArgs& a, void* workspace, cudaStream_t s) {
+  const size_t rows = static_cast<size_t>(a.batch) * a.q_len * a.num_splits * a.heads;
+  a.part_u = workspace != nullptr ? static_cast<float*>(workspace) : nullptr;
+  a.part_lse = workspace != nullptr
+                   ? reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * 512 * sizeof(float)))
+                   : nullptr;
+  cudaError_t e;
+  if (use_tc_decode(a.heads, a.page_size, a.act, a.cache_dtype) && decode_tc_supported(a))
+    e = launch_decode_tc(a, s);
+  else
+    e = launch_decode_simt(a, s);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  return from_cuda(launch_combine(a, s));
+}
+
 }  // namespace mla
 
 using namespace mla;
@@ -271,57 +334,32 @@ mla_status_t mla_decode_paged(const void* q_lat, const void* q_rope, const void*
                               int32_t num_splits, void* workspace, size_t workspace_bytes, void* u_out,
                               float* lse_out, int32_t* dev_error, mla_dims_t dims, mla_dtype_t act,
                               mla_dtype_t cache_dtype, mla_stream_t stream) {
-  if (!dims_ok(dims) || batch < 0 || q_len < 1 || static_cast<int64_t>(batch) * q_len > kMaxBatchQ ||
-      max_pages_per_seq < 1 || num_pages < 1 || page_size < 1 || num_splits < 0 || !std::isfinite(softmax_scale))
-    return MLA_ERR_INVALID_ARG;
-  if (act != MLA_F32 && act != MLA_BF16) return MLA_ERR_UNSUPPORTED;
-  if (!(cache_dtype == act || (cache_dtype == MLA_E4M3 && act == MLA_BF16))) return MLA_ERR_UNSUPPORTED;
-  if ((cache_dtype == MLA_E4M3) != (scales != nullptr)) return MLA_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(max_pages_per_seq) * page_size > (int64_t(1) << 30)) return MLA_ERR_INVALID_ARG;
-  if (batch == 0) return MLA_OK;
-  if (q_lat == nullptr || q_rope == nullptr || cache == nullptr || block_table == nullptr || seq_lens == nullptr ||
-      u_out == nullptr)
-    return MLA_ERR_INVALID_ARG;
-  if (!aligned16(q_lat) || !aligned16(q_rope) || !aligned16(cache) || !aligned16(u_out))
-    return MLA_ERR_INVALID_ARG;
-  const int32_t S = resolve_splits(batch, q_len, max_pages_per_seq, page_size, num_splits, dims, cache_dtype);
-  if (S < 1) return MLA_ERR_INVALID_ARG;
-  const size_t need = workspace_bytes_for(batch, q_len, S, dims.num_heads);
+  DecodeArgs a{};
+  size_t need = 0;
+  const mla_status_t st = decode_prepare(q_lat, q_rope, cache, scales, block_table, seq_lens, batch, q_len,
+                                         max_pages_per_seq, num_pages, page_size, softmax_scale, num_splits, u_out,
+                                         lse_out, dev_error, dims, act, cache_dtype, &a, &need);
+  if (st != MLA_OK || batch == 0) return st;
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MLA_ERR_WORKSPACE_TOO_SMALL;
   if (need > 0 && !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+  return decode_run(a, need > 0 ? workspace : nullptr, static_cast<cudaStream_t>(stream));
+}
+
+mla_status_t mla_decode_kernel_path(const void* cache, const float* scales, int64_t num_pages, int32_t page_size,
+                                    mla_dims_t dims, mla_dtype_t act, mla_dtype_t cache_dtype, int32_t* path_out) {
+  if (path_out == nullptr || !dims_ok(dims) || num_pages < 1 || page_size < 1) return MLA_ERR_INVALID_ARG;
   DecodeArgs a{};
-  a.q_lat = q_lat;
-  a.q_rope = q_rope;
   a.cache = cache;
   a.scales = scales;
-  a.block_table = block_table;
-  a.seq_lens = seq_lens;
-  a.batch = batch;
-  a.q_len = q_len;
-  a.max_pages = max_pages_per_seq;
   a.num_pages = num_pages;
   a.page_size = page_size;
-  a.softmax_scale = softmax_scale;
-  a.num_splits = S;
-  a.pages_per_split = (max_pages_per_seq + S - 1) / S;
-  const size_t rows = static_cast<size_t>(batch) * q_len * S * dims.num_heads;
-  a.part_u = need > 0 ? static_cast<float*>(workspace) : nullptr;
-  a.part_lse = need > 0 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * 512 * sizeof(float)))
-                        : nullptr;
-  a.u_out = u_out;
-  a.lse_out = lse_out;
-  a.dev_error = dev_error;
   a.heads = dims.num_heads;
   a.act = act;
   a.cache_dtype = cache_dtype;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (use_tc_decode(dims.num_heads, page_size, act, cache_dtype) && decode_tc_supported(a))
-    e = launch_decode_tc(a, s);
-  else
-    e = launch_decode_simt(a, s);
-  if (e != cudaSuccess) return MLA_ERR_CUDA;
-  return from_cuda(launch_combine(a, s));
+  *path_out = (use_tc_decode(dims.num_heads, page_size, act, cache_dtype) && decode_tc_supported(a))
+                  ? MLA_DECODE_PATH_TENSOR_CORE
+                  : MLA_DECODE_PATH_CUDA_CORE;
+  return MLA_OK;
 }
 
 mla_status_t mla_read_device_error(const int32_t* dev_error, mla_stream_t stream, int32_t* code_out) {

@@ -115,6 +115,7 @@ struct __align__(1024) Smem {
   uint64_t cvt_bar;                           // both converter warps have read their page
   uint32_t tmem_base;
   int32_t abort_flag;
+  int32_t peer_abort;  // the peer's abort flag, stored here by the peer at teardown
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + realignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
@@ -192,6 +193,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
     mbar_init(smem_u32(&sm->l_bar), 1);
     mbar_init(smem_u32(&sm->drain), 1);
     sm->abort_flag = 0;
+    sm->peer_abort = 0;
     fence_mbar_init_cluster();
     prefetch_tmap(&tmap);
     prefetch_tmap(&qmap);
@@ -912,11 +914,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
     }
   }
 
-  // ---- teardown: nothing of this CTA may still be in flight towards the peer
+  // ---- teardown: nothing of this CTA may still be in flight towards the peer.
+  // If either CTA of the pair gave up on a wait (timeout), the work item's
+  // outputs are incomplete: both then write them as for an empty item (zeros,
+  // lse -inf), so that the combine skips this split instead of reading partials
+  // an earlier call left behind.
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) st_cluster_u32(map_to_rank(smem_u32(&sm->peer_abort), peer), *abort_flag != 0 ? 1u : 0u);
   cluster_sync();
+  if (n_tiles > 0 && (*abort_flag != 0 || sm->peer_abort != 0)) write_empty(a, row0, bj, split, r);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

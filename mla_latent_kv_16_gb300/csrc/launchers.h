@@ -153,6 +153,18 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 bool decode_tc_supported(const DecodeArgs& a);
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);
+// Argument checks, split count and workspace size of a decode call (api.cu),
+// shared by mla_decode_paged and mla_decode_paged_static_scratch so that both
+// return the same errors; fills *out except the workspace pointers.
+mla_status_t decode_prepare(const void* q_lat, const void* q_rope, const void* cache, const float* scales,
+                            const int32_t* block_table, const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                            int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size, float softmax_scale,
+                            int32_t num_splits, void* u_out, float* lse_out, int32_t* dev_error, mla_dims_t dims,
+                            mla_dtype_t act, mla_dtype_t cache_dtype, DecodeArgs* out, size_t* workspace_need);
+// Sets the workspace pointers (workspace: at least the size decode_prepare
+// reported, 16-byte aligned; may be null when that size is 0) and launches the
+// decode and combine kernels.
+mla_status_t decode_run(DecodeArgs& a, void* workspace, cudaStream_t s);
 
 int device_sm_count();
 

@@ -172,6 +172,12 @@ __device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v, 
                : "memory");
 }
 
+// Plain 4-byte store into another CTA's shared memory (ordered for the peer by a
+// following release/acquire cluster barrier).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // Named-barrier sync of kThreads threads (a multiple of 32) on barrier kId that
 // also returns the AND of their predicates: every participant learns whether
 // all of them succeeded, so they can leave a loop together.

@@ -10,13 +10,14 @@ directly would compute, per head h and token t,
 
 with q_lat and q_rope quantised to E4M3 too (scales sq per head and group).
 This script measures what that does to the decode output against the exact
-fp64 result, next to the current path (codes dequantised to bf16, q_lat in
-bf16), on seeded inputs of the E4M3 workload's recipe; also with the query as
-two E4M3 terms (the code and the code of its residual), which doubles the FP8
-score MMAs. In those rows the latent sum u = P V is left as it is (dequantised
-rows), so only the score path differs. The last rows take the latent sum to
-FP8 as well: each token's group scale folded into P (P_g[h, t] = p[h, t] *
-sk[t, g]), P_g quantised to E4M3 per head (one or two terms), times the codes.
+fp64 result (the cache read back as code x scale, no rounding), next to the
+current path (code x scale rounded to bf16, q_lat in bf16), on seeded inputs
+of the E4M3 workload's recipe; also with the query as two E4M3 terms (the code
+and the code of its residual), which doubles the FP8 score MMAs. In those rows
+the latent sum u = P V uses the exact read-back, so only the score path
+differs. The last rows take the latent sum to FP8 as well: each token's group
+scale folded into P (P_g[h, t] = p[h, t] * sk[t, g]), P_g quantised to E4M3
+per head (one or two terms), times the codes.
 
     python -m oracle.fp8_qk_study [n_seq] [seq_len]
 """
@@ -69,21 +70,23 @@ def study(n_seq: int = 3, seq_len: int = 2048, seed: int = 4):
             "two-term q; P in E4M3 per (head, group), two terms": []}
     for b in range(w.batch):
         L = int(w.seq_lens[b])
-        rows_bf16 = O.gather_rows(pool, sc, d["block_table"].numpy()[b], L, w.page_size, "e4m3")  # bf16-rounded
-        # the same rows, code x scale without the bf16 rounding (what an FP8 score path multiplies)
+        # exact read-back (code x scale in fp64): the definition, and what an FP8
+        # score path multiplies; the current kernel rounds it to bf16 first
+        rows_exact = O.gather_rows(pool, sc, d["block_table"].numpy()[b], L, w.page_size, "e4m3")
+        rows_bf16 = O.round_bf16(rows_exact)
         slots = [int(d["block_table"][b, t // w.page_size]) * w.page_size + t % w.page_size for t in range(L)]
         codes_k = pool.reshape(-1, 576)[slots]
         sc_k = sc.reshape(-1, 5)[slots]
         rows_exact_codes = dequantise(codes_k, sc_k, groups)
         for j in range(w.q_len):
             T = O.visible_tokens(L, w.q_len, j)
-            u_ref, lse_ref = O.attend_absorbed(q_lat[b, j], q_rope[b, j], rows_bf16[:T], scale)
+            u_ref, lse_ref = O.attend_absorbed(q_lat[b, j], q_rope[b, j], rows_exact[:T], scale)
             qfull = np.concatenate([q_lat[b, j], q_rope[b, j]], axis=-1)  # [H, 576]
 
             def run(q_eff, k_rows, pv=None):
                 s = (q_eff @ k_rows[:T].T) * scale
                 p, lse = O.softmax_stats(s)
-                return (p @ rows_bf16[:T, :512] if pv is None else pv(p)), lse
+                return (p @ k_rows[:T, :512] if pv is None else pv(p)), lse
 
             def pv_fp8(p, terms):
                 # u[:, g] = sum_t (p[:, t] sk[t, g]) code[t, g]: P_g quantised per head

@@ -252,8 +252,9 @@ def gather_rows(pool, scales, block_table_row, n_tokens: int, page_size: int,
                 cache_dtype: str) -> np.ndarray:
     """Logical rows 0..n_tokens-1 of one sequence, decoded to fp64, read through
     its block table (paged layout, [P1] §4.1 'block size 64 page allocations').
-    E4M3 rows come back dequantised and rounded to bf16, the operand type of
-    the activations an E4M3 cache is used with."""
+    E4M3 rows come back exactly dequantised: decode(byte) * scale of the
+    element's group, in fp64 ([P2] "High-Throughput Serving Kernels": E4M3
+    values with per-block scaling factors)."""
     pos = np.arange(n_tokens)
     pages = np.asarray(block_table_row, dtype=np.int64)[pos // page_size]
     slots = pages * page_size + pos % page_size
@@ -266,10 +267,7 @@ def gather_rows(pool, scales, block_table_row, n_tokens: int, page_size: int,
     sc = scales[slots].astype(np.float64)
     for gi, (a, b) in enumerate(E4M3_GROUPS):
         vals[:, a:b] *= sc[:, gi:gi + 1]
-    # An E4M3 cache pairs with bf16 activations, and the dequantised value
-    # code * scale (exact in fp64) enters the products as a bf16 operand:
-    # rounded to fp32 and then to bf16, both to nearest-even.
-    return round_bf16(vals)
+    return vals
 
 
 # ---------------------------------------------------------------------------
@@ -341,19 +339,6 @@ def round_bf16(x) -> np.ndarray:
     """fp64 values rounded as a GPU stores an fp32 result in bf16: to fp32
     (nearest) and then to bf16 (nearest-even); returned as fp64."""
     return bf16_bits_to_f64(f32_to_bf16_bits(np.asarray(x, np.float64).astype(np.float32)))
-
-
-def decode_full_bf16_interface(q_nope, q_rope, w_uk, w_uv, pool, scales, block_table, seq_lens, q_len: int,
-                               page_size: int, cache_dtype: str, scale: float, batch_index=None):
-    """The decode step computed exactly except that the two intermediates the
-    library exchanges in bf16 -- the absorbed query q_lat and the latent
-    output u -- are rounded to bf16 between the steps. Returns dict b -> o
-    [Lq,H,128]. Used to separate a kernel's own error from the rounding its
-    bf16 interface implies."""
-    q_lat = round_bf16(absorb_q(q_nope, w_uk))
-    lat = decode_latent(q_lat, q_rope, pool, scales, block_table, seq_lens, q_len, page_size, cache_dtype, scale,
-                        batch_index=batch_index)
-    return {b: out_proj(round_bf16(u), w_uv) for b, (u, _) in lat.items()}
 
 
 def default_scale(d_nope: int = D_NOPE, d_rope: int = D_ROPE) -> float:

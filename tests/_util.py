@@ -1,23 +1,29 @@
-"""Shared test helpers: parity metrics with the stated tolerances, and the
-oracle-side input plumbing (re-exported from oracle.harness)."""
+"""Shared test helpers: parity metrics with the stated tolerances, the error
+bound behind the log-sum-exp checks, and the oracle-side input plumbing
+(re-exported from oracle.harness)."""
 from __future__ import annotations
 
 import numpy as np
 
+from oracle import mla_oracle as O
 from oracle.harness import bits, f64, oracle_pool, seq_token_mask  # noqa: F401
 
-# Tolerances for bf16-in / fp32-accumulate outputs against the fp64 oracle:
-# rel-L2 <= 5e-3 and max-abs <= 2e-2. The max-abs bound is read as applying on
-# top of each element's own output rounding (2^-8 |ref|, one bf16 ulp): a bf16
-# value of magnitude 16 (reached with the x4 outlier tokens) cannot be closer
-# than 0.0625 to its fp64 reference whatever computed it. The bound is also
-# read as stated for unit-scale outputs: it is multiplied by max(1, rms(ref)).
-# Only the x4-outlier workload has rms(ref) > 1 (latent outputs of rms ~2.1),
-# where rounding u to bf16 alone (the ABI's latent output type), with every
-# other step exact, already gives max-abs 0.0235.
+# Tolerances for bf16-in / fp32-accumulate outputs against the fp64 oracle, as
+# stated: rel-L2 <= 5e-3 and max-abs <= 2e-2, both plain (absolute max-abs).
 REL_L2 = 5e-3
 MAX_ABS = 2e-2
+# One reading is kept for the long-context workload only, whose 1% x4 outlier
+# tokens give latent outputs of magnitude 16 and more: there the max-abs bound
+# is measured beyond each element's own output rounding (2^-8 |ref|, half a
+# bf16 ulp at most) and scaled by max(1, rms(ref)) -- a bf16 value near 16
+# cannot be within 2e-2 of its fp64 reference whatever computed it.
 OUT_ULP_REL = 2.0 ** -8
+OUTLIER_TOL = dict(ulp_rel=OUT_ULP_REL, rms_scaled=True)
+# fp32 paths are held to fp32-level error.
+F32_TOL = dict(rel=1e-5, mabs=1e-4)
+
+U_BF16 = 2.0 ** -8      # unit roundoff of bf16 (8 significant bits)
+U_F32 = 2.0 ** -24      # unit roundoff of fp32
 
 
 def rel_l2(x, ref) -> float:
@@ -27,15 +33,82 @@ def rel_l2(x, ref) -> float:
 
 
 def max_abs(x, ref, ulp_rel: float = 0.0) -> float:
-    """Largest |x - ref| beyond ulp_rel * |ref| (the output format's own rounding)."""
+    """Largest |x - ref| beyond ulp_rel * |ref| (0: the plain max-abs)."""
     x = np.asarray(x, np.float64)
     ref = np.asarray(ref, np.float64)
     return float(np.max(np.abs(x - ref) - ulp_rel * np.abs(ref)))
 
 
-def assert_close(x, ref, rel=REL_L2, mabs=MAX_ABS, what="", ulp_rel=OUT_ULP_REL):
+def assert_close(x, ref, rel=REL_L2, mabs=MAX_ABS, what="", ulp_rel=0.0, rms_scaled=False):
     r, m = rel_l2(x, ref), max_abs(x, ref, ulp_rel)
-    mabs = mabs * max(1.0, float(np.sqrt(np.mean(np.asarray(ref, np.float64) ** 2))))
+    if rms_scaled:
+        mabs = mabs * max(1.0, float(np.sqrt(np.mean(np.asarray(ref, np.float64) ** 2))))
     assert np.all(np.isfinite(np.asarray(x, np.float64))), f"{what}: non-finite values"
-    assert r <= rel and m <= mabs, f"{what}: rel_l2={r:.3e} (<= {rel}) max_abs={m:.3e} (<= {mabs})"
+    assert r <= rel and m <= mabs, f"{what}: rel_l2={r:.3e} (<= {rel}) max_abs={m:.3e} (<= {mabs:.3e})"
     return r, m
+
+
+def tol_for(w):
+    """Tolerance keywords for a workload's floating outputs."""
+    if w.act_dtype == "f32":
+        return dict(F32_TOL)
+    if w.outlier_frac > 0:
+        return dict(rel=REL_L2, mabs=MAX_ABS, **OUTLIER_TOL)
+    return dict(rel=REL_L2, mabs=MAX_ABS)
+
+
+def lse_bound(q_gpu, dq, q_rope, rows, scale, eps_c: float, p_bf16: bool = True) -> np.ndarray:
+    """Bound on |lse_gpu - lse_ref| per head for one query, from the error
+    analysis of the kernel's arithmetic:
+      * log-sum-exp is 1-Lipschitz in the max-norm of the scores, so a score
+        error of at most d_t per token moves lse by at most max_t d_t;
+      * the kernel's score is scale * sum_k q~_k c~_k over the 576 columns, with
+        q~ = q + dq the query the GPU was given (dq = its difference from the
+        reference's exact query, known to the test), c~ the cache values as
+        the kernel multiplies them (within eps_c relative of the exact
+        read-back: 0 for bf16/fp32 caches, 2^-8 when the kernel rounds
+        dequantised E4M3 values to bf16), accumulated in fp32:
+        d_t <= scale * (sum_k |dq_k c_k| + (eps_c + 600 u_f32) sum_k |q~_k c_k|);
+      * the row sum adds the bf16-rounded weights the latent sum uses (each
+        within 2^-8 of its value, so the sum within a factor 1 +- 2^-8 and its
+        log within log(1 + 2^-8)), in fp32 over the visible tokens.
+    q_gpu, dq [H,512] (latent part), q_rope [H,64] (given to both sides),
+    rows [T,576] fp64 (the visible rows, exact read-back)."""
+    rows = np.abs(np.asarray(rows, np.float64))
+    qg = np.concatenate([np.abs(np.asarray(q_gpu, np.float64)), np.abs(np.asarray(q_rope, np.float64))], -1)
+    d_q = np.abs(np.asarray(dq, np.float64)) @ rows[:, :512].T                # [H, T]
+    d_round = (eps_c + 600 * U_F32) * (qg @ rows.T)                           # [H, T]
+    d_score = scale * np.max(d_q + d_round, axis=-1)
+    d_sum = (np.log1p(U_BF16) if p_bf16 else 0.0) + (rows.shape[0] + 64) * U_F32
+    return d_score + d_sum + 1e-6
+
+
+def check_lse(lse, ref_lse, q_gpu, q_exact, q_rope, rows_by_query, scale, eps_c, what="", p_bf16=True):
+    """lse [Lq,H] against the reference, each query within lse_bound."""
+    q_gpu = np.asarray(q_gpu, np.float64)
+    q_exact = np.asarray(q_exact, np.float64)
+    for j in range(ref_lse.shape[0]):
+        bound = lse_bound(q_gpu[j], q_gpu[j] - q_exact[j], q_rope[j], rows_by_query[j], scale, eps_c, p_bf16)
+        err = np.abs(np.asarray(lse[j], np.float64) - ref_lse[j])
+        k = int(np.argmax(err - bound))
+        assert np.all(err <= bound), f"{what} query {j}: lse error {err[k]:.3e} > bound {bound[k]:.3e}"
+
+
+def visible_rows(w, d, pool, sc, b):
+    """The rows each query of sequence b attends to (exact read-back), [Lq] list."""
+    L = int(w.seq_lens[b])
+    rows = O.gather_rows(pool, sc, d["block_table"].numpy()[b], L, w.page_size, w.cache_dtype)
+    return [rows[:O.visible_tokens(L, w.q_len, j)] for j in range(w.q_len)]
+
+
+def decode_full_bf16_interface(q_nope, q_rope, w_uk, w_uv, pool, scales, block_table, seq_lens, q_len: int,
+                               page_size: int, cache_dtype: str, scale: float, batch_index=None):
+    """The decode step computed by the oracle exactly, except that the two
+    intermediates the library exchanges in bf16 -- the absorbed query q_lat
+    and the latent output u -- are rounded to bf16 between the steps. Returns
+    dict b -> o [Lq,H,128]. Used only for the long-context workload's x4
+    outlier tokens, where rounding q_lat alone moves o by more than 2e-2."""
+    q_lat = O.round_bf16(O.absorb_q(q_nope, w_uk))
+    lat = O.decode_latent(q_lat, q_rope, pool, scales, block_table, seq_lens, q_len, page_size, cache_dtype, scale,
+                          batch_index=batch_index)
+    return {b: O.out_proj(O.round_bf16(u), w_uv) for b, (u, _) in lat.items()}

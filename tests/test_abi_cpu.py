@@ -139,3 +139,41 @@ def test_linear_and_front_validation(capi):
     # workspace: the fp32 sums of both products plus c_q
     need = capi.mla_decode_front_workspace_size(32, 7168, 1536, 128)
     assert need >= 32 * (2112 + 24576) * 4 + 32 * 1536 * 2
+
+
+def test_static_scratch_checks_arguments_before_its_size(capi):
+    """mla_decode_paged_static_scratch returns mla_decode_paged's argument errors
+    even for a problem whose partials would not fit its scratch array."""
+    L = capi.load()
+    D = capi.dims(128)
+    # 64 sequences x 64 splits x 128 heads of fp32 partials: far beyond the array
+    big = (64, 1, 64, 4096, 64, 0.1, 64)
+    assert capi.mla_decode_workspace_size(64, 1, 64, 64, 64, 128, "bf16") > capi.MLA_STATIC_SCRATCH_BYTES
+
+    def call(act, cache_dt, scales=16, q=16):
+        B, Lq, maxp, npages, page, sc, splits = big
+        return L.mla_decode_paged_static_scratch(q, 16, 16, scales, 16, 16, B, Lq, maxp, npages, page, sc, splits,
+                                                 16, None, None, D, act, cache_dt, None)
+    assert call(capi.MLA_F32, capi.MLA_E4M3) == capi.MLA_ERR_UNSUPPORTED       # fp32 activations, E4M3 cache
+    assert call(capi.MLA_BF16, capi.MLA_E4M3, scales=None) == capi.MLA_ERR_INVALID_ARG  # E4M3 without scales
+    assert call(capi.MLA_BF16, capi.MLA_BF16, scales=None, q=None) == capi.MLA_ERR_INVALID_ARG   # missing q_lat
+    assert call(capi.MLA_BF16, capi.MLA_BF16, scales=None, q=8) == capi.MLA_ERR_INVALID_ARG      # misaligned q_lat
+    assert call(capi.MLA_BF16, capi.MLA_BF16, scales=None) == capi.MLA_ERR_WORKSPACE_TOO_SMALL  # valid, too big
+    # the same answers from mla_decode_paged (with no workspace)
+    B, Lq, maxp, npages, page, sc, splits = big
+    assert L.mla_decode_paged(16, 16, 16, 16, 16, 16, B, Lq, maxp, npages, page, sc, splits, None, 0, 16, None, None,
+                              D, capi.MLA_F32, capi.MLA_E4M3, None) == capi.MLA_ERR_UNSUPPORTED
+
+
+def test_decode_kernel_path_query(capi):
+    """The kernel-choice query: argument errors, and the CUDA-core kernel for
+    the cases the tensor-core kernel does not take (fp32, 16 heads, 100-token pages)."""
+    L = capi.load()
+    import ctypes
+    out = ctypes.c_int32(0)
+    assert L.mla_decode_kernel_path(16, None, 4, 64, capi.dims(128), capi.MLA_BF16, capi.MLA_BF16,
+                                    None) == capi.MLA_ERR_INVALID_ARG
+    for dims_, act, page in ((capi.dims(16), capi.MLA_F32, 256), (capi.dims(16), capi.MLA_BF16, 64),
+                             (capi.dims(128), capi.MLA_BF16, 100)):
+        assert L.mla_decode_kernel_path(16, None, 4, page, dims_, act, act, ctypes.byref(out)) == capi.MLA_OK
+        assert out.value == capi.MLA_DECODE_PATH_CUDA_CORE

@@ -321,11 +321,11 @@ def test_decode_independent_of_page_permutation():
 
 
 def test_e4m3_readback_values_by_hand():
-    """E4M3 rows read back as fl32(code * scale) rounded to bf16 (nearest-even),
-    each element scaled by its own group's factor. Expected values worked by hand:
-    0x38 is 1.0 and 0x3A is 1.25 (exponent field 7, mantissa 010); 0x7E is 448.
-    fl32(0.1) = 1.6000000238 * 2^-4 -> bf16 mantissa 205/128 -> 0.10009765625;
-    1.25 * fl32(1/3) = 0.41666668 -> 213/512 = 0.416015625; 448 * 3 = 1344 exact."""
+    """E4M3 rows read back as decode(byte) * scale, exactly (in fp64), each
+    element scaled by its own group's factor. Expected values worked by hand:
+    0x38 is 1.0 and 0x3A is 1.25 (exponent field 7, mantissa 010); 0x7E is 448;
+    0xB8 is -1.0. fl32(0.1) = 13421773 * 2^-27 exactly, fl32(1/3) = 11184811 *
+    2^-25; 1.25 * fl32(1/3) = 55924055 * 2^-27; 448 * 3 = 1344."""
     pool = np.full((2, O.ROW), 0x38, dtype=np.uint8)
     sc = np.ones((2, len(O.E4M3_GROUPS)), dtype=np.float32)
     sc[1] = [0.1, 1.0 / 3.0, 3.0, 2.0, 0.5]
@@ -333,9 +333,10 @@ def test_e4m3_readback_values_by_hand():
     pool[1, 256] = 0x7E
     pool[1, 512] = 0xB8                      # -1.0 in the RoPE group
     rows = O.gather_rows(pool, sc, np.array([0]), 2, 2, "e4m3")
-    assert np.all(rows[0] == 1.0)            # power-of-two scale: no rounding
-    assert rows[1, 0] == 0.10009765625 and rows[1, 127] == 0.10009765625
-    assert rows[1, 128] == 0.416015625
+    assert np.all(rows[0] == 1.0)            # unit scale: the codes themselves
+    assert rows[1, 0] == 13421773 * 2.0 ** -27 and rows[1, 127] == 13421773 * 2.0 ** -27
+    assert rows[1, 129] == 11184811 * 2.0 ** -25
+    assert rows[1, 128] == 55924055 * 2.0 ** -27   # not representable in fp32 or bf16: no rounding
     assert rows[1, 256] == 1344.0
     assert rows[1, 511] == 2.0               # last latent element: group 3
     assert rows[1, 512] == -0.5 and rows[1, 575] == 0.5   # RoPE part: group 4
