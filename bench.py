@@ -39,7 +39,13 @@ FUSED_METRIC = "MLA fused output projection (W~ = W_O W_UV) weight-stream GB/s a
 # paged decode, fused output projection) at the DeepSeek-V3 shape: its own line.
 LAYER_WORKLOAD = "dsv3_layer"
 LAYER_METRIC = "MLA decode layer (front end + latent attention + fused output projection) tokens/s at 1 GB300"
+# Prefill in the MHA form (K and V expanded from the latent rows, causal
+# attention) for one DeepSeek-V3-shaped prompt of 4096 tokens: its own line.
+PREFILL_WORKLOAD = "dsv3_prefill"
+PREFILL_METRIC = "MLA prefill (MHA form: K/V expansion + causal attention) TFLOP/s at 1 GB300; % of bf16 tensor peak"
+PREFILL_T = 4096
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20  # read (not written) before every timed step
 
 
@@ -684,6 +690,163 @@ def run_layer(args):
     print(json.dumps(out), flush=True)
 
 
+def prefill_flops(T: int, Tq: int, H: int) -> float:
+    """Algorithmic FLOPs of one prefill call: the expansion (K_nope and V, each
+    [T x 512] x [512 x 128 H]) and the causal attention (query j sees
+    T - Tq + j + 1 keys; 192-wide scores, 128-wide values)."""
+    vis = sum(T - Tq + j + 1 for j in range(Tq))
+    return 2.0 * 2 * T * 512 * 128 * H + 2.0 * H * vis * (192 + 128)
+
+
+def cpu_prefill_run(d, seconds: float):
+    """The oracle's per-query non-absorbed attention (materialised K/V of the
+    visible rows, every head) on queries spread over the prompt, for a bounded
+    time; returns (TFLOP/s, sample, threads, seconds)."""
+    import numpy as np
+    from oracle import mla_oracle as O
+    from oracle.harness import f64
+    rows = f64(d["rows"])
+    qn, qr, wuk, wuv = f64(d["q_nope"]), f64(d["q_rope"]), f64(d["w_uk"]), f64(d["w_uv"])
+    T, H = rows.shape[0], qn.shape[1]
+    order = np.random.default_rng(7).permutation(T)
+    t0 = time.time()
+    flops, n = 0.0, 0
+    for j in order:
+        O.attend_nonabsorbed(qn[j], qr[j], wuk, wuv, rows[:j + 1], O.default_scale())
+        flops += 2.0 * H * (j + 1) * (512 * 256 + 192 + 128)
+        n += 1
+        if time.time() - t0 > seconds:
+            break
+    el = time.time() - t0
+    return flops / el / 1e12, f"{n} queries of the {T}-token prompt (all {H} heads; non-absorbed fp64 oracle, K/V materialised per query)", \
+        os.cpu_count() or 1, el
+
+
+def run_prefill(args):
+    """One mla_prefill_mha call per step on a 4096-token prompt (128 heads)."""
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    from mla_latent_kv_16_gb300 import build as B
+    B.build()
+    from mla_latent_kv_16_gb300 import capi, workloads as W
+    capi.load()
+    T, H = PREFILL_T, 128
+    d = W.make_prefill_inputs(T, T, H, seed=1)
+    dev = {k: v.cuda() for k, v in d.items()}
+    ws = torch.empty(capi.mla_prefill_workspace_size(T, H), dtype=torch.uint8, device="cuda")
+    o = torch.empty(T, H, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        capi.mla_prefill_mha(dev["q_nope"], dev["q_rope"], dev["rows"], dev["w_uk"], dev["w_uv"], workspace=ws,
+                             o_out=o, lse_out=lse)
+
+    def capture(fn):
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                fn()
+        stream.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    def timed(graph, k, clk=None):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        if clk is not None:
+            clk.start()
+            time.sleep(0.3)
+        for i in range(k):
+            flush.sum()
+            evs[i][0].record(stream)
+            graph.replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    g_call = capture(call)
+    for _ in range(args.warmup):
+        flush.sum()
+        g_call.replay()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    call_ms = timed(g_call, args.steps, clk)
+    clocks = clk.stop()
+    host = {k: d[k].pin_memory() for k in ("q_nope", "q_rope", "rows")}
+    host_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+
+    def e2e():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        call()
+        host_o.copy_(o, non_blocking=True)
+
+    g_e2e = capture(e2e)
+    for _ in range(args.warmup):
+        flush.sum()
+        g_e2e.replay()
+    e2e_ms = statistics.mean(timed(g_e2e, args.steps))
+    fl = prefill_flops(T, T, H)
+    ms = statistics.mean(call_ms)
+    tfs = fl / (ms * 1e-3) / 1e12
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    out = {
+        "metric": PREFILL_METRIC, "value": round(tfs, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded rows, q ~ N(0,1); W_UK, W_UV ~ N(0,1/sqrt(512)))",
+        "config": {"workload": PREFILL_WORKLOAD, "tokens": T, "queries": T, "heads": H,
+                   "l2": "flushed before every timed call by reading a 256 MiB buffer",
+                   "parallelism": "dp1 (one sequence)"},
+        "tokens_per_s": round(T / (ms * 1e-3), 1),
+        "roofline": {"bound": "tensor", "achieved": round(tfs, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tfs / peak, 4), "traffic": None,
+                     "kernel": "mla_prefill_mha (2 tcgen05 expansion GEMMs + causal attention), algorithmic FLOPs",
+                     "peak_source": f"bf16_tflops of {src}"},
+        "e2e": {"value": round(fl / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+                "d2h_bytes_per_step": host_o.numel() * 2},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        v, sample, thr, el = cpu_prefill_run(d, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                               "sample": sample, "seconds": round(el, 2)}
+    print(json.dumps(out), flush=True)
+
+
+def run_reference_prefill(args):
+    from mla_latent_kv_16_gb300 import workloads as W
+    T, H = PREFILL_T, 128
+    d = W.make_prefill_inputs(T, T, H, seed=1)
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_prefill_run(d, min(budget, 2.0))
+    vals, secs, sample, thr = [], 0.0, "", 1
+    for _ in range(args.steps):
+        v, sample, thr, el = cpu_prefill_run(d, budget)
+        vals.append(v)
+        secs += el
+    value = statistics.mean(vals)
+    out = {"impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded)", "config": {"workload": PREFILL_WORKLOAD, "tokens": T, "queries": T,
+                                                     "heads": H},
+           "cpu_baseline": {"kind": "oracle", "cores": thr, "sample": sample, "value": round(value, 6),
+                            "unit": "TFLOP/s"},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
 def run_reference_fused(args):
     from mla_latent_kv_16_gb300 import workloads as W
     w = W.preset(DEFAULT_WORKLOAD)
@@ -740,6 +903,8 @@ def run_reference(args):
         return run_reference_fused(args)
     if args.workload == LAYER_WORKLOAD:
         return run_reference_layer(args)
+    if args.workload == PREFILL_WORKLOAD:
+        return run_reference_prefill(args)
     from mla_latent_kv_16_gb300 import workloads as W
     w = W.preset(args.workload)
     d = W.make_inputs(w)
@@ -772,6 +937,8 @@ def main():
         run_fused(args)
     elif args.workload == LAYER_WORKLOAD:
         run_layer(args)
+    elif args.workload == PREFILL_WORKLOAD:
+        run_prefill(args)
     else:
         run_ours(args)
 

@@ -270,6 +270,43 @@ mla_status_t mla_decode_paged_static_scratch(const void *q_lat, const void *q_ro
                                              mla_stream_t stream);
 
 /*
+ * mla_prefill_mha -- prefill in the MHA form: causal attention of the last
+ * n_queries positions of one sequence over all its n_tokens cached rows, with
+ * the per-head keys and values expanded from the latent rows.
+ * "DeepSeek's attention evolution - [MLA]" §2.5 (the latent expanded back into
+ * per-head K and V: multi-head attention for prefill); "Model Architecture
+ * Driving Inference Systems" FAQ Q2 (prefill runs uncompressed; absorption is
+ * for decode) and §2.3 (k = [k^C ; k^R], the RoPE key shared by all heads).
+ *
+ *   K_h[t] = [W_UK[h] c_KV[t] ; k_R[t]] (192),  V_h[t] = W_UV[h] c_KV[t] (128)
+ *   o[j][h] = sum_{t <= n_tokens - n_queries + j} softmax_t(q[j][h] . K_h[t] * scale) V_h[t]
+ * with q[j][h] = [q_nope[j][h] ; q_rope[j][h]].
+ *
+ *   q_nope  [n_queries][H][128] bf16, q_rope [n_queries][H][64] bf16 (rotated)
+ *   rows    [n_tokens][576] bf16: c_KV (512) and the rotated k_R (64) of every
+ *           token, the layout of a cache row
+ *   w_uk, w_uv [H][128][512] bf16
+ *   workspace : >= mla_prefill_workspace_size(n_tokens, dims) bytes, 16-byte
+ *           aligned (the expanded K and V; its contents are overwritten)
+ *   o_out   [n_queries][H][128] bf16; lse_out [n_queries][H] fp32 or NULL
+ *   dev_error : device int32 for MLA_DEVERR_TIMEOUT, or NULL
+ * The expansion runs on the tensor cores (fp32 accumulation, K and V rounded
+ * to bf16), then the attention (fp32 scores and sums, P rounded to bf16 for
+ * the PV product). Asynchronous on `stream`.
+ * Errors: MLA_ERR_INVALID_ARG (dims, sizes with 1 <= n_queries <= n_tokens <=
+ * 2^20, NULL or misaligned pointers, non-finite scale), MLA_ERR_UNSUPPORTED
+ * (act other than MLA_BF16, or no tensor-map encoder in the driver),
+ * MLA_ERR_WORKSPACE_TOO_SMALL, MLA_ERR_CUDA (launch).
+ */
+size_t mla_prefill_workspace_size(int32_t n_tokens, mla_dims_t dims);
+mla_status_t mla_prefill_mha(const void *q_nope, const void *q_rope, const void *rows,
+                             const void *w_uk, const void *w_uv, int32_t n_tokens,
+                             int32_t n_queries, float softmax_scale, void *workspace,
+                             size_t workspace_bytes, void *o_out, float *lse_out,
+                             int32_t *dev_error, mla_dims_t dims, mla_dtype_t act,
+                             mla_stream_t stream);
+
+/*
  * mla_out_proj -- per-head value up-projection, o[t][h][:] = W_UV[h] u[t][h][:].
  * [P1] §3.2 (W_UV moved after the attention-weighted sum); [P2] "Value Output
  * Matrix Absorption" with W_UV viewed as [n_heads][d_head][d_c].

@@ -31,7 +31,8 @@ EXPORTED = ("mla_status_string", "mla_version", "mla_rope_table", "mla_cache_app
             "mla_decode_num_splits", "mla_decode_workspace_size", "mla_decode_paged", "mla_out_proj",
             "mla_read_device_error", "mla_decode_paged_static_scratch", "mla_fuse_out_weights",
             "mla_out_proj_fused_workspace_size", "mla_out_proj_fused", "mla_linear_workspace_size", "mla_linear",
-            "mla_decode_front_workspace_size", "mla_decode_front", "mla_decode_kernel_path")
+            "mla_decode_front_workspace_size", "mla_decode_front", "mla_decode_kernel_path",
+            "mla_prefill_workspace_size", "mla_prefill_mha")
 
 
 class MlaDims(ctypes.Structure):
@@ -106,6 +107,10 @@ def load(path: Optional[str] = None):
                                    vp, MlaDims, ctypes.c_int, vp]
     L.mla_read_device_error.restype = ctypes.c_int
     L.mla_decode_kernel_path.restype = ctypes.c_int
+    L.mla_prefill_workspace_size.restype = sz
+    L.mla_prefill_workspace_size.argtypes = [i32, MlaDims]
+    L.mla_prefill_mha.restype = ctypes.c_int
+    L.mla_prefill_mha.argtypes = [vp, vp, vp, vp, vp, i32, i32, f32, vp, sz, vp, vp, vp, MlaDims, ctypes.c_int, vp]
     L.mla_decode_kernel_path.argtypes = [vp, vp, i64, i32, MlaDims, ctypes.c_int, ctypes.c_int, vp]
     L.mla_read_device_error.argtypes = [vp, vp, vp]
     _LIB = L
@@ -333,6 +338,34 @@ def mla_decode_paged_static_scratch(q_lat, q_rope, cache, scales, block_table, s
         _ptr(dev_error), dims(H), _act_code(q_lat), DTYPE_CODE[cache_dtype], _stream(stream))
     _check("mla_decode_paged_static_scratch", st)
     return u_out, lse_out
+
+
+def mla_prefill_workspace_size(n_tokens: int, heads: int) -> int:
+    return load().mla_prefill_workspace_size(n_tokens, dims(heads))
+
+
+def mla_prefill_mha(q_nope, q_rope, rows, w_uk, w_uv, softmax_scale: Optional[float] = None, workspace=None,
+                    o_out=None, lse_out=None, dev_error=None, stream=None, want_lse: bool = True):
+    """Prefill in the MHA form for one sequence: q_nope [Tq, H, 128], q_rope [Tq, H, 64],
+    rows [T, 576] (the sequence's cache rows) -> (o [Tq, H, 128], lse [Tq, H] or None)."""
+    _contig_cuda(q_nope, q_rope, rows, w_uk, w_uv, workspace, o_out, lse_out, dev_error)
+    Tq, H = q_nope.shape[0], q_nope.shape[1]
+    T = rows.shape[0]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(128 + 64)
+    if o_out is None:
+        o_out = torch.empty(Tq, H, 128, dtype=q_nope.dtype, device=q_nope.device)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty(Tq, H, dtype=torch.float32, device=q_nope.device)
+    need = mla_prefill_workspace_size(T, H)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_nope.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().mla_prefill_mha(_ptr(q_nope), _ptr(q_rope), _ptr(rows), _ptr(w_uk), _ptr(w_uv), T, Tq,
+                                softmax_scale, _ptr(workspace), ws_bytes, _ptr(o_out), _ptr(lse_out), _ptr(dev_error),
+                                dims(H), _act_code(q_nope), _stream(stream))
+    _check("mla_prefill_mha", st)
+    return o_out, lse_out
 
 
 def mla_decode_kernel_path(cache, scales, page_size: int, heads: int, act: str, cache_dtype: str) -> int:

@@ -28,6 +28,7 @@ constexpr int32_t kMaxTokens = 1 << 20;
 constexpr int32_t kMaxBatchQ = 65535;
 constexpr int32_t kMaxDModel = 1 << 16;
 constexpr int32_t kMaxLinearDim = 1 << 20;
+constexpr int32_t kMaxPrefillTokens = 1 << 20;
 
 bool dims_ok(const mla_dims_t& d) {
   return d.d_nope == 128 && d.d_c == 512 && d.d_rope == 64 && d.d_v == 128 && d.num_heads >= 1 &&
@@ -360,6 +361,45 @@ mla_status_t mla_decode_kernel_path(const void* cache, const float* scales, int6
                   ? MLA_DECODE_PATH_TENSOR_CORE
                   : MLA_DECODE_PATH_CUDA_CORE;
   return MLA_OK;
+}
+
+size_t mla_prefill_workspace_size(int32_t n_tokens, mla_dims_t dims) {
+  if (!dims_ok(dims) || n_tokens < 1 || n_tokens > kMaxPrefillTokens) return 0;
+  return prefill_workspace_bytes(n_tokens, dims.num_heads);
+}
+
+mla_status_t mla_prefill_mha(const void* q_nope, const void* q_rope, const void* rows, const void* w_uk,
+                             const void* w_uv, int32_t n_tokens, int32_t n_queries, float softmax_scale,
+                             void* workspace, size_t workspace_bytes, void* o_out, float* lse_out,
+                             int32_t* dev_error, mla_dims_t dims, mla_dtype_t act, mla_stream_t stream) {
+  if (!dims_ok(dims) || n_tokens < 1 || n_tokens > kMaxPrefillTokens || n_queries < 1 || n_queries > n_tokens ||
+      !std::isfinite(softmax_scale))
+    return MLA_ERR_INVALID_ARG;
+  if (act != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q_nope, q_rope, rows, w_uk, w_uv, o_out, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr) return p == workspace ? MLA_ERR_WORKSPACE_TOO_SMALL : MLA_ERR_INVALID_ARG;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MLA_ERR_INVALID_ARG;
+  const size_t need = prefill_workspace_bytes(n_tokens, dims.num_heads);
+  if (workspace_bytes < need) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (!prefill_supported()) return MLA_ERR_UNSUPPORTED;
+  PrefillArgs a{};
+  a.q_nope = q_nope;
+  a.q_rope = q_rope;
+  a.rows = rows;
+  a.w_uk = w_uk;
+  a.w_uv = w_uv;
+  a.k_nope = workspace;
+  a.v = static_cast<char*>(workspace) + need / 2;
+  a.o = o_out;
+  a.lse = lse_out;
+  a.dev_error = dev_error;
+  a.n_tokens = n_tokens;
+  a.n_queries = n_queries;
+  a.heads = dims.num_heads;
+  a.softmax_scale = softmax_scale;
+  return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
 mla_status_t mla_read_device_error(const int32_t* dev_error, mla_stream_t stream, int32_t* code_out) {

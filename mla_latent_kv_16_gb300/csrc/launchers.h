@@ -89,6 +89,8 @@ struct LinearArgs {
   mla_dtype_t act;
   int32_t w_static;  // 1: no kernel still running before this one writes W (its
                      // first ring may be requested before griddepcontrol.wait)
+  int64_t x_stride;  // elements between consecutive rows of x; 0 = n_in (the
+                     // tensor-core path only, a multiple of 8)
 };
 // K splits for these sizes on the current device (1 on the CUDA-core path),
 // and the bytes of their fp32 sums [splits][n][n_out], 256-byte aligned.
@@ -97,6 +99,28 @@ size_t linear_partial_bytes(int32_t n_tokens, int32_t n_out, int32_t n_in, mla_d
 // reduce: with part set, also add the splits into y (otherwise the caller
 // consumes the fp32 sums itself).
 cudaError_t launch_linear(const LinearArgs& a, cudaStream_t s, bool reduce);
+
+// Prefill in the MHA form (prefill.cu): K_nope and V expanded from the latent
+// rows by the linear layer, then causal attention per head on tcgen05.
+struct PrefillArgs {
+  const void* q_nope;  // [Tq][H][128] bf16
+  const void* q_rope;  // [Tq][H][64] bf16, rotated
+  const void* rows;    // [T][576] bf16: c_KV and the rotated k_R of every token
+  const void* w_uk;    // [H][128][512] bf16
+  const void* w_uv;    // [H][128][512] bf16
+  void* k_nope;        // workspace [T][H][128] bf16
+  void* v;             // workspace [T][H][128] bf16
+  void* o;             // [Tq][H][128] bf16
+  float* lse;          // [Tq][H] fp32 or nullptr
+  int32_t* dev_error;
+  int32_t n_tokens;    // T
+  int32_t n_queries;   // Tq: the last Tq positions of the sequence
+  int32_t heads;
+  float softmax_scale;
+};
+size_t prefill_workspace_bytes(int32_t n_tokens, int32_t heads);
+bool prefill_supported();
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 
 // Decode-layer front end (front.cu).
 struct FrontArgs {

@@ -322,10 +322,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// 2D map over a [rows][cols] bf16 matrix, boxes of 64 columns x box_rows.
-bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2D map over a [rows][cols] bf16 matrix (row stride `stride` elements, 0 =
+// cols), boxes of 64 columns x box_rows.
+bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+               uint64_t stride = 0) {
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint64_t strides[1] = {(stride != 0 ? stride : cols) * 2};
   const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -397,6 +399,8 @@ size_t linear_partial_bytes(int32_t n_tokens, int32_t n_out, int32_t n_in, mla_d
 
 cudaError_t launch_linear(const LinearArgs& a, cudaStream_t s, bool reduce) {
   if (a.n_tokens == 0) return cudaSuccess;
+  if (a.x_stride != 0 && a.x_stride != a.n_in && (!use_tc(a.n_in, a.act) || a.x_stride < a.n_in || a.x_stride % 8))
+    return cudaErrorInvalidValue;
   if (!use_tc(a.n_in, a.act)) {
     if (a.k_splits != 1) return cudaErrorInvalidValue;
     const int tok_tiles = (a.n_tokens + 7) / 8;
@@ -410,7 +414,7 @@ cudaError_t launch_linear(const LinearArgs& a, cudaStream_t s, bool reduce) {
   CUtensorMap am, bm;
   if (!encode_2d(&am, a.w, static_cast<uint64_t>(a.n_out), static_cast<uint64_t>(a.n_in), 128) ||
       !encode_2d(&bm, a.x, static_cast<uint64_t>(a.n_tokens), static_cast<uint64_t>(a.n_in),
-                 static_cast<uint32_t>(pl.n_tile)))
+                 static_cast<uint32_t>(pl.n_tile), static_cast<uint64_t>(a.x_stride)))
     return cudaErrorInvalidValue;
   static int attr_dev = -1;
   int dev = 0;

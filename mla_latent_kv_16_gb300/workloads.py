@@ -232,6 +232,22 @@ def make_front_inputs(w: Workload, d_model: int = D_MODEL, d_cq: int = D_CQ) -> 
     return d
 
 
+def make_prefill_inputs(n_tokens: int, n_queries: int, heads: int = 128, seed: int = 5,
+                        act_dtype: str = BF16) -> dict:
+    """One sequence for prefill in the MHA form: its n_tokens cached rows
+    [T, 576] (c_KV and the k_R part, both drawn N(0,1); the k_R part stands for
+    already-rotated keys, as a cache row holds them), the queries of its last
+    n_queries positions q_nope [Tq, H, 128] and q_rope [Tq, H, 64] (rotated)
+    ~ N(0,1), and W_UK, W_UV [H, 128, 512] ~ N(0,1) / sqrt(512)."""
+    g = torch.Generator().manual_seed(seed * 7919 + 3)
+    dt = TORCH_DTYPE[act_dtype]
+    return {"rows": torch.randn(n_tokens, ROW, generator=g).to(dt),
+            "q_nope": torch.randn(n_queries, heads, D_NOPE, generator=g).to(dt),
+            "q_rope": torch.randn(n_queries, heads, D_ROPE, generator=g).to(dt),
+            "w_uk": (torch.randn(heads, D_NOPE, D_C, generator=g) / math.sqrt(D_C)).to(dt),
+            "w_uv": (torch.randn(heads, D_V, D_C, generator=g) / math.sqrt(D_C)).to(dt)}
+
+
 def sample_sequences(w: Workload, k: int, seed: int = 12345):
     """A seeded subset of sequence indices (for checks at full size)."""
     g = torch.Generator().manual_seed(seed)
