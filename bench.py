@@ -52,13 +52,21 @@ L2_FLUSH_BYTES = 256 << 20  # read (not written) before every timed step
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    # default: enough timed steps that the clock sampler (200 ms) sees the
+    # timed region under load for about a second (decode step ~0.13 ms with
+    # its L2 flush); fewer for the longer steps of the other lines
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
-    return p.parse_args()
+    a = p.parse_args()
+    if a.steps is None:
+        a.steps = {FUSED_WORKLOAD: 4000, LAYER_WORKLOAD: 3000, PREFILL_WORKLOAD: 300}.get(a.workload, 8000)
+        if a.impl == "reference":
+            a.steps = 20
+    return a
 
 
 def dist_env():
@@ -175,24 +183,36 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_run(w, d, seconds: float):
-    """Time the fp64 oracle (non-absorbed form, one head at a time) on a bounded
-    sample of the workload: whole sequences with all heads, in order, until
-    `seconds` of oracle work are done (the last sequence may stop part-way
-    through its heads). Building the oracle's cache is set-up, not timed.
-    Returns (GB/s of cache rows processed, sample description, threads, seconds)."""
-    import numpy as np
-    from oracle import mla_oracle as O
-    from oracle.harness import f64, oracle_pool, seq_token_mask
-
-    threads = os.cpu_count()
+def blas_threads() -> int:
+    """Threads numpy's BLAS uses: the *_NUM_THREADS limit if one is set, else
+    threadpoolctl's report where it is installed, else the host's cores."""
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            return int(os.environ[v])
     try:
         from threadpoolctl import threadpool_info
         info = threadpool_info()
         if info:
-            threads = max(i.get("num_threads", 1) for i in info)
+            return max(i.get("num_threads", 1) for i in info)
     except Exception:
         pass
+    return os.cpu_count() or 1
+
+
+def cpu_oracle_run(w, d, seconds: float, absorbed: bool = False):
+    """Time the fp64 oracle on a bounded sample of the workload: whole sequences
+    with all heads, in order, until `seconds` of oracle work are done (the last
+    sequence may stop part-way through its heads). The non-absorbed form (K and
+    V materialised, one head at a time) is the oracle's definition; absorbed=True
+    times its absorbed form instead (q_lat = W_UK^T q_nope, scores and latent sum
+    over the cached rows, all heads at once). Building the oracle's cache is
+    set-up, not timed. Returns (GB/s of cache rows processed, sample
+    description, threads, seconds)."""
+    import numpy as np
+    from oracle import mla_oracle as O
+    from oracle.harness import f64, oracle_pool, seq_token_mask
+
+    threads = blas_threads()
     q_nope, q_rope, w_uk, w_uv = f64(d["q_nope"]), f64(d["q_rope"]), f64(d["w_uk"]), f64(d["w_uv"])
     bt = d["block_table"].numpy()
     H = w.heads
@@ -202,6 +222,18 @@ def cpu_oracle_run(w, d, seconds: float):
         L = int(w.seq_lens[b])
         t0 = time.perf_counter()
         rows = O.gather_rows(pool, sc, bt[b], L, w.page_size, w.cache_dtype)
+        if absorbed:
+            for j in range(w.q_len):
+                T = O.visible_tokens(L, w.q_len, j)
+                q_lat = O.absorb_q(q_nope[b, j], w_uk)
+                u, _ = O.attend_absorbed(q_lat, q_rope[b, j], rows[:T], O.default_scale())
+                O.out_proj(u, w_uv)
+            elapsed += time.perf_counter() - t0
+            done_bytes += L * w.row_bytes()
+            seqs += 1
+            if elapsed > seconds:
+                break
+            continue
         hd = 0
         for h in range(H):
             for j in range(w.q_len):
@@ -220,8 +252,36 @@ def cpu_oracle_run(w, d, seconds: float):
         if elapsed > seconds:
             break
     last = f"the last with {partial}/{H} heads" if partial else "all heads"
-    sample = f"{seqs} sequence(s) of {w.name} ({last}); non-absorbed fp64 oracle, one head at a time"
+    form = "absorbed fp64 oracle, all heads at once" if absorbed else "non-absorbed fp64 oracle, one head at a time"
+    sample = f"{seqs} sequence(s) of {w.name} ({last}); {form}"
     return done_bytes / elapsed / 1e9, sample, threads, elapsed
+
+
+def cpu_variants(workload: str, seconds: float):
+    """The oracle's other reported baselines, each in a child process so that
+    its BLAS thread count is set before numpy loads: the non-absorbed form on
+    one thread, and the absorbed form on one thread and on every thread."""
+    out = []
+    for absorbed, one in ((False, True), (True, False), (True, True)):
+        env = dict(os.environ)
+        if one:
+            for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+                env[v] = "1"
+        code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+                "from mla_latent_kv_16_gb300 import workloads as W; w = W.preset(%r); d = W.make_inputs(w); "
+                "v, s, t, e = bench.cpu_oracle_run(w, d, %r, absorbed=%r); "
+                "print(json.dumps({'value': v, 'sample': s, 'threads': t, 'seconds': e}))"
+                % (ROOT, workload, seconds, absorbed))
+        try:
+            r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+            res = json.loads(r.stdout.strip().splitlines()[-1])
+        except Exception as e:  # reported, not fatal: the main baseline stands
+            out.append({"form": "absorbed" if absorbed else "non-absorbed", "error": str(e)[:200]})
+            continue
+        out.append({"form": "absorbed" if absorbed else "non-absorbed", "value": round(res["value"], 4),
+                    "unit": UNIT, "cores": res["threads"], "sample": res["sample"],
+                    "seconds": round(res["seconds"], 2)})
+    return out
 
 
 def fused_setup(w, d_model: int):
@@ -522,7 +582,8 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample, thr, el = cpu_oracle_run(w, d, args.cpu_seconds)
         out["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": thr, "kind": "oracle",
-                               "sample": sample, "seconds": round(el, 2)}
+                               "sample": sample, "seconds": round(el, 2),
+                               "variants": cpu_variants(w.name, max(2.0, args.cpu_seconds / 2))}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

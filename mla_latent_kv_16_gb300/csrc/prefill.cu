@@ -50,6 +50,7 @@ constexpr int kBox = 128 * 128;   // 128 rows x 64 bf16
 constexpr int kStagesK = 2, kStagesV = 2;
 constexpr uint32_t kTmS = 0, kTmO = 256, kTmP = 384;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kHeadGroup = 16;
 
 struct __align__(1024) PfSmem {
   uint8_t q[3][kBox];
@@ -84,9 +85,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.heads, T = a.n_tokens, Tq = a.n_queries;
   const int n_qt = (Tq + kRowsTile - 1) / kRowsTile;
-  // the longest (last) query tiles first
-  const int h = static_cast<int>(blockIdx.x % static_cast<unsigned>(H));
-  const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / static_cast<unsigned>(H));
+  // Heads go in groups of up to 16, whose K and V (2 MB per head at 4096
+  // tokens) stay in L2 while every query tile of the group reads them; within
+  // a group the longest (last) query tiles go first.
+  const int G = min(kHeadGroup, H);
+  const int grp = static_cast<int>(blockIdx.x / static_cast<unsigned>(G * n_qt));
+  const int gh = min(G, H - grp * G);  // heads in this group (fewer in a last, partial one)
+  const int r_in = static_cast<int>(blockIdx.x) - grp * G * n_qt;
+  const int h = grp * G + r_in % gh;
+  const int qt = n_qt - 1 - r_in / gh;
   const int q0 = qt * kRowsTile;
   const int pos0 = T - Tq + q0;                              // position of the tile's first query
   const int pos_last = min(T - 1, pos0 + kRowsTile - 1);     // of its last real query
