@@ -59,6 +59,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    # decode workloads: override the workload's split count (0 = the library's policy)
+    p.add_argument("--num-splits", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     a = p.parse_args()
@@ -459,12 +461,13 @@ def run_ours(args):
     from mla_latent_kv_16_gb300.engine import build_layer, step_inputs
     capi.load()
 
-    w = W.preset(args.workload)
+    w = W.preset(args.workload, **({} if args.num_splits is None else {"num_splits": args.num_splits}))
     d = W.make_inputs(w)
     layer = build_layer(w, d)
     s = step_inputs(d)
     torch.cuda.synchronize()
     assert layer.device_error() == 0, "device error while filling the cache"
+    path = capi.mla_decode_kernel_path(layer.cache, layer.scales, w.page_size, w.heads, w.act_dtype, w.cache_dtype)
     # L2 flush by READING a buffer larger than L2: it evicts the previous step's
     # data and leaves only clean lines (a write would leave dirty lines whose
     # write-back would then compete with the timed step for HBM)
@@ -566,7 +569,9 @@ def run_ours(args):
         "vs_baseline": None, "dtype": w.cache_dtype, "data": "synthetic (seeded N(0,1) values, N(0,1/sqrt(512)) weights)",
         "config": {"workload": w.name, "batch": w.batch, "q_len": w.q_len, "heads": w.heads,
                    "seq_len": int(max(w.seq_lens)), "page_size": w.page_size, "cache_dtype": w.cache_dtype,
-                   "num_splits": splits, "l2": "flushed before every timed step by reading a 256 MiB buffer (clean lines); cache > L2",
+                   "num_splits": splits, "decode_kernel": {capi.MLA_DECODE_PATH_TENSOR_CORE: "tcgen05",
+                                                            capi.MLA_DECODE_PATH_CUDA_CORE: "cuda-core"}.get(path),
+                   "l2": "flushed before every timed step by reading a 256 MiB buffer (clean lines); cache > L2",
                    "parallelism": f"dp{world} (independent replicas, no collective)"},
         "tokens_per_s": round(tok_s, 1),
         "decode_call_ms": round(dec, 5),

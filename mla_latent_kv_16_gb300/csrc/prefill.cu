@@ -19,8 +19,9 @@
 //                (bf16) in TMEM as the A operand and V an MN-major operand
 // Warp 0 streams K and V tiles through TMA rings of two, warp 1 issues the
 // MMAs (QK of tile j + 1 before PV of tile j, so that the softmax of one tile
-// overlaps the other's products), warps 2-5 (one per TMEM lane quarter, thread
-// = query row) run the online softmax: running max with a lazy rescale of O
+// overlaps the other's products), warps 2-9 (two per TMEM lane quarter, thread
+// = query row, each warp half of the tile's keys) run the online softmax:
+// running max with a lazy rescale of O
 // (only when the max grows by more than 2^8), row sums of the bf16 weights the
 // PV product uses. Tiles past the query's position are not visited; the
 // diagonal ones are masked per element. Every wait is bounded; on a timeout
@@ -44,7 +45,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kPfThreads = 192;   // TMA warp, MMA warp, four softmax warps
+constexpr int kPfThreads = 320;   // TMA warp, MMA warp, eight softmax warps (two per TMEM lane quarter)
 constexpr int kRowsTile = 128;    // queries per CTA and keys per tile
 constexpr int kBox = 128 * 128;   // 128 rows x 64 bf16
 constexpr int kStagesK = 2, kStagesV = 2;
@@ -59,10 +60,12 @@ struct __align__(1024) PfSmem {
   uint64_t q_full;
   uint64_t k_full[kStagesK], k_empty[kStagesK];
   uint64_t v_full[kStagesV], v_empty[kStagesV];
-  uint64_t s_full[2], s_free[2];  // S of tile j in buffer j & 1: written by QK / read by the 4 softmax warps
-  uint64_t p_full[2];             // P of tile j in buffer j & 1 (and any O rescale) complete: 4 warps
+  uint64_t s_full[2], s_free[2];  // S of tile j in buffer j & 1: written by QK / read by the 8 softmax warps
+  uint64_t p_full[2];             // P of tile j in buffer j & 1 (and any O rescale) complete: 8 warps
   uint64_t p_free[2];             // PV of the tile that last used P buffer x is done
   uint64_t o_done, drain;
+  float mx_part[2][2][128];       // tile j's row max over key half t, in [j & 1][t]
+  float lsum[2][128];             // each softmax warp's row sum, for the epilogue
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -112,8 +115,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&sm->s_full[x]), 1);
-      mbar_init(smem_u32(&sm->s_free[x]), 4);
-      mbar_init(smem_u32(&sm->p_full[x]), 4);
+      mbar_init(smem_u32(&sm->s_free[x]), 8);
+      mbar_init(smem_u32(&sm->p_full[x]), 8);
       mbar_init(smem_u32(&sm->p_free[x]), 1);
     }
     mbar_init(smem_u32(&sm->o_done), 1);
@@ -237,8 +240,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
       pf_drain(smem_u32(&sm->drain), 0, a.dev_error);
     }
   } else {
-    // ================= softmax (warps 2-5), one query row per thread
+    // ================= softmax (warps 2-9): two warps per TMEM lane quarter,
+    // thread = query row, warp t the key columns [64t, 64t+64) of every tile.
+    // The two warps of a quarter meet once per tile on a named barrier that also
+    // ANDs their status, to combine their halves' row maxima (each then derives
+    // the same running max); a failed wait is carried to the next meeting, so
+    // both leave the loop together.
     const uint32_t q4 = static_cast<uint32_t>(warp & 3);
+    const int t = (warp - 2) >> 2;
     const int row = static_cast<int>(q4 * 32u) + lane;
     const int qpos = pos0 + row;  // this query's position in the sequence
     const uint32_t lanes = (q4 * 32u) << 16;
@@ -246,54 +255,74 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
     auto wwait = [&](uint64_t* bar, uint32_t par) {
       return __all_sync(0xffffffffu, mbar_wait<0>(smem_u32(bar), par, abort_flag, a.dev_error));
     };
+    auto meet = [&](bool v) -> bool {
+      switch (q4) {
+        case 0: return bar_red_and<1, 64>(v);
+        case 1: return bar_red_and<2, 64>(v);
+        case 2: return bar_red_and<3, 64>(v);
+        default: return bar_red_and<4, 64>(v);
+      }
+    };
     float m = -CUDART_INF_F, l = 0.0f;
     bool ok = true;
-    for (int j = 0; ok && j < n_kt; ++j) {
+    for (int j = 0; j < n_kt; ++j) {
       const int sb = j & 1;
-      if (!wwait(&sm->s_full[sb], (j >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      float s[128];
+      bool good = ok && wwait(&sm->s_full[sb], (j >> 1) & 1);
+      float s[64];
+      if (good) {
+        tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 128u + c * 32u, v);
+        for (int c = 0; c < 2; ++c) {
+          float v[32];
+          tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 128u + static_cast<uint32_t>(64 * t + 32 * c), v);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) s[32 * c + x] = v[x] * c2;  // log2 units
+          for (int x = 0; x < 32; ++x) s[32 * c + x] = v[x] * c2;  // log2 units
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
+        // causal mask: key k0 + x is visible to this query if k0 + x <= qpos
+        // (keys past the sequence end are past every query, so masked too)
+        const int k0 = j * kRowsTile + 64 * t;
+        if (k0 + 63 > pos0) {
+#pragma unroll
+          for (int x = 0; x < 64; ++x)
+            if (k0 + x > qpos) s[x] = -CUDART_INF_F;
+        }
+        float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int x = 4; x < 64; ++x) mx4[x & 3] = fmaxf(mx4[x & 3], s[x]);
+        sm->mx_part[sb][t][row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
-      // causal mask: key k0 + x is visible to this query if k0 + x <= qpos
-      // (keys past the sequence end are past every query, so masked too)
-      const int k0 = j * kRowsTile;
-      if (k0 + kRowsTile - 1 > pos0) {
-#pragma unroll
-        for (int x = 0; x < 128; ++x)
-          if (k0 + x > qpos) s[x] = -CUDART_INF_F;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int x = 1; x < 128; ++x) mx = fmaxf(mx, s[x]);
+      if (!meet(good)) { ok = false; break; }
+      const float mx = fmaxf(sm->mx_part[sb][0][row], sm->mx_part[sb][1][row]);
       const bool first = (j == 0);
       const float m_prev = m;
       const float m_new = fmaxf(m_prev, mx);
       const bool resc = !first && (m_new > m_prev + kRescaleLog2);
       const float m_use = (first || resc) ? m_new : m_prev;
-      uint32_t pw[64];
+      uint32_t pw[32];
       float rsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int x = 0; x < 64; ++x) {
+      for (int x = 0; x < 32; ++x) {
         pw[x] = pack_bf16x2(fast_exp2(s[2 * x] - m_use), fast_exp2(s[2 * x + 1] - m_use));
         rsum[x & 3] += __uint_as_float(pw[x] << 16) + __uint_as_float(pw[x] & 0xffff0000u);
       }
       l = (first ? 0.0f : l * fast_exp2(m_prev - m_use)) + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
-      // O rows rescale only after PV(j - 1) (phase (j - 1) >> 1 of p_free[(j - 1) & 1]);
-      // the P buffer of this tile was last read by PV(j - 2).
-      if (__any_sync(0xffffffffu, resc)) {
-        if (!wwait(&sm->p_free[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
+      m = m_use;
+      const bool resc_any = __any_sync(0xffffffffu, resc);
+      const float alpha = resc ? fast_exp2(m_prev - m_use) : 1.0f;
+      // P of this tile: the buffer was last read by PV(j - 2); this warp's 64
+      // keys are its columns [32t, 32t+32) (bf16 pairs)
+      if (j >= 2 && !wwait(&sm->p_free[sb], ((j - 2) >> 1) & 1)) { ok = false; continue; }
+      tc_fence_after();
+      tmem_st32(tmem + lanes + kTmP + static_cast<uint32_t>(sb) * 64u + static_cast<uint32_t>(32 * t), pw);
+      // O rows (this warp's 64 of the 128 columns) rescale only after PV(j - 1)
+      // (phase (j - 1) >> 1 of p_free[(j - 1) & 1])
+      if (resc_any) {
+        if (!wwait(&sm->p_free[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; continue; }
         tc_fence_after();
-        const float alpha = resc ? fast_exp2(m_prev - m_use) : 1.0f;
-        for (int c = 0; c < 128; c += 32) {
+        for (int c = 64 * t; c < 64 * t + 64; c += 32) {
           float o[32];
           tmem_ld32_sync(tmem + lanes + kTmO + static_cast<uint32_t>(c), o);
           uint32_t w32[32];
@@ -302,33 +331,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
           tmem_st32(tmem + lanes + kTmO + static_cast<uint32_t>(c), w32);
         }
       }
-      m = m_use;
-      if (j >= 2 && !wwait(&sm->p_free[sb], ((j - 2) >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t half[32];
-#pragma unroll
-      for (int x = 0; x < 32; ++x) half[x] = pw[x];
-      tmem_st32(tmem + lanes + kTmP + static_cast<uint32_t>(sb) * 64u, half);
-#pragma unroll
-      for (int x = 0; x < 32; ++x) half[x] = pw[32 + x];
-      tmem_st32(tmem + lanes + kTmP + static_cast<uint32_t>(sb) * 64u + 32u, half);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm->p_full[sb]));
     }
-    // ---- epilogue: o = O / l (bf16), lse; an aborted CTA writes NaN
-    ok = ok && wwait(&sm->o_done, 0);
+    // ---- epilogue: o = O / l (bf16), lse; an aborted CTA writes NaN. Both warps
+    // of a quarter hold the same running max, so the row sum is the sum of theirs.
+    sm->lsum[t][row] = l;
+    const bool done = meet(ok && wwait(&sm->o_done, 0));
     tc_fence_after();
+    const float l_row = sm->lsum[0][row] + sm->lsum[1][row];
     const int q = q0 + row;
-    const float inv_l = 1.0f / l;
-    // stage this warp's 32 rows x 256 bytes in the (idle) Q tile, then copy them
-    // out with consecutive lanes on consecutive addresses
-    uint8_t* stage = sm->q[0] + (warp - 2) * (32 * 256);
-    for (int c = 0; c < 4; ++c) {
+    const float inv_l = 1.0f / l_row;
+    // stage this warp's 32 rows x 128 bytes (its 64 columns) in the (idle) Q
+    // tile, then copy them out with consecutive lanes on consecutive addresses
+    uint8_t* stage = sm->q[0] + (warp - 2) * (32 * 128);
+    for (int c = 0; c < 2; ++c) {
       float o[32];
-      if (ok) {
-        tmem_ld32_sync(tmem + lanes + kTmO + static_cast<uint32_t>(c * 32), o);
+      if (done) {
+        tmem_ld32_sync(tmem + lanes + kTmO + static_cast<uint32_t>(64 * t + 32 * c), o);
       } else {
 #pragma unroll
         for (int k = 0; k < 32; ++k) o[k] = CUDART_NAN_F;
@@ -339,21 +361,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         const int cc = c * 4 + v;
-        *reinterpret_cast<uint4*>(stage + lane * 256 + ((cc ^ (lane & 15)) << 4)) =
+        *reinterpret_cast<uint4*>(stage + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
             make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
       }
     }
     __syncwarp();
     uint8_t* out = static_cast<uint8_t*>(a.o);
-    for (int k = 0; k < 16; ++k) {
-      const int r = k * 2 + (lane >> 4), ch = lane & 15;
+    for (int k = 0; k < 8; ++k) {
+      const int r = k * 4 + (lane >> 3), ch = lane & 7;
       const int qr = q0 + static_cast<int>(q4 * 32u) + r;
       if (qr < Tq)
-        *reinterpret_cast<uint4*>(out + (static_cast<int64_t>(qr) * H + h) * 256 + ch * 16) =
-            *reinterpret_cast<const uint4*>(stage + r * 256 + ((ch ^ (r & 15)) << 4));
+        *reinterpret_cast<uint4*>(out + (static_cast<int64_t>(qr) * H + h) * 256 + t * 128 + ch * 16) =
+            *reinterpret_cast<const uint4*>(stage + r * 128 + ((ch ^ (r & 7)) << 4));
     }
-    if (a.lse != nullptr && q < Tq)
-      a.lse[static_cast<int64_t>(q) * H + h] = ok ? (m + log2f(l)) * kLn2 : CUDART_NAN_F;
+    if (t == 0 && a.lse != nullptr && q < Tq)
+      a.lse[static_cast<int64_t>(q) * H + h] = done ? (m + log2f(l_row)) * kLn2 : CUDART_NAN_F;
   }
 
   __syncwarp();
