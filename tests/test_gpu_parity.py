@@ -53,11 +53,13 @@ SMALL = {
     "ragged_bf16": dict(batch=5, seq_lens=[1, 63, 64, 65, 1000]),
     "long_splitkv_bf16": dict(batch=2, seq_lens=[20000, 9000], num_splits=16),
     "fp8_lq2": dict(batch=3, seq_lens=[2, 130, 515]),
+    # two draft tokens on the bf16 cache (the query positions' causal cut on the bf16 kernel)
+    "dsv3_bf16_lq2": dict(batch=3, q_len=2, seq_lens=[2, 300, 1030], num_splits=2),
 }
 
 
 def _small(name):
-    return _W().preset(name, **SMALL[name])
+    return _W().preset(name.replace("_lq2", "") if name.startswith("dsv3") else name, **SMALL[name])
 
 
 # ----------------------------------------------------------------------------- append
