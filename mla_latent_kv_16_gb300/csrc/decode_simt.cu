@@ -163,6 +163,32 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
   }
 }
 
+constexpr int kFewSplits = 4;
+
+// The merged row of (query bj, head h): this lane's 16 columns of u = acc / sum,
+// and lse = mx + log(sum) (lane 0).
+template <typename T>
+__device__ __forceinline__ void combine_store(const DecodeArgs& a, int bj, int h, int lane, const float (&acc)[16],
+                                              bool none, float mx, float sum) {
+  const float inv = none ? 0.0f : 1.0f / sum;
+  const int64_t row = static_cast<int64_t>(bj) * a.heads + h;
+  T* u = static_cast<T*>(a.u_out) + row * kDC + lane * 16;
+  if constexpr (sizeof(T) == 2) {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = pack_bf16x2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+    uint4* d = reinterpret_cast<uint4*>(u);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  } else {
+    float4* d = reinterpret_cast<float4*>(u);
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      d[v] = make_float4(acc[4 * v] * inv, acc[4 * v + 1] * inv, acc[4 * v + 2] * inv, acc[4 * v + 3] * inv);
+  }
+  if (lane == 0 && a.lse_out != nullptr) a.lse_out[row] = none ? -CUDART_INF_F : mx + logf(sum);
+}
+
 // Split-KV merge ("Model Architecture Driving Inference Systems" §4.1, split
 // KV with a log-sum-exp combine): u = sum_s e^(lse_s - lse*) u_s / sum_s
 // e^(lse_s - lse*), lse = lse* + log sum_s e^(lse_s - lse*). One warp per
@@ -177,6 +203,49 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
   if (h >= a.heads) return;
   const int S = a.num_splits;
   const float* lse_s = a.part_lse + static_cast<int64_t>(bj) * S * a.heads + h;  // stride a.heads
+  if (S <= kFewSplits) {
+    // Few splits (the common case): every split's log-sum-exp and partial
+    // columns are requested at once, so the merge costs one memory round trip.
+    // A split whose lse is -inf is selected out, never multiplied (its partial
+    // may hold anything).
+    float ls[kFewSplits];
+    float4 x[kFewSplits][4];
+#pragma unroll
+    for (int s = 0; s < kFewSplits; ++s) {
+      if (s < S) {
+        ls[s] = lse_s[static_cast<int64_t>(s) * a.heads];
+        const float4* src = reinterpret_cast<const float4*>(
+            a.part_u + ((static_cast<int64_t>(bj) * S + s) * a.heads + h) * kDC + lane * 16);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) x[s][v] = src[v];
+      } else {
+        ls[s] = -CUDART_INF_F;
+      }
+    }
+    float mx = ls[0];
+#pragma unroll
+    for (int s = 1; s < kFewSplits; ++s) mx = fmaxf(mx, ls[s]);
+    const bool none = (mx == -CUDART_INF_F);
+    float sum = 0.0f;
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+#pragma unroll
+    for (int s = 0; s < kFewSplits; ++s) {
+      const bool use = !none && ls[s] != -CUDART_INF_F;
+      const float wv = use ? fast_exp2((ls[s] - mx) * kLog2e) : 0.0f;
+      sum += wv;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        acc[4 * v] = use ? fmaf(wv, x[s][v].x, acc[4 * v]) : acc[4 * v];
+        acc[4 * v + 1] = use ? fmaf(wv, x[s][v].y, acc[4 * v + 1]) : acc[4 * v + 1];
+        acc[4 * v + 2] = use ? fmaf(wv, x[s][v].z, acc[4 * v + 2]) : acc[4 * v + 2];
+        acc[4 * v + 3] = use ? fmaf(wv, x[s][v].w, acc[4 * v + 3]) : acc[4 * v + 3];
+      }
+    }
+    combine_store<T>(a, bj, h, lane, acc, none, mx, sum);
+    return;
+  }
   float mx = -CUDART_INF_F;
   for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lse_s[static_cast<int64_t>(s) * a.heads]);
   mx = warp_max(mx);
@@ -207,23 +276,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
       }
     }
   }
-  const float inv = none ? 0.0f : 1.0f / sum;
-  const int64_t row = static_cast<int64_t>(bj) * a.heads + h;
-  T* u = static_cast<T*>(a.u_out) + row * kDC + lane * 16;
-  if constexpr (sizeof(T) == 2) {
-    uint32_t w[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) w[k] = pack_bf16x2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
-    uint4* d = reinterpret_cast<uint4*>(u);
-    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  } else {
-    float4* d = reinterpret_cast<float4*>(u);
-#pragma unroll
-    for (int v = 0; v < 4; ++v)
-      d[v] = make_float4(acc[4 * v] * inv, acc[4 * v + 1] * inv, acc[4 * v + 2] * inv, acc[4 * v + 3] * inv);
-  }
-  if (lane == 0 && a.lse_out != nullptr) a.lse_out[row] = none ? -CUDART_INF_F : mx + logf(sum);
+  combine_store<T>(a, bj, h, lane, acc, none, mx, sum);
 }
 
 // Opt the kernel into its dynamic shared memory once per device (a host call
