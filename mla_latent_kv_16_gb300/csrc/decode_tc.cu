@@ -27,6 +27,8 @@
 //
 // TMEM (512 columns): O half [0,256), two score buffers [256,320) and
 // [320,384), Q's own latent half as bf16 pairs [384,512) (A of the QK MMAs).
+// The rows (TMEM lanes) of Q, S, P and O are heads in an order rotated by 64
+// in one CTA, so that each CTA's own heads occupy the same two lane quarters.
 // Shared memory: a 4-deep ring of page halves (4 boxes of 64 tokens x 64
 // columns, 128-byte swizzle), a RoPE box, Q's RoPE part, two P tiles
 // (A of the PV MMAs), two inboxes for the peer's partial scores.
@@ -48,7 +50,7 @@
 //
 // E4M3 cache ("Multi-Head Latent Attention (MLA): ..." "High-Throughput Serving
 // Kernels": FP8 latent cache with per-block scales): the TMA brings each page
-// half as bytes into the upper half of its slot, and two more warps decode it
+// half as bytes into the upper half of its slot, and six more warps decode it
 // in place to bf16 x (per-token, per-group) scale in the same swizzled layout
 // before the slot is marked full; everything after that is the bf16 path.
 //
@@ -67,11 +69,15 @@ namespace {
 
 using namespace tc;
 
+// Warps: 0 = TMA, 1 = TMEM allocation + MMA issue, then (E4M3 cache only) the
+// converter warps, then eight softmax / forwarding warps (two per TMEM lane
+// quarter; warp w may access lane quarter w mod 4).
 constexpr int kSmxWarps = 8;
-constexpr int kSmxThreads = kSmxWarps * 32;
-constexpr int kThreads = 64 + kSmxThreads;
-constexpr int kCvtWarp0 = 2 + kSmxWarps;  // first of the two E4M3 converter warps
-__host__ __device__ constexpr int threads_for(bool fp8) { return kThreads + (fp8 ? 64 : 0); }
+constexpr int kCvtWarps = 6;  // E4M3 -> bf16 converter warps (E4M3 cache)
+__host__ __device__ constexpr int smx_warp0(bool fp8) { return 2 + (fp8 ? kCvtWarps : 0); }
+__host__ __device__ constexpr int threads_for(bool fp8) { return 32 * (smx_warp0(fp8) + kSmxWarps); }
+// (E4M3: 16 warps, so at most 128 registers per thread; the softmax code then
+// spills a few bytes, less than a per-warpgroup register split would.)
 constexpr int kFp8BoxBytes = 64 * 64;  // 64 rows x 64 bytes of E4M3
 constexpr int kTileTok = 64;
 constexpr int kStages = 4;                  // ring of page halves
@@ -87,6 +93,15 @@ constexpr uint32_t kTmS = 256;  // two partial-score buffers of 64 columns
 constexpr uint32_t kTmQ = 384;  // Q's own latent half: 128 columns of bf16 pairs
 // Lazy rescale: keep a stale row max until the new one exceeds it by 2^8.
 constexpr float kRescaleLog2 = 8.0f;
+// The lane quarters (2*kOwnQ, 2*kOwnQ + 1) that hold a CTA's own heads, in both
+// CTAs of the pair (the head order in TMEM is rotated by 64 where needed). Warp
+// w runs on SM sub-partition w mod 4, and the softmax warps of the own heads
+// are the busiest: they go where nothing else heavy runs. bf16 cache: quarters
+// 2-3, away from the TMA (warp 0) and MMA (warp 1) issuers. E4M3 cache:
+// quarters 0-1, whose sub-partitions hold one converter warp each (warps 4,
+// 5) where quarters 2-3 hold two (warps 2, 6 and 3, 7).
+template <bool kFp8>
+constexpr uint32_t kOwnQ = kFp8 ? 0u : 1u;
 
 struct __align__(1024) Smem {
   uint8_t kv[kStages][kHalfBytes];  // own latent half of page i in slot i % 4; slots 1-2 first stage Q
@@ -112,7 +127,7 @@ struct __align__(1024) Smem {
   uint64_t p_full[2];               // P of page i complete in tile i & 1 and O rescaled (4 warps)
   uint64_t o_done, sum_bar, l_bar, drain;
   uint64_t raw_full[kStages], raw_rope_full;  // E4M3 bytes landed (TMA)
-  uint64_t cvt_bar;                           // both converter warps have read their page
+  uint64_t cvt_bar;                           // every converter warp has read its chunks of the page
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t peer_abort;  // the peer's abort flag, stored here by the peer at teardown
@@ -150,6 +165,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t r = cluster_ctarank();  // latent half of O and head half of the softmax this CTA owns
   const uint32_t peer = r ^ 1u;
+  // TMEM lane L (row of Q, S, P and O) holds head (L + rot) mod 128, so that in
+  // both CTAs the own heads [64r, 64r+64) sit in lane quarters 2*kOwnQ and
+  // 2*kOwnQ+1, i.e. on the same two SM sub-partitions (see kOwnQ).
+  const uint32_t rot = 64u * (r ^ kOwnQ<kFp8>);
 
   // ---- work item: (sequence b, query j, split) -- identical in both CTAs
   const int item = blockIdx.x >> 1;
@@ -165,15 +184,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
   // they finish: programmatic dependent launch), then the wait for them
   pdl_trigger();
   if (threadIdx.x == 0) {
-    // E4M3: the converter warps (2) complete full_kv / full_rope, the TMA raw_full
+    // E4M3: the converter warps complete full_kv / full_rope, the TMA raw_full
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sm->full_kv[s]), kFp8 ? 2 : 1);
+      mbar_init(smem_u32(&sm->full_kv[s]), kFp8 ? kCvtWarps : 1);
       mbar_init(smem_u32(&sm->empty_kv[s]), 1);
       mbar_init(smem_u32(&sm->raw_full[s]), 1);
     }
     mbar_init(smem_u32(&sm->raw_rope_full), 1);
-    mbar_init(smem_u32(&sm->cvt_bar), 2);
-    mbar_init(smem_u32(&sm->full_rope), kFp8 ? 2 : 1);
+    mbar_init(smem_u32(&sm->cvt_bar), kCvtWarps);
+    mbar_init(smem_u32(&sm->full_rope), kFp8 ? kCvtWarps : 1);
     mbar_init(smem_u32(&sm->empty_rope), 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&sm->s_full[x]), 1);
@@ -205,8 +224,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
   if (threadIdx.x == 0) {
     // Q's RoPE part -> qr; Q's own latent half -> slots 1-2, from where the
     // softmax warps copy it into TMEM before pages 1 and 2 are loaded there
+    // (two 64-row boxes: smem rows [64x, 64x+64) take heads (64x + rot) mod 128)
     mbar_arrive_expect_tx(smem_u32(&sm->q_smem_full), kQBoxBytes);
-    tma_load_2d_nohint(smem_u32(sm->qr), &rmap, smem_u32(&sm->q_smem_full), 0, static_cast<int32_t>(row0));
+    for (uint32_t x = 0; x < 2; ++x)
+      tma_load_2d_nohint(smem_u32(sm->qr) + x * (kQBoxBytes / 2), &rmap, smem_u32(&sm->q_smem_full), 0,
+                         static_cast<int32_t>(row0 + ((64u * x + rot) & 127u)));
     mbar_arrive_expect_tx(smem_u32(&sm->q_tm_full), 4 * kQBoxBytes);
     for (int k = 0; k < 4; ++k)
       tma_load_2d_nohint(smem_u32(sm->kv[1]) + k * kQBoxBytes, &qmap, smem_u32(&sm->q_tm_full), col_half + 64 * k,
@@ -468,17 +490,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       mma_commit(smem_u32(&sm->drain));
       drain_wait(smem_u32(&sm->drain), 0, a.dev_error);
     }
-  } else if (kFp8 && warp >= kCvtWarp0) {
+  } else if (kFp8 && warp < smx_warp0(kFp8)) {
     // ================= E4M3 -> bf16 (x scale) in place
     // The raw bytes of box k (64 rows x 64 B, unswizzled) sit at kHalfBytes/2 +
-    // k * 4 KB of the slot. Converter thread c (0..63) takes the 16-byte chunks
-    // g = 64 j + c, j = 0..15 (box g / 256, row (g / 4) mod 64, chunk g mod 4), so
-    // every warp-wide load reads 512 contiguous bytes (no bank conflicts); the
-    // RoPE box's 256 chunks go the same way, j = 0..3. A thread's chunks cover
-    // rows c/4 + 16m (m = 0..3) of every box, so it needs 8 latent scales (groups
-    // 2r for boxes 0-1, 2r+1 for boxes 2-3) and, on RoPE pages, 4 RoPE scales.
-    const int c = (warp - kCvtWarp0) * 32 + lane;
-    const int row_base = c >> 2, chunk = c & 3;
+    // k * 4 KB of the slot: 1,024 chunks of 16 bytes, chunk g in box g / 256,
+    // row (g / 4) mod 64, column chunk g mod 4 (the RoPE box's 256 chunks the
+    // same way). Converter thread c (0..191) takes the chunks g = c + 192 j, so
+    // every warp-wide load reads 512 contiguous bytes (no bank conflicts). Each
+    // chunk has one scale: (its token row, group 2r + box / 2), or the RoPE group.
+    constexpr int kCvtThreads = kCvtWarps * 32;
+    constexpr int kLatChunks = 4 * kFp8BoxBytes / 16, kRopeChunks = kFp8BoxBytes / 16;
+    constexpr int kJLat = (kLatChunks + kCvtThreads - 1) / kCvtThreads;
+    constexpr int kJRope = (kRopeChunks + kCvtThreads - 1) / kCvtThreads;
+    const int c = (warp - 2) * 32 + lane;
     const float* scales = a.scales;
     bool ok = true;
     // (x, y) * sc with one packed fp32 multiply (each product rounded once, as two
@@ -491,8 +515,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           : "f"(v.x), "f"(v.y), "f"(sc));
       return pack_bf16x2(__uint_as_float(static_cast<uint32_t>(p)), __uint_as_float(static_cast<uint32_t>(p >> 32)));
     };
-    // 16 E4M3 values (one uint4) x scale -> 16 bf16 (two 16-byte chunks)
-    auto convert16 = [&](const uint4& x, float sc, uint4& lo, uint4& hi) {
+    // 16 E4M3 values (one uint4) x scale -> 16 bf16, written as two 16-byte
+    // chunks of the 128-byte swizzled row at dst_row
+    auto convert16 = [&](const uint4& x, float sc, uint8_t* dst_row, int rr, int ch) {
       const uint32_t wds[4] = {x.x, x.y, x.z, x.w};
       uint32_t outw[8];
 #pragma unroll
@@ -506,21 +531,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           outw[2 * q + hh] = pack_bf16x2_scaled(f, sc);
         }
       }
-      lo = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-      hi = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+      *reinterpret_cast<uint4*>(dst_row + (((2 * ch) ^ (rr & 7)) << 4)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+      *reinterpret_cast<uint4*>(dst_row + (((2 * ch + 1) ^ (rr & 7)) << 4)) =
+          make_uint4(outw[4], outw[5], outw[6], outw[7]);
     };
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int slot = i % kStages;
       const bool rope_page = (i & 1) == static_cast<int>(r);
       const int tok = tok_begin + i * kTileTok;
       const int64_t y0 = static_cast<int64_t>(bt[tok / P]) * P + (tok % P);  // pool row of page row 0
-      float sc_lat[4][2], sc_rope[4];
+      // this thread's scales, fetched before the page lands
+      float sc_lat[kJLat], sc_rope[kJRope];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float* srow = scales + (y0 + row_base + 16 * m) * MLA_E4M3_GROUPS;
-        sc_lat[m][0] = srow[2 * r];
-        sc_lat[m][1] = srow[2 * r + 1];
-        sc_rope[m] = rope_page ? srow[4] : 0.0f;
+      for (int j = 0; j < kJLat; ++j) {
+        const int g = c + kCvtThreads * j;
+        sc_lat[j] = g < kLatChunks ? scales[(y0 + ((g >> 2) & 63)) * MLA_E4M3_GROUPS + 2 * r + (g >> 9)] : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kJRope; ++j) {
+        const int g = c + kCvtThreads * j;
+        sc_rope[j] = (rope_page && g < kRopeChunks) ? scales[(y0 + (g >> 2)) * MLA_E4M3_GROUPS + 4] : 0.0f;
       }
       if (!__all_sync(0xffffffffu, mbar_wait<kPlain>(smem_u32(&sm->raw_full[slot]), (i / kStages) & 1, abort_flag,
                                                       a.dev_error))) { ok = false; break; }
@@ -528,12 +558,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
                                                                    abort_flag, a.dev_error))) { ok = false; break; }
       // read every chunk first: the bf16 output overlaps the raw bytes of other chunks
       uint8_t* kvs = sm->kv[slot];
-      uint4 raw[16], rraw[4];
+      uint4 raw[kJLat], rraw[kJRope];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) raw[j] = *reinterpret_cast<const uint4*>(kvs + kHalfBytes / 2 + (j * 64 + c) * 16);
+      for (int j = 0; j < kJLat; ++j) {
+        const int g = c + kCvtThreads * j;
+        if (g < kLatChunks) raw[j] = *reinterpret_cast<const uint4*>(kvs + kHalfBytes / 2 + g * 16);
+      }
       if (rope_page) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) rraw[j] = *reinterpret_cast<const uint4*>(sm->rope + kBoxBytes / 2 + (j * 64 + c) * 16);
+        for (int j = 0; j < kJRope; ++j) {
+          const int g = c + kCvtThreads * j;
+          if (g < kRopeChunks) rraw[j] = *reinterpret_cast<const uint4*>(sm->rope + kBoxBytes / 2 + g * 16);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm->cvt_bar));
@@ -542,24 +578,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
         break;
       }
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int k = j >> 2, m = j & 3;  // box; which of this thread's rows
-        const int rr = row_base + 16 * m;
-        uint4 lo, hi;
-        convert16(raw[j], sc_lat[m][k >> 1], lo, hi);
-        uint8_t* dst = kvs + k * kBoxBytes + rr * 128;
-        *reinterpret_cast<uint4*>(dst + (((2 * chunk) ^ (rr & 7)) << 4)) = lo;
-        *reinterpret_cast<uint4*>(dst + (((2 * chunk + 1) ^ (rr & 7)) << 4)) = hi;
+      for (int j = 0; j < kJLat; ++j) {
+        const int g = c + kCvtThreads * j;
+        if (g < kLatChunks) {
+          const int k = g >> 8, rr = (g >> 2) & 63;  // box, row
+          convert16(raw[j], sc_lat[j], kvs + k * kBoxBytes + rr * 128, rr, g & 3);
+        }
       }
       if (rope_page) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int rr = row_base + 16 * j;
-          uint4 lo, hi;
-          convert16(rraw[j], sc_rope[j], lo, hi);
-          uint8_t* dst = sm->rope + rr * 128;
-          *reinterpret_cast<uint4*>(dst + (((2 * chunk) ^ (rr & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(dst + (((2 * chunk + 1) ^ (rr & 7)) << 4)) = hi;
+        for (int j = 0; j < kJRope; ++j) {
+          const int g = c + kCvtThreads * j;
+          if (g < kRopeChunks) convert16(rraw[j], sc_rope[j], sm->rope + (g >> 2) * 128, g >> 2, g & 3);
         }
       }
       fence_proxy_async_smem();  // generic writes -> the MMAs' operand reads
@@ -572,9 +602,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
   } else {
     // ================= softmax (own heads) / forwarding (peer's heads), epilogue
     const uint32_t q4 = static_cast<uint32_t>(warp & 3);  // TMEM lane quarter
-    const int t = (warp - 2) >> 2;                        // token half of a page; O column half
-    const bool own = (q4 >> 1) == r;                      // rows of this CTA's heads
-    const int h = static_cast<int>(q4 * 32u) + lane;      // head = TMEM lane
+    const int t = (warp - smx_warp0(kFp8)) >> 2;          // token half of a page; O column half
+    const bool own = (q4 >> 1) == kOwnQ<kFp8>;            // rows of this CTA's heads
+    const int h = static_cast<int>(q4 * 32u) + lane;      // TMEM lane (row of Q, S, P, O)
+    const int hd = (h + static_cast<int>(rot)) & 127;     // the head it holds
     const int hl = h & 63;                                // index among the owner's 64 heads
     const uint32_t lanes = (q4 * 32u) << 16;
     const uint32_t tO = tmem + lanes + kTmO + t * 128, tQ = tmem + lanes + kTmQ;
@@ -598,7 +629,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
         uint32_t rq[32];
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
-          const uint8_t* box = sm->kv[1] + (t * 2 + bb) * kQBoxBytes + h * 128;
+          const uint8_t* box = sm->kv[1] + (t * 2 + bb) * kQBoxBytes + hd * 128;  // (hd & 7 == h & 7)
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 x = *reinterpret_cast<const uint4*>(box + ((c ^ (h & 7)) << 4));
@@ -727,7 +758,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           // chunk-major ([16-byte chunk][32 rows]), so that each warp-wide st.async
           // writes 512 contiguous bytes; the peer's P-path warp swizzles them in place.
           uint8_t* prow = sm->pt[sb] + h * 128;
-          const uint32_t remote = peer_pt + static_cast<uint32_t>(sb * kPTileBytes) + q4 * 32u * 128u + lane * 16u;
+          // (in the peer these heads sit in the other pair of lane quarters, q4 ^ 2)
+          const uint32_t remote =
+              peer_pt + static_cast<uint32_t>(sb * kPTileBytes) + (q4 ^ 2u) * 32u * 128u + lane * 16u;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int ch = 4 * t + c;
@@ -850,9 +883,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       const float lse = (m + log2f(l_row)) * kLn2;
       if (t == 0 && ok) {
         if (S == 1) {
-          if (a.lse_out != nullptr) a.lse_out[row0 + h] = lse;
+          if (a.lse_out != nullptr) a.lse_out[row0 + hd] = lse;
         } else {
-          a.part_lse[(static_cast<int64_t>(bj) * S + split) * 128 + h] = lse;
+          a.part_lse[(static_cast<int64_t>(bj) * S + split) * 128 + hd] = lse;
         }
       }
     } else {
@@ -863,11 +896,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
       tc_fence_after();
       const float inv_l = 1.0f / l_row;
       const uint32_t c_out = static_cast<uint32_t>(col_half) + t * 128;
+      const int head0 = static_cast<int>((q4 * 32u + rot) & 127u);  // first head of this warp's 32 rows
       // The page ring is idle once O is complete: each warp stages its 32 rows x
       // 128 columns there (16-byte chunks XOR-swizzled by row against bank
       // conflicts) and copies them out with consecutive lanes on consecutive
       // addresses, instead of one row per lane.
-      const int wl = warp - 2;
+      const int wl = warp - smx_warp0(kFp8);
       if (S == 1) {
         uint8_t* stage = sm->kv[0] + wl * (32 * 256);
         for (int c = 0; c < 4; ++c) {
@@ -884,7 +918,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           }
         }
         __syncwarp();
-        uint8_t* u = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(a.u_out) + (row0 + q4 * 32) * kDC + c_out);
+        uint8_t* u = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(a.u_out) + (row0 + head0) * kDC + c_out);
 #pragma unroll 4
         for (int k = 0; k < 16; ++k) {
           const int row = k * 2 + (lane >> 4), ch = lane & 15;
@@ -904,7 +938,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           }
         }
         __syncwarp();
-        const int64_t prow0 = (static_cast<int64_t>(bj) * S + split) * 128 + q4 * 32;
+        const int64_t prow0 = (static_cast<int64_t>(bj) * S + split) * 128 + head0;
         uint8_t* pu = reinterpret_cast<uint8_t*>(a.part_u + prow0 * kDC + c_out);
 #pragma unroll 4
         for (int row = 0; row < 32; ++row)
@@ -1019,9 +1053,9 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   CUtensorMap map, qmap, rmap;
   const uint64_t q_rows = static_cast<uint64_t>(a.batch) * a.q_len * 128;
   // cache as [num_pages*page_size rows][576] bf16, 64 x 64 boxes; q_lat as
-  // [batch*q_len*128 rows][512] and q_rope as [..][64], 128 x 64 boxes
+  // [batch*q_len*128 rows][512] (128 x 64 boxes) and q_rope as [..][64] (64 x 64 boxes)
   if (!cache.get(a.cache, static_cast<uint64_t>(a.num_pages) * a.page_size, kRow, kTileTok, &map, fp8) ||
-      !cache.get(a.q_lat, q_rows, kDC, 128, &qmap) || !cache.get(a.q_rope, q_rows, kDRope, 128, &rmap))
+      !cache.get(a.q_lat, q_rows, kDC, 128, &qmap) || !cache.get(a.q_rope, q_rows, kDRope, 64, &rmap))
     return cudaErrorInvalidValue;
   const int64_t items = static_cast<int64_t>(a.batch) * a.q_len * a.num_splits;
   const dim3 grid(static_cast<unsigned>(2 * items));
