@@ -246,33 +246,45 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
     combine_store<T>(a, bj, h, lane, acc, none, mx, sum);
     return;
   }
-  float mx = -CUDART_INF_F;
-  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lse_s[static_cast<int64_t>(s) * a.heads]);
+  // Many splits: the maximum log-sum-exp first (lane s holds split s's for
+  // S <= 32), then the splits in groups of kFewSplits whose partial columns are
+  // all requested at once: 1 + ceil(S / kFewSplits) memory round trips.
+  const float ls_lane = lane < S ? lse_s[static_cast<int64_t>(lane) * a.heads] : -CUDART_INF_F;
+  float mx = ls_lane;
+  for (int s = lane + 32; s < S; s += 32) mx = fmaxf(mx, lse_s[static_cast<int64_t>(s) * a.heads]);
   mx = warp_max(mx);
   const bool none = (mx == -CUDART_INF_F);
   float sum = 0.0f;
-  for (int s = lane; s < S; s += 32) {
-    const float ls = lse_s[static_cast<int64_t>(s) * a.heads];
-    sum += (none || ls == -CUDART_INF_F) ? 0.0f : fast_exp2((ls - mx) * kLog2e);
-  }
-  sum = warp_sum(sum);
   float acc[16];
 #pragma unroll
   for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
-  if (!none) {
-    for (int s = 0; s < S; ++s) {
-      const float ls = lse_s[static_cast<int64_t>(s) * a.heads];
-      if (ls == -CUDART_INF_F) continue;
-      const float wv = fast_exp2((ls - mx) * kLog2e);
-      const float4* src = reinterpret_cast<const float4*>(
-          a.part_u + ((static_cast<int64_t>(bj) * S + s) * a.heads + h) * kDC + lane * 16);
+  for (int s0 = 0; !none && s0 < S; s0 += kFewSplits) {
+    float ls[kFewSplits];
+    float4 x[kFewSplits][4];
+#pragma unroll
+    for (int u = 0; u < kFewSplits; ++u) {
+      const int s = s0 + u;  // uniform across the warp
+      if (s < S) {
+        ls[u] = S <= 32 ? __shfl_sync(0xffffffffu, ls_lane, s) : lse_s[static_cast<int64_t>(s) * a.heads];
+        const float4* src = reinterpret_cast<const float4*>(
+            a.part_u + ((static_cast<int64_t>(bj) * S + s) * a.heads + h) * kDC + lane * 16);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) x[u][v] = src[v];
+      } else {
+        ls[u] = -CUDART_INF_F;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kFewSplits; ++u) {
+      const bool use = ls[u] != -CUDART_INF_F;  // a -inf split is selected out, never multiplied
+      const float wv = use ? fast_exp2((ls[u] - mx) * kLog2e) : 0.0f;
+      sum += wv;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        const float4 x = src[v];
-        acc[4 * v] = fmaf(wv, x.x, acc[4 * v]);
-        acc[4 * v + 1] = fmaf(wv, x.y, acc[4 * v + 1]);
-        acc[4 * v + 2] = fmaf(wv, x.z, acc[4 * v + 2]);
-        acc[4 * v + 3] = fmaf(wv, x.w, acc[4 * v + 3]);
+        acc[4 * v] = use ? fmaf(wv, x[u][v].x, acc[4 * v]) : acc[4 * v];
+        acc[4 * v + 1] = use ? fmaf(wv, x[u][v].y, acc[4 * v + 1]) : acc[4 * v + 1];
+        acc[4 * v + 2] = use ? fmaf(wv, x[u][v].z, acc[4 * v + 2]) : acc[4 * v + 2];
+        acc[4 * v + 3] = use ? fmaf(wv, x[u][v].w, acc[4 * v + 3]) : acc[4 * v + 3];
       }
     }
   }
