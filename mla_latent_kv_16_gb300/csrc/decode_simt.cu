@@ -31,22 +31,63 @@ __device__ __forceinline__ float ld_act(const void* base, int64_t idx) {
   return ActIO<T>::load(static_cast<const T*>(base) + idx);
 }
 
+// One cached row (576 values) as 16-byte chunks: 144 of fp32, 72 of bf16, 36 of E4M3.
 template <int kCache>
-__device__ __forceinline__ void load_row(const void* cache, const float* scales, int64_t slot, int k0,
-                                         float* dst, int lane) {
-  // lane-strided copy of one 576-value row into fp32 shared memory
-  if constexpr (kCache == MLA_F32) {
-    const float* r = static_cast<const float*>(cache) + slot * kRow;
-    for (int k = k0 + lane; k < kRow; k += 32) dst[k] = r[k];
-  } else if constexpr (kCache == MLA_BF16) {
-    const uint16_t* r = static_cast<const uint16_t*>(cache) + slot * kRow;
-    for (int k = k0 + lane; k < kRow; k += 32) dst[k] = bf16_bits_to_f32(r[k]);
-  } else {
-    const uint8_t* r = static_cast<const uint8_t*>(cache) + slot * kRow;
-    const float* sc = scales + slot * kGroups;
-    // dequantised value rounded to the bf16 operand type the E4M3 cache pairs with
-    for (int k = k0 + lane; k < kRow; k += 32)
-      dst[k] = bf16_bits_to_f32(f32_to_bf16_bits(e4m3_to_f32(r[k]) * sc[k >> 7]));
+struct RowChunks {
+  static constexpr int kBytes = kCache == MLA_F32 ? 4 : (kCache == MLA_BF16 ? 2 : 1);
+  static constexpr int kPer = 16 / kBytes;   // values per chunk
+  static constexpr int kN = kRow / kPer;     // chunks per row
+  static constexpr int kK = (kN + 31) / 32;  // chunks per lane
+};
+
+// Rows of one tile into fp32 shared memory, warp w taking rows w, w + 8, ...:
+// every 16-byte load of the warp's rows is issued before any is used, so a
+// tile costs one memory round trip instead of one per load. Rows past the
+// visible range are zero-filled (poisoned page tails never enter).
+template <int kCache>
+__device__ __forceinline__ void load_tile_rows(const DecodeArgs& a, const int32_t* bt, int t0, int end, float* rs,
+                                               int warp, int lane) {
+  using RC = RowChunks<kCache>;
+  constexpr int kRowsPerWarp = kTile / 8;
+  uint4 v[kRowsPerWarp][RC::kK];
+  int64_t slot[kRowsPerWarp];
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int tok = t0 + warp + 8 * r;
+    slot[r] = tok < end ? static_cast<int64_t>(bt[tok / a.page_size]) * a.page_size + tok % a.page_size : -1;
+    const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.cache) +
+                                                      (slot[r] < 0 ? 0 : slot[r]) * (kRow * RC::kBytes));
+#pragma unroll
+    for (int k = 0; k < RC::kK; ++k) {
+      const int c = lane + 32 * k;
+      v[r][k] = (slot[r] >= 0 && c < RC::kN) ? row[c] : make_uint4(0, 0, 0, 0);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    float* dst = rs + (warp + 8 * r) * kRowPad;
+    const float* sc = kCache == MLA_E4M3 && slot[r] >= 0 ? a.scales + slot[r] * kGroups : nullptr;
+#pragma unroll
+    for (int k = 0; k < RC::kK; ++k) {
+      const int c = lane + 32 * k;
+      if (c >= RC::kN) continue;
+      const uint32_t w[4] = {v[r][k].x, v[r][k].y, v[r][k].z, v[r][k].w};
+      const int k0 = c * RC::kPer;
+      if constexpr (kCache == MLA_F32) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[k0 + e] = __uint_as_float(w[e]);
+      } else if constexpr (kCache == MLA_BF16) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dst[k0 + e] = bf16_bits_to_f32(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
+      } else {
+        // dequantised value rounded to the bf16 operand type the E4M3 cache pairs with
+        const float s = sc != nullptr ? sc[k0 >> 7] : 0.0f;  // a chunk lies in one 128-wide group
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          dst[k0 + e] = bf16_bits_to_f32(
+              f32_to_bf16_bits(e4m3_to_f32(static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)))) * s));
+      }
+    }
   }
 }
 
@@ -109,24 +150,20 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
   const int end = bad ? tok_begin : tok_end;
   for (int t0 = tok_begin; t0 < end; t0 += kTile) {
     __syncthreads();
-    // warp w loads rows t0 + w, t0 + w + 8, ...
-    for (int r = warp; r < kTile; r += 8) {
-      const int tok = t0 + r;
-      float* dst = rs + r * kRowPad;
-      if (tok < end) {
-        const int64_t slot = static_cast<int64_t>(bt[tok / P]) * P + tok % P;
-        load_row<kCache>(a.cache, a.scales, slot, 0, dst, lane);
-      } else {
-        for (int k = lane; k < kRow; k += 32) dst[k] = 0.0f;
-      }
-    }
+    load_tile_rows<kCache>(a, bt, t0, end, rs, warp, lane);
     __syncthreads();
     if (head_ok) {
       const float* qh = qs + warp * kRow;
       const float* rr = rs + lane * kRowPad;
-      float s = 0.0f;
+      float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four chains (summed in a fixed order)
 #pragma unroll 8
-      for (int k = 0; k < kRow; ++k) s = fmaf(qh[k], rr[k], s);
+      for (int k = 0; k < kRow; k += 4) {
+        s4[0] = fmaf(qh[k], rr[k], s4[0]);
+        s4[1] = fmaf(qh[k + 1], rr[k + 1], s4[1]);
+        s4[2] = fmaf(qh[k + 2], rr[k + 2], s4[2]);
+        s4[3] = fmaf(qh[k + 3], rr[k + 3], s4[3]);
+      }
+      float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
       if (t0 + lane >= end) s = -CUDART_INF_F;
       const float m_new = fmaxf(m, warp_max(s));
       const float alpha = fast_exp2(m - m_new);   // m = -inf on the first tile -> 0
