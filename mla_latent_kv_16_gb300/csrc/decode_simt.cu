@@ -328,6 +328,87 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
   combine_store<T>(a, bj, h, lane, acc, none, mx, sum);
 }
 
+// The same merge for many splits (S > kManySplits): one CTA of eight warps per
+// (query, head) row. Every warp finds the row's maximum log-sum-exp itself (so
+// all weights share one reference and no rescaling between warps is needed),
+// merges the groups of four splits 4w, 4w + 32, ... with their partials all
+// requested at once, and the eight sums and 512-column rows are added in
+// shared memory in warp order. Each row then costs ceil(S / 32) + 1 round
+// trips instead of ceil(S / 4) + 1, with eight times the loads in flight.
+constexpr int kManySplits = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(256) combine_many_kernel(DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float4 red[8][kDC / 4];
+  __shared__ float red_sum[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x, bj = blockIdx.y;
+  const int S = a.num_splits;
+  const float* lse_s = a.part_lse + static_cast<int64_t>(bj) * S * a.heads + h;  // stride a.heads
+  float mx = -CUDART_INF_F;
+  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lse_s[static_cast<int64_t>(s) * a.heads]);
+  mx = warp_max(mx);
+  const bool none = (mx == -CUDART_INF_F);
+  float sum = 0.0f;
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+  for (int s0 = kFewSplits * warp; !none && s0 < S; s0 += 8 * kFewSplits) {
+    float ls[kFewSplits];
+    float4 x[kFewSplits][4];
+#pragma unroll
+    for (int u = 0; u < kFewSplits; ++u) {
+      const int s = s0 + u;  // uniform across the warp
+      if (s < S) {
+        ls[u] = lse_s[static_cast<int64_t>(s) * a.heads];
+        const float4* src = reinterpret_cast<const float4*>(
+            a.part_u + ((static_cast<int64_t>(bj) * S + s) * a.heads + h) * kDC + lane * 16);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) x[u][v] = src[v];
+      } else {
+        ls[u] = -CUDART_INF_F;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kFewSplits; ++u) {
+      const bool use = ls[u] != -CUDART_INF_F;  // a -inf split is selected out, never multiplied
+      const float wv = use ? fast_exp2((ls[u] - mx) * kLog2e) : 0.0f;
+      sum += wv;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        acc[4 * v] = use ? fmaf(wv, x[u][v].x, acc[4 * v]) : acc[4 * v];
+        acc[4 * v + 1] = use ? fmaf(wv, x[u][v].y, acc[4 * v + 1]) : acc[4 * v + 1];
+        acc[4 * v + 2] = use ? fmaf(wv, x[u][v].z, acc[4 * v + 2]) : acc[4 * v + 2];
+        acc[4 * v + 3] = use ? fmaf(wv, x[u][v].w, acc[4 * v + 3]) : acc[4 * v + 3];
+      }
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < 4; ++v)
+    red[warp][lane * 4 + v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+  if (lane == 0) red_sum[warp] = sum;
+  __syncthreads();
+  if (warp != 0) return;
+  float tot = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    tot += red_sum[w];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float4 y = red[w][lane * 4 + v];
+      acc[4 * v] += y.x;
+      acc[4 * v + 1] += y.y;
+      acc[4 * v + 2] += y.z;
+      acc[4 * v + 3] += y.w;
+    }
+  }
+  combine_store<T>(a, bj, h, lane, acc, none, mx, tot);
+}
+
 // Opt the kernel into its dynamic shared memory once per device (a host call
 // that costs microseconds, kept out of every launch).
 template <typename K>
@@ -368,7 +449,12 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s) {
 
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
   if (a.batch == 0 || a.num_splits == 1) return cudaSuccess;
-  dim3 grid((a.heads + 3) / 4, a.batch * a.q_len);
+  if (a.num_splits > kManySplits) {
+    const dim3 grid(a.heads, a.batch * a.q_len);
+    if (a.act == MLA_F32) return launch_pdl(combine_many_kernel<float>, grid, dim3(256), 0, s, a);
+    return launch_pdl(combine_many_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, a);
+  }
+  const dim3 grid((a.heads + 3) / 4, a.batch * a.q_len);
   if (a.act == MLA_F32) return launch_pdl(combine_kernel<float>, grid, dim3(128), 0, s, a);
   return launch_pdl(combine_kernel<__nv_bfloat16>, grid, dim3(128), 0, s, a);
 }
