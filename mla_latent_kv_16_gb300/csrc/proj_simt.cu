@@ -36,10 +36,15 @@ __global__ void __launch_bounds__(128) absorb_simt_kernel(ProjArgs a) {
   float acc[kAbsorbTok];
 #pragma unroll
   for (int t = 0; t < kAbsorbTok; ++t) acc[t] = 0.0f;
-  for (int d = 0; d < kDNope; ++d) {
-    const float wv = ActIO<T>::load(w + d * kDC + c);
+  // 16 rows of W_UK requested at once: 8 memory round trips per thread, not 128
+  for (int d0 = 0; d0 < kDNope; d0 += 16) {
+    float wv[16];
 #pragma unroll
-    for (int t = 0; t < kAbsorbTok; ++t) acc[t] = fmaf(qs[t][d], wv, acc[t]);
+    for (int i = 0; i < 16; ++i) wv[i] = ActIO<T>::load(w + (d0 + i) * kDC + c);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+#pragma unroll
+      for (int t = 0; t < kAbsorbTok; ++t) acc[t] = fmaf(qs[t][d0 + i], wv[i], acc[t]);
   }
   T* y = static_cast<T*>(a.y);
 #pragma unroll
@@ -67,17 +72,22 @@ __global__ void __launch_bounds__(128) out_proj_simt_kernel(ProjArgs a) {
   }
   __syncthreads();
   T* y = static_cast<T*>(a.y);
-  for (int d = warp; d < kDV; d += 4) {
-    float wr[16];
+  // four rows of W_UV per warp requested at once (64 loads in flight per lane)
+  for (int d0 = warp; d0 < kDV; d0 += 16) {
+    float wr[4][16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) wr[i] = ActIO<T>::load(w + d * kDC + lane + 32 * i);
-    for (int t = 0; t < kOutTok; ++t) {
-      float p = 0.0f;
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int i = 0; i < 16; ++i) p = fmaf(wr[i], us[t][lane + 32 * i], p);
-      p = warp_sum(p);
-      if (lane == 0 && t0 + t < a.n_tokens)
-        ActIO<T>::store(y + (static_cast<int64_t>(t0 + t) * a.heads + h) * kDV + d, p);
+      for (int i = 0; i < 16; ++i) wr[r][i] = ActIO<T>::load(w + (d0 + 4 * r) * kDC + lane + 32 * i);
+    for (int t = 0; t < kOutTok && t0 + t < a.n_tokens; ++t) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        float p = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) p = fmaf(wr[r][i], us[t][lane + 32 * i], p);
+        p = warp_sum(p);
+        if (lane == 0) ActIO<T>::store(y + (static_cast<int64_t>(t0 + t) * a.heads + h) * kDV + d0 + 4 * r, p);
+      }
     }
   }
 }
