@@ -271,13 +271,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
       float s[64];
       if (good) {
         tc_fence_after();
+        // this warp's 64 key columns in one TMEM load (one round trip)
+        tmem_ld64_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 128u + static_cast<uint32_t>(64 * t), s);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float v[32];
-          tmem_ld32_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 128u + static_cast<uint32_t>(64 * t + 32 * c), v);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) s[32 * c + x] = v[x] * c2;  // log2 units
-        }
+        for (int x = 0; x < 64; ++x) s[x] *= c2;  // log2 units
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
