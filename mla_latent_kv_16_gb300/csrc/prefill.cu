@@ -18,8 +18,9 @@
 //   O += P V   : M = 128 queries, N = 128 (d_v), K = 128 keys (8 MMAs), with P
 //                (bf16) in TMEM as the A operand and V an MN-major operand
 // Warp 0 streams K and V tiles through TMA rings of two, warp 1 issues the
-// MMAs (QK of tile j + 1 before PV of tile j, so that the softmax of one tile
-// overlaps the other's products), warps 2-9 (two per TMEM lane quarter, thread
+// QK products and warp 10 the PV products, each as soon as its inputs are
+// ready (two issuing threads: the tensor pipe interleaves their MMAs, and the
+// softmax of one tile overlaps the products of the others), warps 2-9 (two per TMEM lane quarter, thread
 // = query row, each warp half of the tile's keys) run the online softmax:
 // running max with a lazy rescale of O
 // (only when the max grows by more than 2^8), row sums of the bf16 weights the
@@ -45,7 +46,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int kPfThreads = 320;   // TMA warp, MMA warp, eight softmax warps (two per TMEM lane quarter)
+// TMA warp, QK-issue warp, eight softmax warps (two per TMEM lane quarter), PV-issue warp
+constexpr int kPfThreads = 352;
+constexpr int kPvWarp = 10;
 constexpr int kRowsTile = 128;    // queries per CTA and keys per tile
 constexpr int kBox = 128 * 128;   // 128 rows x 64 bf16
 constexpr int kStagesK = 2, kStagesV = 2;
@@ -63,7 +66,7 @@ struct __align__(1024) PfSmem {
   uint64_t s_full[2], s_free[2];  // S of tile j in buffer j & 1: written by QK / read by the 8 softmax warps
   uint64_t p_full[2];             // P of tile j in buffer j & 1 (and any O rescale) complete: 8 warps
   uint64_t p_free[2];             // PV of the tile that last used P buffer x is done
-  uint64_t o_done, drain;
+  uint64_t o_done, drain, drain_pv;
   float mx_part[2][2][128];       // tile j's row max over key half t, in [j & 1][t]
   float lsum[2][128];             // each softmax warp's row sum, for the epilogue
   uint32_t tmem_base;
@@ -121,6 +124,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
     }
     mbar_init(smem_u32(&sm->o_done), 1);
     mbar_init(smem_u32(&sm->drain), 1);
+    mbar_init(smem_u32(&sm->drain_pv), 1);
     sm->abort_flag = 0;
     fence_mbar_init_cluster();
     prefetch_tmap(&maps.q);
@@ -191,18 +195,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
       pf_drain(smem_u32(&sm->q_full), 0, a.dev_error);
     }
   } else if (warp == 1) {
-    // ================= MMA issuer: QK(0); then per tile j: QK(j + 1), PV(j)
+    // ================= QK issue: S(j) = Q K(j)^T as soon as K(j) has landed and
+    // score buffer j & 1 has been read out. The PV products are issued by
+    // another warp: an issuing thread stays busy while the tensor pipe takes
+    // its MMAs, so with one thread for both a ready PV waited behind the next
+    // QK's issue, and the next QK behind the PV.
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t kIdPV = idesc_bf16_f32(128, 128, false, true);
       const uint64_t dQ = sdesc_sw128(smem_u32(sm->q[0]), 16, 1024);
       const uint64_t dK = sdesc_sw128(smem_u32(sm->k[0][0]), 16, 1024);
-      const uint64_t dV = sdesc_sw128(smem_u32(sm->v[0][0]), kBox, 1024);  // MN-major: boxes of 64 d apart
-      auto issue_qk = [&](int j) -> bool {
+      bool ok = mbar_wait<2>(smem_u32(&sm->q_full), 0, abort_flag, a.dev_error);
+      for (int j = 0; ok && j < n_kt; ++j) {
         const int s = j % kStagesK, sb = j & 1;
-        if (!mbar_wait<2>(smem_u32(&sm->k_full[s]), (j / kStagesK) & 1, abort_flag, a.dev_error)) return false;
-        if (j >= 2 && !mbar_wait<2>(smem_u32(&sm->s_free[sb]), ((j - 2) >> 1) & 1, abort_flag, a.dev_error))
-          return false;
+        ok = mbar_wait<2>(smem_u32(&sm->k_full[s]), (j / kStagesK) & 1, abort_flag, a.dev_error);
+        if (ok && j >= 2) ok = mbar_wait<2>(smem_u32(&sm->s_free[sb]), ((j - 2) >> 1) & 1, abort_flag, a.dev_error);
+        if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + kTmS + static_cast<uint32_t>(sb) * 128u;
         const uint64_t dk = dK + static_cast<uint64_t>((s * 3 * kBox) >> 4);
@@ -213,12 +220,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
         }
         mma_commit(smem_u32(&sm->k_empty[s]));
         mma_commit(smem_u32(&sm->s_full[sb]));
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {
+      }
+      mma_commit(smem_u32(&sm->drain));
+      pf_drain(smem_u32(&sm->drain), 0, a.dev_error);
+    }
+  } else if (warp == kPvWarp) {
+    // ================= PV issue: O += P(j) V(j) once P(j) is complete (P in TMEM)
+    if (lane == 0) {
+      constexpr uint32_t kIdPV = idesc_bf16_f32(128, 128, false, true);
+      const uint64_t dV = sdesc_sw128(smem_u32(sm->v[0][0]), kBox, 1024);  // MN-major: boxes of 64 d apart
+      bool ok = true;
+      for (int j = 0; ok && j < n_kt; ++j) {
         const int s = j % kStagesV, pb = j & 1;
-        if (!mbar_wait<2>(smem_u32(&sm->p_full[pb]), (j >> 1) & 1, abort_flag, a.dev_error)) return false;
-        if (!mbar_wait<2>(smem_u32(&sm->v_full[s]), (j / kStagesV) & 1, abort_flag, a.dev_error)) return false;
+        ok = mbar_wait<2>(smem_u32(&sm->p_full[pb]), (j >> 1) & 1, abort_flag, a.dev_error) &&
+             mbar_wait<2>(smem_u32(&sm->v_full[s]), (j / kStagesV) & 1, abort_flag, a.dev_error);
+        if (!ok) break;
         tc_fence_after();
         const uint64_t dv = dV + static_cast<uint64_t>((s * 2 * kBox) >> 4);
 #pragma unroll
@@ -228,16 +244,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
         mma_commit(smem_u32(&sm->v_empty[s]));
         mma_commit(smem_u32(&sm->p_free[pb]));
         if (j == n_kt - 1) mma_commit(smem_u32(&sm->o_done));
-        return true;
-      };
-      bool ok = mbar_wait<2>(smem_u32(&sm->q_full), 0, abort_flag, a.dev_error);
-      ok = ok && issue_qk(0);
-      for (int j = 0; ok && j < n_kt; ++j) {
-        if (j + 1 < n_kt) ok = issue_qk(j + 1);
-        ok = ok && issue_pv(j);
       }
-      mma_commit(smem_u32(&sm->drain));
-      pf_drain(smem_u32(&sm->drain), 0, a.dev_error);
+      mma_commit(smem_u32(&sm->drain_pv));
+      pf_drain(smem_u32(&sm->drain_pv), 0, a.dev_error);
     }
   } else {
     // ================= softmax (warps 2-9): two warps per TMEM lane quarter,
