@@ -890,7 +890,9 @@ def run_prefill(args):
                    "parallelism": "dp1 (one sequence)"},
         "tokens_per_s": round(T / (ms * 1e-3), 1),
         "roofline": {"bound": "tensor", "achieved": round(tfs, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(tfs / peak, 4), "traffic": None,
+                     "frac": round(tfs / peak, 4),
+                     "traffic": recorded_traffic(os.path.join(ROOT, "mla_latent_kv_16_gb300", "csrc", "prefill.cu"),
+                                                 PREFILL_WORKLOAD, prefix="prefill_attn"),
                      "kernel": "mla_prefill_mha (2 tcgen05 expansion GEMMs + causal attention), algorithmic FLOPs",
                      "peak_source": f"bf16_tflops of {src}"},
         "e2e": {"value": round(fl / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 5),
