@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
     const int qpos = pos0 + row;  // this query's position in the sequence
     const uint32_t lanes = (q4 * 32u) << 16;
     const float c2 = a.softmax_scale * kLog2e;
+    const float masked = c2 >= 0.0f ? -CUDART_INF_F : CUDART_INF_F;  // raw score whose scaled value is -inf
     auto wwait = [&](uint64_t* bar, uint32_t par) {
       return __all_sync(0xffffffffu, mbar_wait<0>(smem_u32(bar), par, abort_flag, a.dev_error));
     };
@@ -281,24 +282,31 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
       if (good) {
         tc_fence_after();
         // this warp's 64 key columns in one TMEM load (one round trip)
+        // raw scores; the scale into log2 units is folded into each exponent's FMA below
         tmem_ld64_sync(tmem + lanes + kTmS + static_cast<uint32_t>(sb) * 128u + static_cast<uint32_t>(64 * t), s);
-#pragma unroll
-        for (int x = 0; x < 64; ++x) s[x] *= c2;  // log2 units
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm->s_free[sb]));
         // causal mask: key k0 + x is visible to this query if k0 + x <= qpos
-        // (keys past the sequence end are past every query, so masked too)
+        // (keys past the sequence end are past every query, so masked too); a
+        // masked score is the one whose scaled value is -inf
         const int k0 = j * kRowsTile + 64 * t;
         if (k0 + 63 > pos0) {
 #pragma unroll
           for (int x = 0; x < 64; ++x)
-            if (k0 + x > qpos) s[x] = -CUDART_INF_F;
+            if (k0 + x > qpos) s[x] = masked;
         }
+        // the largest scaled score: the raw maximum (or minimum, for a negative scale) times c2
         float mx4[4] = {s[0], s[1], s[2], s[3]};
+        if (c2 >= 0.0f) {
 #pragma unroll
-        for (int x = 4; x < 64; ++x) mx4[x & 3] = fmaxf(mx4[x & 3], s[x]);
-        sm->mx_part[sb][t][row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          for (int x = 4; x < 64; ++x) mx4[x & 3] = fmaxf(mx4[x & 3], s[x]);
+          sm->mx_part[sb][t][row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c2;
+        } else {
+#pragma unroll
+          for (int x = 4; x < 64; ++x) mx4[x & 3] = fminf(mx4[x & 3], s[x]);
+          sm->mx_part[sb][t][row] = fminf(fminf(mx4[0], mx4[1]), fminf(mx4[2], mx4[3])) * c2;
+        }
       }
       if (!meet(good)) { ok = false; break; }
       const float mx = fmaxf(sm->mx_part[sb][0][row], sm->mx_part[sb][1][row]);
@@ -311,7 +319,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
       float rsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int x = 0; x < 32; ++x) {
-        pw[x] = pack_bf16x2(fast_exp2(s[2 * x] - m_use), fast_exp2(s[2 * x + 1] - m_use));
+        pw[x] = pack_bf16x2(fast_exp2(fmaf(s[2 * x], c2, -m_use)), fast_exp2(fmaf(s[2 * x + 1], c2, -m_use)));
         rsum[x & 3] += __uint_as_float(pw[x] << 16) + __uint_as_float(pw[x] & 0xffff0000u);
       }
       l = (first ? 0.0f : l * fast_exp2(m_prev - m_use)) + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
