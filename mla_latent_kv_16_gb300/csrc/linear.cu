@@ -10,7 +10,10 @@
 // and an n x 64 box of x, both 128-byte swizzled) without a break between
 // units, an MMA warp accumulates each unit in one of two TMEM buffers, and four
 // epilogue warps empty the other. Rows of W past n_out read as zero and are
-// not written. With a K split (or when the caller asks for fp32 sums) the
+// not written. With many tokens (512 or more, n_out % 8 == 0: a prefill's
+// expansion of the latent rows) the roles swap: 128 tokens are M and 256 rows
+// of W are N, K whole, so that each epilogue thread writes one token's 256
+// outputs as 16-byte vectors. With a K split (or when the caller asks for fp32 sums) the
 // partial sums go to an fp32 workspace and a second kernel adds them in split
 // order, so results do not depend on timing. Other types and shapes run on
 // CUDA cores.
@@ -39,6 +42,13 @@ constexpr int kABytes = 128 * 128;  // one W box: 128 rows x 64 bf16
 constexpr int kMaxStages = 12;
 constexpr int kMaxSplits = 32;
 constexpr int kRingBudget = 200 * 1024;  // shared memory for the TMA ring
+// Many tokens (a prefill's expansion of the latent rows): the roles swap, 128
+// tokens are the MMA M dimension and 256 rows of W are N, so that a thread of
+// the epilogue holds 256 consecutive outputs of one token and writes them as
+// 16-byte vectors (with rows of W as M, a warp's store covers 32 outputs x 2
+// bytes of one token).
+constexpr int kTmMinTok = 512;
+constexpr int kTmOut = 256;
 
 struct LinearCtl {
   uint64_t full[kMaxStages];
@@ -97,8 +107,18 @@ struct Unit {
   int o0, split, t0, c_lo, nc;
 };
 
-__device__ __forceinline__ Unit unit_at(const LinearArgs& p, int u, int o_tiles, int chunks) {
+__device__ __forceinline__ Unit unit_at(const LinearArgs& p, int u, int o_tiles, int chunks, bool tm) {
   Unit r;
+  if (tm) {
+    // tokens as M: 128 tokens x 256 rows of W, K whole
+    const int ot = (p.n_out + kTmOut - 1) / kTmOut;
+    r.o0 = (u % ot) * kTmOut;
+    r.t0 = (u / ot) * 128;
+    r.split = 0;
+    r.c_lo = 0;
+    r.nc = chunks;
+    return r;
+  }
   const int rest = u / o_tiles;
   r.o0 = (u - rest * o_tiles) * 128;
   r.split = rest % p.k_splits;
@@ -116,7 +136,8 @@ __device__ __forceinline__ Unit unit_at(const LinearArgs& p, int u, int o_tiles,
 __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const __grid_constant__ CUtensorMap amap,
                                                                 const __grid_constant__ CUtensorMap bmap,
                                                                 LinearArgs p, int n_tile, int stages,
-                                                                uint32_t acc_cols, int units) {
+                                                                uint32_t acc_cols, int units, int tm_flag) {
+  const bool tm = tm_flag != 0;  // tokens as M (x in the A slot, W in the B slot of each stage)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int b_bytes = n_tile * 128;
@@ -166,9 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const __grid_con
           tma_load_2d_nohint(dst, &amap, bar, xk, o0);
       };
       uint32_t pre = 0;  // chunks whose W box was requested before the wait
-      if (p.w_static) {
+      if (p.w_static && !tm) {
         for (int u = blockIdx.x; u < units && pre < static_cast<uint32_t>(stages); u += gridDim.x) {
-          const Unit w = unit_at(p, u, o_tiles, chunks);
+          const Unit w = unit_at(p, u, o_tiles, chunks, tm);
           for (int k = 0; k < w.nc && pre < static_cast<uint32_t>(stages); ++k, ++pre) {
             const uint32_t bar = smem_u32(&ctl->full[pre]);
             mbar_arrive_expect_tx(bar, kABytes + b_bytes);
@@ -180,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const __grid_con
       uint32_t g = 0;  // chunks issued so far, over all of this CTA's units
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = unit_at(p, u, o_tiles, chunks);
+        const Unit w = unit_at(p, u, o_tiles, chunks, tm);
         for (int k = 0; k < w.nc; ++k, ++g) {
           const int s = static_cast<int>(g % stages);
           const uint32_t dst = smem_u32(base + s * stage_bytes);
@@ -193,9 +214,15 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const __grid_con
               break;
             }
             mbar_arrive_expect_tx(bar, kABytes + b_bytes);
-            load_w(dst, bar, xk, w.o0);
+            if (tm)
+              tma_load_2d_nohint(dst + kABytes, &amap, bar, xk, w.o0);  // 256 rows of W as B (past n_out: zero)
+            else
+              load_w(dst, bar, xk, w.o0);
           }
-          tma_load_2d_nohint(dst + kABytes, &bmap, bar, xk, w.t0);  // token rows past n read as zero
+          if (tm)
+            tma_load_2d_nohint(dst, &bmap, bar, xk, w.t0);  // 128 tokens of x as A (past n: zero)
+          else
+            tma_load_2d_nohint(dst + kABytes, &bmap, bar, xk, w.t0);  // token rows past n read as zero
         }
       }
       if (!ok) {
@@ -214,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const __grid_con
       bool ok = true;
       int i = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
-        const Unit w = unit_at(p, u, o_tiles, chunks);
+        const Unit w = unit_at(p, u, o_tiles, chunks, tm);
         const int b = i & 1;
         if (i >= 2 && !mbar_wait<2>(smem_u32(&ctl->acc_empty[b]), ((i >> 1) - 1) & 1, abort_flag, nullptr)) {
           ok = false;
@@ -251,12 +278,46 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const __grid_con
     bool ok = true;
     int i = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
-      const Unit w = unit_at(p, u, o_tiles, chunks);
+      const Unit w = unit_at(p, u, o_tiles, chunks, tm);
       const int b = i & 1;
       const bool got =
           __all_sync(0xffffffffu, ok && mbar_wait<0>(smem_u32(&ctl->acc_full[b]), (i >> 1) & 1, abort_flag, nullptr));
       ok = got;
       tc_fence_after();
+      if (tm) {
+        // thread = token (TMEM lane), columns = its 256 outputs o0 ...: 16-byte vectors
+        const int tok = w.t0 + q * 32 + lane;
+        for (int c = 0; c < kTmOut; c += 32) {
+          float v[32];
+          if (got) {
+            tmem_ld32_sync(tmem + static_cast<uint32_t>(b) * acc_cols + lanes + c, v);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = CUDART_NAN_F;  // an aborted unit reads as NaN
+          }
+          if (tok >= p.n_tokens) continue;
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {
+            const int o = w.o0 + c + 8 * g8;
+            if (o >= p.n_out) break;  // n_out % 8 == 0: a group of 8 is all in or all out
+            const int64_t idx = static_cast<int64_t>(tok) * p.n_out + o;
+            if (p.part == nullptr) {
+              uint32_t wd[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) wd[e] = pack_bf16x2(v[8 * g8 + 2 * e], v[8 * g8 + 2 * e + 1]);
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + idx) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            } else {
+              float4* d = reinterpret_cast<float4*>(p.part + idx);
+              d[0] = make_float4(v[8 * g8], v[8 * g8 + 1], v[8 * g8 + 2], v[8 * g8 + 3]);
+              d[1] = make_float4(v[8 * g8 + 4], v[8 * g8 + 5], v[8 * g8 + 6], v[8 * g8 + 7]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (got && lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[b]));
+        continue;
+      }
       const int n_tok = min(kMaxTok, p.n_tokens - w.t0);
       const int o = w.o0 + q * 32 + lane;
       for (int c = 0; c < n_tile; c += 32) {
@@ -346,6 +407,7 @@ struct LinearPlan {
   int grid;           // persistent CTAs: min(units, SMs)
   size_t smem;        // dynamic shared memory per CTA
   uint32_t acc_cols;  // TMEM columns of one of the two accumulators
+  bool tm;            // tokens as M (many tokens)
 };
 
 // Tile shape, ring depth and K split of the persistent tcgen05 kernel. One CTA
@@ -354,6 +416,23 @@ struct LinearPlan {
 // + about one chunk's worth of partial-sum traffic).
 LinearPlan plan_tc(int32_t n_tokens, int32_t n_out, int32_t n_in) {
   LinearPlan p{};
+  if (n_tokens >= kTmMinTok && n_out % 8 == 0) {
+    // tokens as M: units of 128 tokens x 256 rows of W, K whole
+    p.tm = true;
+    p.n_tile = kTmOut;
+    p.tok_tiles = (n_tokens + 127) / 128;
+    const int stage = kABytes + kTmOut * 128;
+    p.stages = kRingBudget / stage;
+    if (p.stages > kMaxStages) p.stages = kMaxStages;
+    p.smem = 1024 + static_cast<size_t>(p.stages) * stage + sizeof(LinearCtl);
+    p.acc_cols = kTmOut;
+    p.splits = 1;
+    const int64_t units = static_cast<int64_t>(p.tok_tiles) * ((n_out + kTmOut - 1) / kTmOut);
+    const int64_t sms = device_sm_count();
+    p.units = static_cast<int>(units);
+    p.grid = static_cast<int>(units < sms ? units : sms);
+    return p;
+  }
   p.n_tile = n_tokens >= kMaxTok ? kMaxTok : ((n_tokens + 15) / 16) * 16;
   p.tok_tiles = (n_tokens + kMaxTok - 1) / kMaxTok;
   const int stage = kABytes + ((p.n_tile * 128 + 1023) & ~1023);
@@ -412,9 +491,10 @@ cudaError_t launch_linear(const LinearArgs& a, cudaStream_t s, bool reduce) {
   const LinearPlan pl = plan_tc(a.n_tokens, a.n_out, a.n_in);
   if (pl.splits != a.k_splits || (pl.splits > 1 && a.part == nullptr)) return cudaErrorInvalidValue;
   CUtensorMap am, bm;
-  if (!encode_2d(&am, a.w, static_cast<uint64_t>(a.n_out), static_cast<uint64_t>(a.n_in), 128) ||
+  // boxes: W rows 128 (as A) or 256 (as B, tokens as M); x rows n_tile (as B) or 128 (as A)
+  if (!encode_2d(&am, a.w, static_cast<uint64_t>(a.n_out), static_cast<uint64_t>(a.n_in), pl.tm ? kTmOut : 128) ||
       !encode_2d(&bm, a.x, static_cast<uint64_t>(a.n_tokens), static_cast<uint64_t>(a.n_in),
-                 static_cast<uint32_t>(pl.n_tile), static_cast<uint64_t>(a.x_stride)))
+                 pl.tm ? 128u : static_cast<uint32_t>(pl.n_tile), static_cast<uint64_t>(a.x_stride)))
     return cudaErrorInvalidValue;
   static int attr_dev = -1;
   int dev = 0;
@@ -426,7 +506,7 @@ cudaError_t launch_linear(const LinearArgs& a, cudaStream_t s, bool reduce) {
     attr_dev = dev;
   }
   e = launch_pdl(linear_tc_kernel, dim3(pl.grid), dim3(kThreads), pl.smem, s, am, bm, a, pl.n_tile, pl.stages,
-                 pl.acc_cols, pl.units);
+                 pl.acc_cols, pl.units, pl.tm ? 1 : 0);
   if (e != cudaSuccess || a.part == nullptr || !reduce) return e;
   const int64_t n = static_cast<int64_t>(a.n_tokens) * a.n_out;
   if ((n + 255) / 256 > 0x7fffffff) return cudaErrorInvalidConfiguration;

@@ -39,13 +39,18 @@ def _W():
 
 
 # (act, n_tokens, n_out, n_in): tensor cores with a K split and a ragged last
-# row tile, the front end's first product, one token, two token tiles; CUDA
-# cores for n_in % 64 != 0 and for fp32
+# row tile, the front end's first product, one token, two token tiles; many
+# tokens (tokens as the MMA M dimension: ragged token and output tiles, and
+# n_out % 8 != 0, which keeps rows of W as M); CUDA cores for n_in % 64 != 0
+# and for fp32
 LINEAR_CASES = [
     ("bf16", 5, 200, 7168),
     ("bf16", 32, 2112, 7168),
     ("bf16", 1, 64, 128),
     ("bf16", 300, 256, 256),
+    ("bf16", 640, 264, 192),
+    ("bf16", 1000, 512, 512),
+    ("bf16", 600, 100, 64),
     ("bf16", 7, 96, 100),
     ("f32", 3, 70, 96),
 ]
