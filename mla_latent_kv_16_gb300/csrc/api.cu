@@ -55,8 +55,17 @@ int32_t resolve_splits(int32_t batch, int32_t q_len, int32_t max_pages, int32_t 
   const int64_t slots = tc ? sms / 2 : sms * 2;            // concurrent work items
   const int64_t per_item = tc ? 1 : (d.num_heads + 7) / 8;
   const int64_t items0 = static_cast<int64_t>(batch > 0 ? batch : 1) * q_len * per_item;
-  // cost = waves * (pages per split + partial-output overhead in page units)
-  const double part_cost = tc ? 2.0 : 0.5;
+  // Cost in the time one work item takes per page (measured on GB300 for the
+  // tensor-core kernel: ~1.6 us per 64-token bf16 page, ~1.9x that for E4M3, and
+  // ~8 us = 5 pages of set-up and epilogue per item):
+  //   waves x (pages per split + item overhead)
+  //   + the split partials' HBM traffic, written by the decode and read by the
+  //     merge (B Lq S H 513 x 4 bytes each way), at 6.8 TB/s
+  const double item_cost = tc ? 5.0 : 0.5;
+  const double page_us =
+      tc ? 1.6 * (page_size / 64.0) * (cache_dtype == MLA_E4M3 ? 1.9 : 1.0) : 1.0;
+  const double part_bytes_per_split =
+      2.0 * static_cast<double>(batch > 0 ? batch : 1) * q_len * d.num_heads * (512 + 1) * 4.0;  // u (512 fp32) + lse
   int32_t best = 1;
   double best_cost = 1e300;
   const int32_t smax = max_pages < 256 ? max_pages : 256;
@@ -65,7 +74,8 @@ int32_t resolve_splits(int32_t batch, int32_t q_len, int32_t max_pages, int32_t 
     const int32_t s_eff = static_cast<int32_t>((max_pages + pps - 1) / pps);
     if (s_eff != s) continue;
     const int64_t waves = (items0 * s + slots - 1) / slots;
-    const double cost = static_cast<double>(waves) * (static_cast<double>(pps) + (s > 1 ? part_cost : 0.0));
+    const double part_pages = s > 1 ? part_bytes_per_split * s / 6.8e6 / page_us : 0.0;
+    const double cost = static_cast<double>(waves) * (static_cast<double>(pps) + item_cost) + part_pages;
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;
