@@ -23,8 +23,10 @@
 // softmax of one tile overlaps the products of the others), warps 2-9 (two per TMEM lane quarter, thread
 // = query row, each warp half of the tile's keys) run the online softmax:
 // running max with a lazy rescale of O
-// (only when the max grows by more than 2^8), row sums of the bf16 weights the
-// PV product uses. Tiles past the query's position are not visited; the
+// (only when the max grows by more than 2^8), fp32 row sums of the weights
+// (before their bf16 rounding for the PV product: the two differ by at most one
+// bf16 rounding, and summing the rounded values cost the softmax 1.5 more
+// instructions per weight). Tiles past the query's position are not visited; the
 // diagonal ones are masked per element. Every wait is bounded; on a timeout
 // the CTA raises MLA_DEVERR_TIMEOUT, lets its own copies and MMAs land, writes
 // NaN outputs for its rows and frees TMEM.
@@ -319,8 +321,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
       float rsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int x = 0; x < 32; ++x) {
-        pw[x] = pack_bf16x2(fast_exp2(fmaf(s[2 * x], c2, -m_use)), fast_exp2(fmaf(s[2 * x + 1], c2, -m_use)));
-        rsum[x & 3] += __uint_as_float(pw[x] << 16) + __uint_as_float(pw[x] & 0xffff0000u);
+        const float p0 = fast_exp2(fmaf(s[2 * x], c2, -m_use)), p1 = fast_exp2(fmaf(s[2 * x + 1], c2, -m_use));
+        pw[x] = pack_bf16x2(p0, p1);
+        rsum[x & 3] += p0 + p1;
       }
       l = (first ? 0.0f : l * fast_exp2(m_prev - m_use)) + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
       m = m_use;
