@@ -740,8 +740,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
           const float p0 = fast_exp2(fmaf(s[2 * x], c2, -m_use));
           const float p1 = fast_exp2(fmaf(s[2 * x + 1], c2, -m_use));
           pw[x] = pack_bf16x2(p0, p1);
-          // normalise by the weights the PV product actually uses (bf16-rounded)
-          rsum[x & 3] += __uint_as_float(pw[x] << 16) + __uint_as_float(pw[x] & 0xffff0000u);
+          // fp32 row sum of the weights before their bf16 rounding for PV (the two
+          // differ by at most one bf16 rounding; the rounded values cost more instructions)
+          rsum[x & 3] += p0 + p1;
         }
         // this warp's row sum over its columns, carried to the new max
         l = (first ? 0.0f : l * fast_exp2(m_prev - m_use)) + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
