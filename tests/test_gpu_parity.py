@@ -145,7 +145,7 @@ def _check_latent(w, d, pool, sc, u_gpu, lse_gpu, q_gpu, seqs=None, what=""):
         assert_close(u_gpu[b], ru, **tol, what=f"{what} u seq {b}")
         if lse_gpu is not None:
             check_lse(lse_gpu[b], rl, q_gpu[b], q_ex[b], f64(d["q_rope"])[b], visible_rows(w, d, pool, sc, b),
-                      O.default_scale(), _eps_c(w), what=f"{what} lse seq {b}", p_bf16=w.act_dtype != "f32")
+                      O.default_scale(), _eps_c(w), what=f"{what} lse seq {b}")
     return ref
 
 
