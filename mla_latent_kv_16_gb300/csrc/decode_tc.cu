@@ -435,8 +435,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
         const uint64_t db = dKV0 + static_cast<uint64_t>(((i % kStages) * kHalfBytes) >> 4);
 #pragma unroll
         for (uint32_t kk = 0; kk < 16; ++kk)
-          mma_ts(dS, tmem + kTmQ + kk * 8u, db + (((kk >> 2) * kBoxBytes + (kk & 3u) * 32u) >> 4), kIdQK,
-                 kk > 0 ? 1u : 0u);
+          mma_ts<kIdQK>(dS, tmem + kTmQ + kk * 8u, db + (((kk >> 2) * kBoxBytes + (kk & 3u) * 32u) >> 4),
+                        kk > 0 ? 1u : 0u);
         if ((i & 1) == static_cast<int>(r)) {
 #pragma unroll
           for (uint32_t kk = 0; kk < 4; ++kk)

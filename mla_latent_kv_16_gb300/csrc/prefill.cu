@@ -241,8 +241,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const __gri
         const uint64_t dv = dV + static_cast<uint64_t>((s * 2 * kBox) >> 4);
 #pragma unroll
         for (uint32_t kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + kTmO, tmem + kTmP + static_cast<uint32_t>(pb) * 64u + kk * 8u, dv + ((kk * 16u * 128u) >> 4),
-                 kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts<kIdPV>(tmem + kTmO, tmem + kTmP + static_cast<uint32_t>(pb) * 64u + kk * 8u,
+                        dv + ((kk * 16u * 128u) >> 4), (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(smem_u32(&sm->v_empty[s]));
         mma_commit(smem_u32(&sm->p_free[pb]));
         if (j == n_kt - 1) mma_commit(smem_u32(&sm->o_done));

@@ -286,13 +286,22 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem desc]. The PTX ISA's operand rules for an A
+// matrix in tensor memory are checked on the descriptor at compile time: A is
+// K-major (the transpose-A bit is zero; only B may be MN-major), and with
+// cta_group::1 the tile is 128 rows (A fills all 128 lanes from lane 0, so the
+// caller's address carries only a column offset) and N a multiple of 16.
+template <uint32_t kIdesc>
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
+  static_assert(((kIdesc >> 15) & 1u) == 0u, "an A operand in tensor memory must be K-major");
+  static_assert(((kIdesc >> 24) & 0x1Fu) == (128u >> 4), "the tensor-memory A form is used with M = 128");
+  static_assert(((kIdesc >> 17) & 0x3Fu) != 0u && ((kIdesc >> 17) & 0x3Fu) <= (256u >> 3) &&
+                    ((kIdesc >> 17) & 1u) == 0u,
+                "with M = 128, N is a multiple of 16 in 16..256");
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "r"(a_tmem), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
       : "memory");
 }
 
