@@ -49,6 +49,9 @@ constexpr int kRingBudget = 200 * 1024;  // shared memory for the TMA ring
 // bytes of one token).
 constexpr int kTmMinTok = 512;
 constexpr int kTmOut = 256;
+// Epilogue staging with tokens as M: each epilogue warp's 32 tokens x 64
+// outputs (bf16, 4 KB), so that its stores cover whole 128-byte row segments.
+constexpr int kEpiStageBytes = 4 * 4096;
 
 struct LinearCtl {
   uint64_t full[kMaxStages];
@@ -142,7 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const __grid_con
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int b_bytes = n_tile * 128;
   const int stage_bytes = kABytes + ((b_bytes + 1023) & ~1023);
-  LinearCtl* ctl = reinterpret_cast<LinearCtl*>(base + stages * stage_bytes);
+  uint8_t* epi_stage = base + stages * stage_bytes;  // tokens as M: the epilogue warps' staging
+  LinearCtl* ctl = reinterpret_cast<LinearCtl*>(epi_stage + (tm ? kEpiStageBytes : 0));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int o_tiles = (p.n_out + 127) / 128;
   const int chunks = p.n_in / kChunkK;
@@ -285,29 +289,46 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const __grid_con
       ok = got;
       tc_fence_after();
       if (tm) {
-        // thread = token (TMEM lane), columns = its 256 outputs o0 ...: 16-byte vectors
-        const int tok = w.t0 + q * 32 + lane;
-        for (int c = 0; c < kTmOut; c += 32) {
-          float v[32];
+        // thread = token (TMEM lane) while reading TMEM, 64 outputs at a time. bf16
+        // outputs are staged in shared memory (16-byte chunk j of token row r at
+        // chunk j ^ (r mod 8), against bank conflicts) and stored as whole 128-byte
+        // row segments, four tokens per warp-wide store; a warp storing one 16-byte
+        // vector per token instead touched 32 rows per store. n_out % 8 == 0: a
+        // chunk of 8 outputs is all in or all out.
+        uint8_t* st = epi_stage + (warp - 2) * 4096;
+        const int tok0 = w.t0 + q * 32;
+        for (int c = 0; c < kTmOut; c += 64) {
+          float v[64];
           if (got) {
-            tmem_ld32_sync(tmem + static_cast<uint32_t>(b) * acc_cols + lanes + c, v);
+            tmem_ld64_sync(tmem + static_cast<uint32_t>(b) * acc_cols + lanes + c, v);
           } else {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = CUDART_NAN_F;  // an aborted unit reads as NaN
+            for (int k = 0; k < 64; ++k) v[k] = CUDART_NAN_F;  // an aborted unit reads as NaN
           }
-          if (tok >= p.n_tokens) continue;
+          if (p.part == nullptr) {
 #pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) {
-            const int o = w.o0 + c + 8 * g8;
-            if (o >= p.n_out) break;  // n_out % 8 == 0: a group of 8 is all in or all out
-            const int64_t idx = static_cast<int64_t>(tok) * p.n_out + o;
-            if (p.part == nullptr) {
-              uint32_t wd[4];
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                  make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                             pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+            __syncwarp();
 #pragma unroll
-              for (int e = 0; e < 4; ++e) wd[e] = pack_bf16x2(v[8 * g8 + 2 * e], v[8 * g8 + 2 * e + 1]);
-              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + idx) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-            } else {
-              float4* d = reinterpret_cast<float4*>(p.part + idx);
+            for (int k = 0; k < 8; ++k) {
+              const int row = 4 * k + (lane >> 3), j = lane & 7;
+              const int tok = tok0 + row, o = w.o0 + c + 8 * j;
+              const uint4 x = *reinterpret_cast<const uint4*>(st + row * 128 + ((j ^ (row & 7)) << 4));
+              if (tok < p.n_tokens && o < p.n_out)
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + static_cast<int64_t>(tok) * p.n_out + o) = x;
+            }
+            __syncwarp();  // the staging area is rewritten by the next 64 outputs
+          } else {
+            const int tok = tok0 + lane;  // fp32 sums, thread = token
+            if (tok >= p.n_tokens) continue;
+#pragma unroll
+            for (int g8 = 0; g8 < 8; ++g8) {
+              const int o = w.o0 + c + 8 * g8;
+              if (o >= p.n_out) break;
+              float4* d = reinterpret_cast<float4*>(p.part + static_cast<int64_t>(tok) * p.n_out + o);
               d[0] = make_float4(v[8 * g8], v[8 * g8 + 1], v[8 * g8 + 2], v[8 * g8 + 3]);
               d[1] = make_float4(v[8 * g8 + 4], v[8 * g8 + 5], v[8 * g8 + 6], v[8 * g8 + 7]);
             }
@@ -424,7 +445,7 @@ LinearPlan plan_tc(int32_t n_tokens, int32_t n_out, int32_t n_in) {
     const int stage = kABytes + kTmOut * 128;
     p.stages = kRingBudget / stage;
     if (p.stages > kMaxStages) p.stages = kMaxStages;
-    p.smem = 1024 + static_cast<size_t>(p.stages) * stage + sizeof(LinearCtl);
+    p.smem = 1024 + static_cast<size_t>(p.stages) * stage + kEpiStageBytes + sizeof(LinearCtl);
     p.acc_cols = kTmOut;
     p.splits = 1;
     const int64_t units = static_cast<int64_t>(p.tok_tiles) * ((n_out + kTmOut - 1) / kTmOut);

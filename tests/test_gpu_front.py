@@ -51,6 +51,11 @@ LINEAR_CASES = [
     ("bf16", 640, 264, 192),
     ("bf16", 1000, 512, 512),
     ("bf16", 600, 100, 64),
+    # tokens as M over more units than CTAs: a ragged last token tile, a ragged
+    # last tile of W rows, and a K of ten chunks
+    ("bf16", 4100, 2048, 512),
+    ("bf16", 3000, 2056, 384),
+    ("bf16", 700, 512, 640),
     ("bf16", 7, 96, 100),
     ("f32", 3, 70, 96),
 ]
