@@ -201,6 +201,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
 }
 
 constexpr int kFewSplits = 4;
+constexpr int kCombineWarps = 16;  // heads per CTA of the split merge
 
 // The merged row of (query bj, head h): this lane's 16 columns of u = acc / sum,
 // and lse = mx + log(sum) (lane 0).
@@ -231,58 +232,69 @@ __device__ __forceinline__ void combine_store(const DecodeArgs& a, int bj, int h
 // e^(lse_s - lse*), lse = lse* + log sum_s e^(lse_s - lse*). One warp per
 // (query, head): the lanes reduce the split log-sum-exps with shuffles, then
 // each lane merges 16 consecutive columns of the 512 with 16-byte loads.
-template <typename T>
-__global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
+// kCombineWarps heads per CTA: few CTAs, so that the whole grid is resident
+// (and has let the next kernel launch) within a fraction of a microsecond.
+//
+// Few splits (kS = S <= kFewSplits, the common case): every split's
+// log-sum-exp and partial columns are requested at once, so the merge costs
+// one memory round trip; with kS a compile-time count the registers hold just
+// those splits, and two CTAs fit an SM at kS = 2 (one wave of CTAs for the
+// DeepSeek-V3-shaped batch). A split whose lse is -inf is selected out, never
+// multiplied (its partial may hold anything).
+template <typename T, int kS>
+__global__ void __launch_bounds__(32 * kCombineWarps, kS <= 2 ? 2 : 1) combine_few_kernel(DecodeArgs a) {
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x * 4 + warp, bj = blockIdx.y;
+  const int h = blockIdx.x * kCombineWarps + warp, bj = blockIdx.y;
   if (h >= a.heads) return;
+  const uint64_t pol = l2_evict_first_policy();  // the partials are read once
+  const float* lse_s = a.part_lse + static_cast<int64_t>(bj) * kS * a.heads + h;  // stride a.heads
+  float ls[kS];
+  float4 x[kS][4];
+#pragma unroll
+  for (int s = 0; s < kS; ++s) {
+    ls[s] = lse_s[static_cast<int64_t>(s) * a.heads];
+    const float4* src = reinterpret_cast<const float4*>(
+        a.part_u + ((static_cast<int64_t>(bj) * kS + s) * a.heads + h) * kDC + lane * 16);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) x[s][v] = ld_global_v4_hint(src + v, pol);
+  }
+  float mx = ls[0];
+#pragma unroll
+  for (int s = 1; s < kS; ++s) mx = fmaxf(mx, ls[s]);
+  const bool none = (mx == -CUDART_INF_F);
+  float sum = 0.0f;
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < kS; ++s) {
+    const bool use = !none && ls[s] != -CUDART_INF_F;
+    const float wv = use ? fast_exp2((ls[s] - mx) * kLog2e) : 0.0f;
+    sum += wv;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      acc[4 * v] = use ? fmaf(wv, x[s][v].x, acc[4 * v]) : acc[4 * v];
+      acc[4 * v + 1] = use ? fmaf(wv, x[s][v].y, acc[4 * v + 1]) : acc[4 * v + 1];
+      acc[4 * v + 2] = use ? fmaf(wv, x[s][v].z, acc[4 * v + 2]) : acc[4 * v + 2];
+      acc[4 * v + 3] = use ? fmaf(wv, x[s][v].w, acc[4 * v + 3]) : acc[4 * v + 3];
+    }
+  }
+  combine_store<T>(a, bj, h, lane, acc, none, mx, sum);
+}
+
+// More splits (kFewSplits < S <= kManySplits), the same merge and grid.
+template <typename T>
+__global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x * kCombineWarps + warp, bj = blockIdx.y;
+  if (h >= a.heads) return;
+  const uint64_t pol = l2_evict_first_policy();  // the partials are read once
   const int S = a.num_splits;
   const float* lse_s = a.part_lse + static_cast<int64_t>(bj) * S * a.heads + h;  // stride a.heads
-  if (S <= kFewSplits) {
-    // Few splits (the common case): every split's log-sum-exp and partial
-    // columns are requested at once, so the merge costs one memory round trip.
-    // A split whose lse is -inf is selected out, never multiplied (its partial
-    // may hold anything).
-    float ls[kFewSplits];
-    float4 x[kFewSplits][4];
-#pragma unroll
-    for (int s = 0; s < kFewSplits; ++s) {
-      if (s < S) {
-        ls[s] = lse_s[static_cast<int64_t>(s) * a.heads];
-        const float4* src = reinterpret_cast<const float4*>(
-            a.part_u + ((static_cast<int64_t>(bj) * S + s) * a.heads + h) * kDC + lane * 16);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) x[s][v] = src[v];
-      } else {
-        ls[s] = -CUDART_INF_F;
-      }
-    }
-    float mx = ls[0];
-#pragma unroll
-    for (int s = 1; s < kFewSplits; ++s) mx = fmaxf(mx, ls[s]);
-    const bool none = (mx == -CUDART_INF_F);
-    float sum = 0.0f;
-    float acc[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
-#pragma unroll
-    for (int s = 0; s < kFewSplits; ++s) {
-      const bool use = !none && ls[s] != -CUDART_INF_F;
-      const float wv = use ? fast_exp2((ls[s] - mx) * kLog2e) : 0.0f;
-      sum += wv;
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        acc[4 * v] = use ? fmaf(wv, x[s][v].x, acc[4 * v]) : acc[4 * v];
-        acc[4 * v + 1] = use ? fmaf(wv, x[s][v].y, acc[4 * v + 1]) : acc[4 * v + 1];
-        acc[4 * v + 2] = use ? fmaf(wv, x[s][v].z, acc[4 * v + 2]) : acc[4 * v + 2];
-        acc[4 * v + 3] = use ? fmaf(wv, x[s][v].w, acc[4 * v + 3]) : acc[4 * v + 3];
-      }
-    }
-    combine_store<T>(a, bj, h, lane, acc, none, mx, sum);
-    return;
-  }
   // Many splits: the maximum log-sum-exp first (lane s holds split s's for
   // S <= 32), then the splits in groups of kFewSplits whose partial columns are
   // all requested at once: 1 + ceil(S / kFewSplits) memory round trips.
@@ -306,7 +318,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
         const float4* src = reinterpret_cast<const float4*>(
             a.part_u + ((static_cast<int64_t>(bj) * S + s) * a.heads + h) * kDC + lane * 16);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) x[u][v] = src[v];
+        for (int v = 0; v < 4; ++v) x[u][v] = ld_global_v4_hint(src + v, pol);
       } else {
         ls[u] = -CUDART_INF_F;
       }
@@ -346,6 +358,7 @@ __global__ void __launch_bounds__(256) combine_many_kernel(DecodeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, bj = blockIdx.y;
   const int S = a.num_splits;
+  const uint64_t pol = l2_evict_first_policy();  // the partials are read once
   const float* lse_s = a.part_lse + static_cast<int64_t>(bj) * S * a.heads + h;  // stride a.heads
   float mx = -CUDART_INF_F;
   for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lse_s[static_cast<int64_t>(s) * a.heads]);
@@ -366,7 +379,7 @@ __global__ void __launch_bounds__(256) combine_many_kernel(DecodeArgs a) {
         const float4* src = reinterpret_cast<const float4*>(
             a.part_u + ((static_cast<int64_t>(bj) * S + s) * a.heads + h) * kDC + lane * 16);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) x[u][v] = src[v];
+        for (int v = 0; v < 4; ++v) x[u][v] = ld_global_v4_hint(src + v, pol);
       } else {
         ls[u] = -CUDART_INF_F;
       }
@@ -454,9 +467,22 @@ cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
     if (a.act == MLA_F32) return launch_pdl(combine_many_kernel<float>, grid, dim3(256), 0, s, a);
     return launch_pdl(combine_many_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, a);
   }
-  const dim3 grid((a.heads + 3) / 4, a.batch * a.q_len);
-  if (a.act == MLA_F32) return launch_pdl(combine_kernel<float>, grid, dim3(128), 0, s, a);
-  return launch_pdl(combine_kernel<__nv_bfloat16>, grid, dim3(128), 0, s, a);
+  const dim3 grid((a.heads + kCombineWarps - 1) / kCombineWarps, a.batch * a.q_len), block(32 * kCombineWarps);
+  static_assert(kFewSplits == 4, "few-split instances for 2..4 splits");
+  if (a.act == MLA_F32) {
+    switch (a.num_splits) {
+      case 2: return launch_pdl(combine_few_kernel<float, 2>, grid, block, 0, s, a);
+      case 3: return launch_pdl(combine_few_kernel<float, 3>, grid, block, 0, s, a);
+      case 4: return launch_pdl(combine_few_kernel<float, 4>, grid, block, 0, s, a);
+      default: return launch_pdl(combine_kernel<float>, grid, block, 0, s, a);
+    }
+  }
+  switch (a.num_splits) {
+    case 2: return launch_pdl(combine_few_kernel<__nv_bfloat16, 2>, grid, block, 0, s, a);
+    case 3: return launch_pdl(combine_few_kernel<__nv_bfloat16, 3>, grid, block, 0, s, a);
+    case 4: return launch_pdl(combine_few_kernel<__nv_bfloat16, 4>, grid, block, 0, s, a);
+    default: return launch_pdl(combine_kernel<__nv_bfloat16>, grid, block, 0, s, a);
+  }
 }
 
 }  // namespace mla

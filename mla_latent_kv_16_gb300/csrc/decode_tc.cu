@@ -941,10 +941,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
         __syncwarp();
         const int64_t prow0 = (static_cast<int64_t>(bj) * S + split) * 128 + head0;
         uint8_t* pu = reinterpret_cast<uint8_t*>(a.part_u + prow0 * kDC + c_out);
+        // kept in L2 for the split merge that reads them next (the page stream is evict-first)
+        const uint64_t pol = l2_evict_last_policy();
 #pragma unroll 4
         for (int row = 0; row < 32; ++row)
-          *reinterpret_cast<uint4*>(pu + static_cast<size_t>(row) * kDC * 4 + lane * 16) =
-              *reinterpret_cast<const uint4*>(stage + row * 512 + ((lane ^ row) << 4));
+          st_global_v4_hint(pu + static_cast<size_t>(row) * kDC * 4 + lane * 16,
+                            *reinterpret_cast<const uint4*>(stage + row * 512 + ((lane ^ row) << 4)), pol);
       }
     }
   }
