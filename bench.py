@@ -3,8 +3,9 @@
 workload (batch 32, q_len 1, 128 heads, d_c 512 + d_R 64, 4096 cached tokens per
 sequence, bf16 paged cache, page size 64, shuffled pages) through the C ABI.
 
-A step = append of the step's new tokens + absorb_q + paged decode (+ split
-combine) + out_proj. The latent cache (151 MB) is larger than L2, and L2 is
+A step = append of the step's new tokens + absorb_q + paged decode + out_proj
+(mla_decode_out_proj: with 2-4 KV splits the split merge runs inside the
+projection kernel). The latent cache (151 MB) is larger than L2, and L2 is
 additionally flushed before every timed step, outside the per-step CUDA-event
 window, by reading a 256 MiB buffer.
 
@@ -474,7 +475,7 @@ def run_ours(args):
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
-    # one decode step = append + absorb + decode (+ combine) + out_proj, replayed
+    # one decode step = append + absorb + decode + out_proj (split merge inside it), replayed
     # as a CUDA graph so that host launch overhead stays out of the step
     def one_step():
         layer.step(**s)
@@ -562,7 +563,7 @@ def run_ours(args):
                               "decode_tc.cu" if (w.heads == 128 and w.act_dtype == "bf16") else "decode_simt.cu")
     traffic = recorded_traffic(kernel_src, w.name)
     splits = layer.splits
-    launches_per_step = 4 + (1 if splits > 1 else 0)
+    launches_per_step = 4 + capi.merge_kernel_launches(path, splits, with_out_proj=True)
     out = {
         "metric": METRIC, "value": round(gbs, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -577,7 +578,7 @@ def run_ours(args):
         "decode_call_ms": round(dec, 5),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "mla_decode_paged (decode + combine), algorithmic bytes = cache rows + q + u + lse",
+                     "kernel": "mla_decode_paged (decode + split merge), algorithmic bytes = cache rows + q + u + lse",
                      "peak_source": f"hbm_gbs of {src}"},
         "e2e": {"value": round(job_rate(world, cache_bytes, e2e_msps) / 1e9, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_msps, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -744,7 +745,8 @@ def run_layer(args):
         out_launches = 2 if capi.mla_out_proj_fused_workspace_size(n, d_model, H) else 1
     else:  # W_UV per head, then W_O over the concatenated heads (+ its split sum)
         out_launches = 1 + (2 if capi.mla_linear_workspace_size(n, d_model, H * 128) else 1)
-    launches = 4 + 1 + 1 + 1 + (1 if layer.splits > 1 else 0) + out_launches
+    path = capi.mla_decode_kernel_path(layer.cache, layer.scales, w.page_size, w.heads, w.act_dtype, w.cache_dtype)
+    launches = 4 + 1 + 1 + 1 + capi.merge_kernel_launches(path, layer.splits, with_out_proj=not use_fused) + out_launches
     out = {
         "metric": LAYER_METRIC, "value": round(n / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,

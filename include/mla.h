@@ -10,7 +10,8 @@
  *                       u[t,h,:] = sum_j p_j c_KV[j]  (split-KV + log-sum-exp combine)
  *   mla_out_proj      : o[t,h,:]     = W_UV[h] u[t,h,:]                 (512 -> 128)
  *
- * or, with W_UV folded into the output projection W_O once at load time
+ * (mla_decode_out_proj runs the last two as one call, merging the KV splits
+ * inside the projection kernel), or, with W_UV folded into the output projection W_O once at load time
  * (mla_fuse_out_weights), in place of mla_out_proj:
  *
  *   mla_out_proj_fused: y[t,:] = sum_h W~[:,h,:] u[t,h,:]     (H*512 -> d_model)
@@ -230,6 +231,30 @@ mla_status_t mla_decode_paged(const void *q_lat, const void *q_rope, const void 
 mla_status_t mla_decode_kernel_path(const void *cache, const float *scales, int64_t num_pages,
                                     int32_t page_size, mla_dims_t dims, mla_dtype_t act,
                                     mla_dtype_t cache_dtype, int32_t *path_out);
+
+/*
+ * mla_decode_out_proj -- mla_decode_paged followed by mla_out_proj, as one
+ * call: u = the latent attention output, then o[t][h][:] = W_UV[h] u[t][h][:]
+ * ([P1] §3.1-3.2: latent scores and sum, then the value up-projection; [P1]
+ * §4.1: split KV with a log-sum-exp combine). Arguments are mla_decode_paged's
+ * plus
+ *   w_uv  [H][128][512] act (as for mla_out_proj)
+ *   o_out [batch][q_len][H][128] act
+ * u_out and lse_out are written as by mla_decode_paged. When the tensor-core
+ * decode runs with 2 to 4 splits, the split merge happens inside the
+ * projection kernel (one kernel fewer; W_UV is requested before that kernel
+ * waits for the decode), with the same arithmetic as the merge kernel, so u,
+ * lse and o are bit-identical to mla_decode_paged + mla_out_proj. Otherwise the
+ * two calls run as they are. Errors: those of the two calls.
+ */
+mla_status_t mla_decode_out_proj(const void *q_lat, const void *q_rope, const void *cache,
+                                 const float *scales, const int32_t *block_table,
+                                 const int32_t *seq_lens, int32_t batch, int32_t q_len,
+                                 int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size,
+                                 float softmax_scale, int32_t num_splits, void *workspace,
+                                 size_t workspace_bytes, const void *w_uv, void *u_out,
+                                 float *lse_out, void *o_out, int32_t *dev_error, mla_dims_t dims,
+                                 mla_dtype_t act, mla_dtype_t cache_dtype, mla_stream_t stream);
 
 /*
  * mla_decode_paged_static_scratch -- mla_decode_paged without a caller

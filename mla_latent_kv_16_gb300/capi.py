@@ -32,7 +32,7 @@ EXPORTED = ("mla_status_string", "mla_version", "mla_rope_table", "mla_cache_app
             "mla_read_device_error", "mla_decode_paged_static_scratch", "mla_fuse_out_weights",
             "mla_out_proj_fused_workspace_size", "mla_out_proj_fused", "mla_linear_workspace_size", "mla_linear",
             "mla_decode_front_workspace_size", "mla_decode_front", "mla_decode_kernel_path",
-            "mla_prefill_workspace_size", "mla_prefill_mha")
+            "mla_prefill_workspace_size", "mla_prefill_mha", "mla_decode_out_proj")
 
 
 class MlaDims(ctypes.Structure):
@@ -87,6 +87,9 @@ def load(path: Optional[str] = None):
     L.mla_decode_paged.restype = ctypes.c_int
     L.mla_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, f32, i32, vp, sz, vp, vp,
                                    vp, MlaDims, ctypes.c_int, ctypes.c_int, vp]
+    L.mla_decode_out_proj.restype = ctypes.c_int
+    L.mla_decode_out_proj.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, f32, i32, vp, sz, vp, vp,
+                                      vp, vp, vp, MlaDims, ctypes.c_int, ctypes.c_int, vp]
     L.mla_decode_paged_static_scratch.restype = ctypes.c_int
     L.mla_decode_paged_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, f32, i32, vp,
                                                   vp, vp, MlaDims, ctypes.c_int, ctypes.c_int, vp]
@@ -320,6 +323,36 @@ def mla_decode_paged(q_lat, q_rope, cache, scales, block_table, seq_lens, page_s
     return u_out, lse_out
 
 
+def mla_decode_out_proj(q_lat, q_rope, cache, scales, block_table, seq_lens, page_size: int, cache_dtype: str,
+                        w_uv, softmax_scale: Optional[float] = None, num_splits: int = 0, workspace=None,
+                        u_out=None, lse_out=None, o_out=None, dev_error=None, stream=None):
+    """mla_decode_paged then mla_out_proj as one call -> (u [B, Lq, H, 512], lse [B, Lq, H], o [B, Lq, H, 128])."""
+    _contig_cuda(q_lat, q_rope, cache, scales, block_table, seq_lens, w_uv, workspace, u_out, lse_out, o_out,
+                 dev_error)
+    B, Lq, H = q_lat.shape[0], q_lat.shape[1], q_lat.shape[2]
+    maxp = block_table.shape[1]
+    rows = cache.shape[0] * cache.shape[1] if cache.dim() == 3 else cache.shape[0]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(128 + 64)
+    if u_out is None:
+        u_out = torch.empty(B, Lq, H, 512, dtype=q_lat.dtype, device=q_lat.device)
+    if lse_out is None:
+        lse_out = torch.empty(B, Lq, H, dtype=torch.float32, device=q_lat.device)
+    if o_out is None:
+        o_out = torch.empty(B, Lq, H, 128, dtype=q_lat.dtype, device=q_lat.device)
+    need = mla_decode_workspace_size(B, Lq, maxp, page_size, num_splits, H, cache_dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_lat.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().mla_decode_out_proj(_ptr(q_lat), _ptr(q_rope), _ptr(cache), _ptr(scales), _ptr(block_table),
+                                    _ptr(seq_lens), B, Lq, maxp, rows // page_size, page_size, softmax_scale,
+                                    num_splits, _ptr(workspace), ws_bytes, _ptr(w_uv), _ptr(u_out), _ptr(lse_out),
+                                    _ptr(o_out), _ptr(dev_error), dims(H), _act_code(q_lat), DTYPE_CODE[cache_dtype],
+                                    _stream(stream))
+    _check("mla_decode_out_proj", st)
+    return u_out, lse_out, o_out
+
+
 def mla_decode_paged_static_scratch(q_lat, q_rope, cache, scales, block_table, seq_lens, page_size: int,
                                     cache_dtype: str, softmax_scale: Optional[float] = None, num_splits: int = 0,
                                     u_out=None, lse_out=None, dev_error=None, stream=None):
@@ -366,6 +399,15 @@ def mla_prefill_mha(q_nope, q_rope, rows, w_uk, w_uv, softmax_scale: Optional[fl
                                 dims(H), _act_code(q_nope), _stream(stream))
     _check("mla_prefill_mha", st)
     return o_out, lse_out
+
+
+def merge_kernel_launches(path: int, splits: int, with_out_proj: bool) -> int:
+    """Split-merge kernel launches of a decode call: none for one split, none
+    when mla_decode_out_proj merges 2..4 splits of the tensor-core decode inside
+    its projection kernel, else one."""
+    if splits <= 1 or (with_out_proj and path == MLA_DECODE_PATH_TENSOR_CORE and splits <= 4):
+        return 0
+    return 1
 
 
 def mla_decode_kernel_path(cache, scales, page_size: int, heads: int, act: str, cache_dtype: str) -> int:

@@ -141,7 +141,7 @@ mla_status_t decode_prepare(const void* q_lat, const void* q_rope, const void* c
   return MLA_OK;
 }
 
-mla_status_t decode_run(DecodeArgs& a, void* workspace, cudaStream_t s) {
+mla_status_t decode_run(DecodeArgs& a, void* workspace, cudaStream_t s, bool merge) {
   const size_t rows = static_cast<size_t>(a.batch) * a.q_len * a.num_splits * a.heads;
   a.part_u = workspace != nullptr ? static_cast<float*>(workspace) : nullptr;
   a.part_lse = workspace != nullptr
@@ -153,6 +153,7 @@ mla_status_t decode_run(DecodeArgs& a, void* workspace, cudaStream_t s) {
   else
     e = launch_decode_simt(a, s);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
+  if (!merge) return MLA_OK;
   return from_cuda(launch_combine(a, s));
 }
 
@@ -354,6 +355,35 @@ mla_status_t mla_decode_paged(const void* q_lat, const void* q_rope, const void*
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MLA_ERR_WORKSPACE_TOO_SMALL;
   if (need > 0 && !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
   return decode_run(a, need > 0 ? workspace : nullptr, static_cast<cudaStream_t>(stream));
+}
+
+mla_status_t mla_decode_out_proj(const void* q_lat, const void* q_rope, const void* cache, const float* scales,
+                                 const int32_t* block_table, const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                                 int32_t max_pages_per_seq, int64_t num_pages, int32_t page_size,
+                                 float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                 const void* w_uv, void* u_out, float* lse_out, void* o_out, int32_t* dev_error,
+                                 mla_dims_t dims, mla_dtype_t act, mla_dtype_t cache_dtype, mla_stream_t stream) {
+  DecodeArgs a{};
+  size_t need = 0;
+  const mla_status_t st = decode_prepare(q_lat, q_rope, cache, scales, block_table, seq_lens, batch, q_len,
+                                         max_pages_per_seq, num_pages, page_size, softmax_scale, num_splits, u_out,
+                                         lse_out, dev_error, dims, act, cache_dtype, &a, &need);
+  if (st != MLA_OK || batch == 0) return st;
+  if (w_uv == nullptr || o_out == nullptr || !aligned16(w_uv) || !aligned16(o_out)) return MLA_ERR_INVALID_ARG;
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int32_t n = batch * q_len;
+  // the split merge inside the projection when the decode runs on the tensor cores with 2..4 splits
+  const bool fused = a.num_splits >= 2 && use_tc_decode(a.heads, a.page_size, a.act, a.cache_dtype) &&
+                     decode_tc_supported(a) && out_proj_merge_supported(a.heads, a.num_splits, act);
+  const mla_status_t sd = decode_run(a, need > 0 ? workspace : nullptr, s, !fused);
+  if (sd != MLA_OK) return sd;
+  if (fused) {
+    const MergeProjArgs m{a.part_u, a.part_lse, a.num_splits, w_uv, u_out, lse_out, o_out, n, a.heads};
+    return from_cuda(launch_out_proj_merge_tc(m, s));
+  }
+  return mla_out_proj(u_out, w_uv, o_out, n, dims, act, stream);
 }
 
 mla_status_t mla_decode_kernel_path(const void* cache, const float* scales, int64_t num_pages, int32_t page_size,

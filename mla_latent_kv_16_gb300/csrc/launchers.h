@@ -66,6 +66,23 @@ cudaError_t launch_out_proj_simt(const ProjArgs& a, cudaStream_t s);
 cudaError_t launch_absorb_tc(const ProjArgs& a, cudaStream_t s);
 cudaError_t launch_out_proj_tc(const ProjArgs& a, cudaStream_t s);
 
+// The split merge of a decode and the value up-projection in one kernel
+// (proj_tc.cu): u[t,h,:] merged from the decode's fp32 split partials, then
+// o[t,h,:] = W_UV[h] u[t,h,:]. bf16, 128 heads, 2..4 splits.
+struct MergeProjArgs {
+  const float* part_u;    // [n][S][H][512] fp32, as the decode wrote them
+  const float* part_lse;  // [n][S][H]
+  int32_t num_splits;
+  const void* w;          // W_UV [H][128][512] bf16
+  void* u_out;            // [n][H][512] bf16: the merged latent output
+  float* lse_out;         // [n][H] or nullptr
+  void* o;                // [n][H][128] bf16
+  int32_t n_tokens;       // n = batch * q_len
+  int32_t heads;
+};
+bool out_proj_merge_supported(int32_t heads, int32_t splits, mla_dtype_t act);
+cudaError_t launch_out_proj_merge_tc(const MergeProjArgs& a, cudaStream_t s);
+
 struct FuseWeightsArgs {
   const void* w_o;   // [d][H][128]
   const void* w_uv;  // [H][128][512]
@@ -187,8 +204,9 @@ mla_status_t decode_prepare(const void* q_lat, const void* q_rope, const void* c
                             mla_dtype_t act, mla_dtype_t cache_dtype, DecodeArgs* out, size_t* workspace_need);
 // Sets the workspace pointers (workspace: at least the size decode_prepare
 // reported, 16-byte aligned; may be null when that size is 0) and launches the
-// decode and combine kernels.
-mla_status_t decode_run(DecodeArgs& a, void* workspace, cudaStream_t s);
+// decode kernel, then (merge) the split merge kernel; without merge the split
+// partials are left in the workspace for a caller that merges them itself.
+mla_status_t decode_run(DecodeArgs& a, void* workspace, cudaStream_t s, bool merge = true);
 
 int device_sm_count();
 

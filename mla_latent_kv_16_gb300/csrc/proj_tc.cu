@@ -18,6 +18,7 @@
 // bound by the weight stream from HBM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <math_constants.h>
 
 #include "common.cuh"
 #include "launchers.h"
@@ -186,6 +187,184 @@ __global__ void __launch_bounds__(kThreads) proj_tc_kernel(const __grid_constant
   }
 }
 
+// ------------------------------------------------------------------ merge + out_proj
+//
+// The step's tail in one kernel: the decode leaves S fp32 partial rows and
+// log-sum-exps per (token, head); here each CTA (head h, up to kMpTok tokens)
+// merges them ("Model Architecture Driving Inference Systems" §4.1, split KV
+// with a log-sum-exp combine, the split merge kernel's arithmetic and order),
+// writes u, and stages u in bf16 as the B operand of o^T = W_UV[h] u^T
+// (§3.2). W_UV[h] (128 KB) is requested before the wait for the decode, so its
+// stream from HBM overlaps the decode's tail and the merge. Sixteen warps merge
+// (at two splits, two tokens each in flight per lane: the 32 tokens of a
+// DeepSeek-V3 batch in one round trip); warps 0-3 read the accumulator back.
+constexpr int kMpThreads = 512;
+constexpr int kMpTok = 64;  // tokens per CTA (MMA N)
+
+struct MergeProjCtl {
+  uint64_t a_full;
+  uint64_t done;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+template <int kS>
+__global__ void __launch_bounds__(kMpThreads) out_proj_merge_kernel(const __grid_constant__ CUtensorMap amap,
+                                                                   MergeProjArgs p, int n_tile, uint32_t tmem_cols) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int kChunks = kDC / kChunkK;  // 8 K chunks of 64 latent columns
+  uint8_t* a_s = base;                              // W_UV[h] chunk k at k * kABytes
+  uint8_t* b_s = base + kChunks * kABytes;          // u chunk k at k * n_tile * 128 (token rows of 128 B)
+  const int b_bytes = n_tile * 128;
+  MergeProjCtl* ctl = reinterpret_cast<MergeProjCtl*>(b_s + kChunks * b_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x;
+  const int t0 = blockIdx.z * kMpTok;
+  const int n_tok = min(kMpTok, p.n_tokens - t0);
+  pdl_trigger();
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&ctl->a_full), 1);
+    mbar_init(smem_u32(&ctl->done), 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init_cluster();
+    prefetch_tmap(&amap);
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&ctl->tmem_base), tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int32_t* abort_flag = &ctl->abort_flag;
+  if (threadIdx.x == 0) {
+    // the weights are static: W_UV[h] rows d in [0, 128), all 512 columns, before the wait
+    mbar_arrive_expect_tx(smem_u32(&ctl->a_full), kChunks * kABytes);
+    for (int k = 0; k < kChunks; ++k)
+      tma_load_2d_nohint(smem_u32(a_s + k * kABytes), &amap, smem_u32(&ctl->a_full), kChunkK * k, h * kDV);
+  }
+  pdl_wait();
+
+  // ---- merge: warp w takes tokens w, w + 16, ... of the tile, kQ at a time;
+  // lane = latent columns [16 lane, 16 lane + 16), i.e. K chunk lane / 4,
+  // 16-byte chunks 2 (lane mod 4) and 2 (lane mod 4) + 1 of its 128-byte rows
+  const uint64_t pol = l2_evict_first_policy();  // the partials are read once
+  const int kc = lane >> 2, j0 = 2 * (lane & 3);
+  constexpr int kQ = kS <= 2 ? 2 : 1;  // tokens in flight per lane (registers)
+  for (int tp = warp; tp < n_tile; tp += kQ * (kMpThreads / 32)) {
+    float ls[kQ][kS];
+    float4 x[kQ][kS][4];
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const int t = tp + q * (kMpThreads / 32);
+      if (t < n_tok) {
+        const int64_t bj = t0 + t;
+#pragma unroll
+        for (int s = 0; s < kS; ++s) {
+          const int64_t row = (bj * kS + s) * p.heads + h;
+          ls[q][s] = p.part_lse[row];
+          const float4* src = reinterpret_cast<const float4*>(p.part_u + row * kDC + lane * 16);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) x[q][s][v] = ld_global_v4_hint(src + v, pol);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const int t = tp + q * (kMpThreads / 32);
+      if (t >= n_tile) continue;
+      uint32_t w[8];
+      if (t < n_tok) {
+        float mx = ls[q][0];
+#pragma unroll
+        for (int s = 1; s < kS; ++s) mx = fmaxf(mx, ls[q][s]);
+        const bool none = (mx == -CUDART_INF_F);
+        float sum = 0.0f;
+        float acc[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+#pragma unroll
+        for (int s = 0; s < kS; ++s) {
+          const bool use = !none && ls[q][s] != -CUDART_INF_F;  // a -inf split is selected out, never multiplied
+          const float wv = use ? fast_exp2((ls[q][s] - mx) * kLog2e) : 0.0f;
+          sum += wv;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            acc[4 * v] = use ? fmaf(wv, x[q][s][v].x, acc[4 * v]) : acc[4 * v];
+            acc[4 * v + 1] = use ? fmaf(wv, x[q][s][v].y, acc[4 * v + 1]) : acc[4 * v + 1];
+            acc[4 * v + 2] = use ? fmaf(wv, x[q][s][v].z, acc[4 * v + 2]) : acc[4 * v + 2];
+            acc[4 * v + 3] = use ? fmaf(wv, x[q][s][v].w, acc[4 * v + 3]) : acc[4 * v + 3];
+          }
+        }
+        const float inv = none ? 0.0f : 1.0f / sum;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = pack_bf16x2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+        const int64_t orow = static_cast<int64_t>(t0 + t) * p.heads + h;
+        uint4* ud = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.u_out) + orow * kDC + lane * 16);
+        ud[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        ud[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        if (lane == 0 && p.lse_out != nullptr) p.lse_out[orow] = none ? -CUDART_INF_F : mx + logf(sum);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = 0u;  // token rows past n: zero (their outputs are not written)
+      }
+      // the same bf16 values as the B operand, 128-byte swizzled token rows
+      uint8_t* brow = b_s + kc * b_bytes + t * 128;
+      *reinterpret_cast<uint4*>(brow + ((j0 ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(brow + (((j0 + 1) ^ (t & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
+  fence_proxy_async_smem();  // generic writes of B, before the tensor core reads them
+  __syncthreads();
+
+  if (threadIdx.x == 0) {
+    const uint32_t idesc = idesc_bf16_f32(128, n_tile, false, false);
+    bool ok = mbar_wait<2>(smem_u32(&ctl->a_full), 0, abort_flag, nullptr);
+    if (ok) {
+      tc_fence_after();
+      for (int k = 0; k < kChunks; ++k) {
+        const uint32_t a0 = smem_u32(a_s + k * kABytes);
+        const uint64_t db = sdesc_sw128(smem_u32(b_s + k * b_bytes), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kChunkK / 16; ++kk)
+          mma_ss(tmem, sdesc_sw128(a0 + kk * 32, 16, 1024), db + ((kk * 32) >> 4), idesc, (k > 0 || kk > 0) ? 1u : 0u);
+      }
+    } else {
+      // let W_UV's copies land before the CTA exits
+      volatile int32_t never = 0;
+      mbar_wait<2>(smem_u32(&ctl->a_full), 0, &never, nullptr);
+    }
+    mma_commit(smem_u32(&ctl->done));
+  }
+  __syncwarp();
+  // epilogue (warps 0-3): thread = output feature d (TMEM lane), columns = tokens
+  if (warp < 4) {
+    volatile int32_t never = 0;
+    const bool ok =
+        __all_sync(0xffffffffu, mbar_wait<0>(smem_u32(&ctl->done), 0, &never, nullptr)) && *abort_flag == 0;
+    tc_fence_after();
+    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+    const int feat = warp * 32 + lane;
+    __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.o);
+    for (int c = 0; c < n_tile; c += 32) {
+      float v[32];
+      tmem_ld32_sync(tmem + lanes + c, v);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int t = c + k;
+        if (t < n_tok)  // an aborted call writes NaN, never stale values
+          y[(static_cast<int64_t>(t0 + t) * p.heads + h) * kDV + feat] = __float2bfloat16_rn(ok ? v[k] : CUDART_NAN_F);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static bool tried = false;
@@ -262,5 +441,37 @@ cudaError_t launch_proj(const ProjArgs& a, cudaStream_t s) {
 
 cudaError_t launch_absorb_tc(const ProjArgs& a, cudaStream_t s) { return launch_proj<0>(a, s); }
 cudaError_t launch_out_proj_tc(const ProjArgs& a, cudaStream_t s) { return launch_proj<1>(a, s); }
+
+bool out_proj_merge_supported(int32_t heads, int32_t splits, mla_dtype_t act) {
+  return act == MLA_BF16 && heads >= 1 && splits >= 2 && splits <= 4 && encoder() != nullptr;
+}
+
+cudaError_t launch_out_proj_merge_tc(const MergeProjArgs& a, cudaStream_t s) {
+  if (!out_proj_merge_supported(a.heads, a.num_splits, MLA_BF16)) return cudaErrorNotSupported;
+  if (a.n_tokens == 0) return cudaSuccess;
+  const int n_tile = a.n_tokens >= kMpTok ? kMpTok : ((a.n_tokens + 15) / 16) * 16;
+  uint32_t cols = 32;
+  while (static_cast<int>(cols) < n_tile) cols <<= 1;
+  const size_t smem = 1024 + static_cast<size_t>(kDC / kChunkK) * (kABytes + n_tile * 128) + sizeof(MergeProjCtl);
+  CUtensorMap am;
+  if (!encode_2d(&am, a.w, static_cast<uint64_t>(a.heads) * kDV, kDC, 128)) return cudaErrorInvalidValue;
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (attr_dev != dev) {
+    for (auto fn : {out_proj_merge_kernel<2>, out_proj_merge_kernel<3>, out_proj_merge_kernel<4>}) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (e != cudaSuccess) return e;
+    }
+    attr_dev = dev;
+  }
+  const dim3 grid(a.heads, 1, (a.n_tokens + kMpTok - 1) / kMpTok);
+  switch (a.num_splits) {
+    case 2: return launch_pdl(out_proj_merge_kernel<2>, grid, dim3(kMpThreads), smem, s, am, a, n_tile, cols);
+    case 3: return launch_pdl(out_proj_merge_kernel<3>, grid, dim3(kMpThreads), smem, s, am, a, n_tile, cols);
+    default: return launch_pdl(out_proj_merge_kernel<4>, grid, dim3(kMpThreads), smem, s, am, a, n_tile, cols);
+  }
+}
 
 }  // namespace mla

@@ -5,10 +5,10 @@ W_UK, W_UV, the paged latent cache (and E4M3 scales), the RoPE tables, the
 block table / sequence lengths, and reusable workspace and output buffers. A
 decode step is
 
-    append(new tokens) -> absorb_q -> decode_paged (+ combine) -> out_proj
+    append(new tokens) -> absorb_q -> decode_out_proj (decode_paged + out_proj)
 
-exactly the four calls of the library, on one stream, with no allocation in
-the step once the buffers exist.
+on one stream, with no allocation in the step once the buffers exist; with
+2 to 4 KV splits the split merge runs inside the projection kernel.
 
 With the model-level weights attached (attach_front, attach_output), a step can
 start from the hidden states of the new tokens and end in the model dimension:
@@ -98,13 +98,20 @@ class MLADecodeLayer:
     def out_proj(self, u, stream=None):
         return capi.mla_out_proj(u, self.w_uv, self.o, stream)
 
+    def decode_out_proj(self, q_lat, q_rope, stream=None):
+        """decode then out_proj as one call (the KV splits merged inside the
+        projection kernel where the library can); fills u, lse and o."""
+        capi.mla_decode_out_proj(q_lat, q_rope, self.cache, self.scales, self.block_table, self.seq_lens, self.P,
+                                 self.cache_dtype, self.w_uv, self.softmax_scale, self.num_splits, self.workspace,
+                                 self.u, self.lse, self.o, self.dev_error, stream)
+        return self.o
+
     def step(self, q_nope, q_rope, new_c_kv, new_k_r, new_positions, new_slots, stream=None):
         """One decode step: append the q_len new tokens, then attend. Returns o."""
         if new_c_kv is not None and new_c_kv.shape[0] > 0:
             self.append(new_c_kv, new_k_r, new_positions, new_slots, stream)
         q_lat = self.absorb(q_nope, stream)
-        u, _ = self.decode(q_lat, q_rope, stream)
-        return self.out_proj(u, stream)
+        return self.decode_out_proj(q_lat, q_rope, stream)
 
     # ------------------------------------------------------------------ model-level weights
 
@@ -171,8 +178,13 @@ class MLADecodeLayer:
         q_nope, q_rope, c_kv, k_r = self.front(h, positions, stream)
         self.append(c_kv, k_r, positions, slots, stream)
         q_lat = self.absorb(q_nope.view(B, Lq, self.H, 128), stream)
-        u, _ = self.decode(q_lat, q_rope.view(B, Lq, self.H, 64), stream)
-        return self.output(u, stream)
+        if self.out_fused:
+            u, _ = self.decode(q_lat, q_rope.view(B, Lq, self.H, 64), stream)
+            return self.output(u, stream)
+        # W_UV per head (with the KV split merge inside its kernel), then W_O
+        o = self.decode_out_proj(q_lat, q_rope.view(B, Lq, self.H, 64), stream)
+        capi.mla_linear(o.view(-1, self.H * 128), self.w_out, self.y.view(-1, self.y.shape[-1]), self.out_ws, stream)
+        return self.y
 
     def device_error(self) -> int:
         return capi.mla_read_device_error(self.dev_error)
