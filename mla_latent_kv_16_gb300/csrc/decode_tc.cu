@@ -159,7 +159,8 @@ __device__ void write_empty(const DecodeArgs& a, int64_t row0, int bj, int split
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
-                     const __grid_constant__ CUtensorMap rmap, const DecodeArgs a) {
+                     const __grid_constant__ CUtensorMap rmap, const __grid_constant__ CUtensorMap pmap,
+                     const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem* sm = reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -927,26 +928,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1
               *reinterpret_cast<const uint4*>(stage + row * 256 + ((ch ^ (row & 15)) << 4));
         }
       } else {
+        // fp32 partial rows of this split: four boxes of 32 rows x 32 columns
+        // (128-byte rows, 16-byte chunk v of row r at v ^ (r mod 8)), stored by
+        // TMA; the CTA goes on while they drain, and they stay in L2 (evict-last)
+        // for the split merge that reads them next
         uint8_t* stage = sm->kv[0] + wl * (32 * 512);
         for (int c = 0; c < 4; ++c) {
           float o[32];
           tmem_ld32_sync(tO + c * 32u, o);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const int cc = c * 8 + v;
-            *reinterpret_cast<float4*>(stage + lane * 512 + ((cc ^ lane) << 4)) =
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<float4*>(stage + c * 4096 + lane * 128 + ((v ^ (lane & 7)) << 4)) =
                 make_float4(o[4 * v] * inv_l, o[4 * v + 1] * inv_l, o[4 * v + 2] * inv_l, o[4 * v + 3] * inv_l);
-          }
         }
+        fence_proxy_async_smem();
         __syncwarp();
-        const int64_t prow0 = (static_cast<int64_t>(bj) * S + split) * 128 + head0;
-        uint8_t* pu = reinterpret_cast<uint8_t*>(a.part_u + prow0 * kDC + c_out);
-        // kept in L2 for the split merge that reads them next (the page stream is evict-first)
-        const uint64_t pol = l2_evict_last_policy();
-#pragma unroll 4
-        for (int row = 0; row < 32; ++row)
-          st_global_v4_hint(pu + static_cast<size_t>(row) * kDC * 4 + lane * 16,
-                            *reinterpret_cast<const uint4*>(stage + row * 512 + ((lane ^ row) << 4)), pol);
+        if (lane == 0) {
+          const int32_t prow0 = static_cast<int32_t>((static_cast<int64_t>(bj) * S + split) * 128 + head0);
+          const uint64_t pol = l2_evict_last_policy();
+          for (int c = 0; c < 4; ++c)
+            tma_store_2d(&pmap, smem_u32(stage + c * 4096), static_cast<int32_t>(c_out) + 32 * c, prow0, pol);
+          bulk_commit_group();
+          bulk_wait_group_read0();  // the staging area has been read before the CTA tears down
+        }
       }
     }
   }
@@ -1004,24 +1008,30 @@ struct MapCache {
     uint64_t rows = 0;
     uint32_t cols = 0, box_rows = 0;
     bool bytes = false;
+    bool f32 = false;
     CUtensorMap map;
   } e[kSlots];
   int next = 0;
   // bf16 elements, 64 x box_rows boxes, 128-byte swizzle; or (bytes) uint8
-  // elements, 64-byte x box_rows boxes, no swizzle
-  bool get(const void* ptr, uint64_t rows, uint32_t cols, uint32_t box_rows, CUtensorMap* out, bool bytes = false) {
+  // elements, 64-byte x box_rows boxes, no swizzle; or (f32) fp32 elements,
+  // 32 x box_rows boxes, 128-byte swizzle
+  bool get(const void* ptr, uint64_t rows, uint32_t cols, uint32_t box_rows, CUtensorMap* out, bool bytes = false,
+           bool f32 = false) {
     for (auto& x : e)
-      if (x.ptr == ptr && x.rows == rows && x.cols == cols && x.box_rows == box_rows && x.bytes == bytes) {
+      if (x.ptr == ptr && x.rows == rows && x.cols == cols && x.box_rows == box_rows && x.bytes == bytes &&
+          x.f32 == f32) {
         *out = x.map;
         return true;
       }
     Entry& n = e[next];
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * (bytes ? 1 : 2)};
-    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * (bytes ? 1 : (f32 ? 4 : 2))};
+    const cuuint32_t box[2] = {f32 ? 32u : 64u, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    if (tensor_map_encoder()(&n.map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const CUtensorMapDataType dt =
+        bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : (f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    if (tensor_map_encoder()(&n.map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE,
                              bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
       n.ptr = nullptr;
@@ -1032,6 +1042,7 @@ struct MapCache {
     n.cols = cols;
     n.box_rows = box_rows;
     n.bytes = bytes;
+    n.f32 = f32;
     next = (next + 1) % kSlots;
     *out = n.map;
     return true;
@@ -1053,17 +1064,26 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
     attr_set_for_device = dev;
   }
   const bool fp8 = a.cache_dtype == MLA_E4M3;
-  CUtensorMap map, qmap, rmap;
+  CUtensorMap map, qmap, rmap, pmap;
   const uint64_t q_rows = static_cast<uint64_t>(a.batch) * a.q_len * 128;
   // cache as [num_pages*page_size rows][576] bf16, 64 x 64 boxes; q_lat as
   // [batch*q_len*128 rows][512] (128 x 64 boxes) and q_rope as [..][64] (64 x 64 boxes)
   if (!cache.get(a.cache, static_cast<uint64_t>(a.num_pages) * a.page_size, kRow, kTileTok, &map, fp8) ||
       !cache.get(a.q_lat, q_rows, kDC, 128, &qmap) || !cache.get(a.q_rope, q_rows, kDRope, 64, &rmap))
     return cudaErrorInvalidValue;
+  // split partials [batch*q_len*splits*128 rows][512] fp32, stored as 32 x 32 boxes (a single split
+  // writes u directly and never uses the map: q_lat's stands in)
+  if (a.num_splits > 1) {
+    if (a.part_u == nullptr || !cache.get(a.part_u, q_rows * a.num_splits, kDC, 32, &pmap, false, true))
+      return cudaErrorInvalidValue;
+  } else {
+    pmap = qmap;
+  }
   const int64_t items = static_cast<int64_t>(a.batch) * a.q_len * a.num_splits;
   const dim3 grid(static_cast<unsigned>(2 * items));
-  if (fp8) return launch_pdl(decode_tc_kernel<true>, grid, dim3(threads_for(true)), kSmemBytes, s, map, qmap, rmap, a);
-  return launch_pdl(decode_tc_kernel<false>, grid, dim3(threads_for(false)), kSmemBytes, s, map, qmap, rmap, a);
+  if (fp8)
+    return launch_pdl(decode_tc_kernel<true>, grid, dim3(threads_for(true)), kSmemBytes, s, map, qmap, rmap, pmap, a);
+  return launch_pdl(decode_tc_kernel<false>, grid, dim3(threads_for(false)), kSmemBytes, s, map, qmap, rmap, pmap, a);
 }
 
 }  // namespace mla

@@ -235,6 +235,23 @@ __device__ __forceinline__ void tma_load_2d_nohint(uint32_t dst, const CUtensorM
       : "memory");
 }
 
+// 2D tiled store of one box from shared memory (bulk-group completion), with
+// an L2 cache policy. The box must be fenced for the async proxy first
+// (fence_proxy_async_smem) and may be reused once bulk_wait_group_read0()
+// returns; the writes reach global memory before the grid completes.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y,
+                                             uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Bring one box of a tensor into L2 ahead of its load (no shared memory used).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
