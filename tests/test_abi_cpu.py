@@ -91,6 +91,30 @@ def test_validation_fails_before_device_work(capi):
                               capi.dims(128), capi.MLA_BF16, capi.MLA_BF16, None) == capi.MLA_ERR_INVALID_ARG
 
 
+def test_decode_out_proj_validation(capi):
+    """mla_decode_out_proj: mla_decode_paged's checks, then a missing or
+    misaligned W_UV / o buffer, all before any device work."""
+    L = capi.load()
+    D = capi.dims(128)
+    args = (16, 16, 16, None, 16, 16, 1, 1, 1, 1, 64, 0.1, 0, None, 0)
+    # decode's own checks come first: an E4M3 cache without scales
+    assert L.mla_decode_out_proj(16, 16, 16, None, 16, 16, 1, 1, 1, 1, 64, 0.1, 0, None, 0, 16, 16, None, 16, None,
+                                 D, capi.MLA_BF16, capi.MLA_E4M3, None) == capi.MLA_ERR_INVALID_ARG
+    # no W_UV, no o, a misaligned o
+    assert L.mla_decode_out_proj(*args, None, 16, None, 16, None, D, capi.MLA_BF16, capi.MLA_BF16, None) == \
+        capi.MLA_ERR_INVALID_ARG
+    assert L.mla_decode_out_proj(*args, 16, 16, None, None, None, D, capi.MLA_BF16, capi.MLA_BF16, None) == \
+        capi.MLA_ERR_INVALID_ARG
+    assert L.mla_decode_out_proj(*args, 16, 16, None, 24, None, D, capi.MLA_BF16, capi.MLA_BF16, None) == \
+        capi.MLA_ERR_INVALID_ARG
+    # workspace too small for an explicit split count
+    assert L.mla_decode_out_proj(16, 16, 16, None, 16, 16, 2, 1, 8, 16, 64, 0.1, 4, None, 0, 16, 16, None, 16, None,
+                                 D, capi.MLA_BF16, capi.MLA_BF16, None) == capi.MLA_ERR_WORKSPACE_TOO_SMALL
+    # an empty batch is a no-op
+    assert L.mla_decode_out_proj(None, None, None, None, None, None, 0, 1, 1, 1, 64, 0.1, 0, None, 0, None, None,
+                                 None, None, None, D, capi.MLA_BF16, capi.MLA_BF16, None) == capi.MLA_OK
+
+
 def test_fused_projection_validation(capi):
     """mla_fuse_out_weights / mla_out_proj_fused reject bad arguments before any
     device work; the workspace size covers one fp32 partial per K split."""
