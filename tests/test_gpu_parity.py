@@ -235,7 +235,7 @@ def test_pages_larger_than_a_tile(cache, page_size, splits):
     _check_latent(w, d, pool, sc, f64(layer.u), layer.lse.cpu().numpy(), f64(layer.q_lat), what=f"page {page_size}")
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
+@pytest.mark.parametrize("splits", [1, 2, 3, 4, 7, 8, 64])
 def test_split_count_invariance(splits):
     w = _W().preset("ragged_bf16", batch=4, seq_lens=[3000, 17, 640, 2049], num_splits=splits)
     d = _W().make_inputs(w)
